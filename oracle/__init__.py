@@ -1,0 +1,163 @@
+"""Scalar fp64 CPU oracle for block-quantized GEMV -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg
+may import this package. The CUDA product path never calls it and shares no
+code with it. The arithmetic lives in ``oracle.cpp`` (plain C++, fp64, built
+without contraction); this module only marshals numpy arrays through ctypes.
+
+Each function states what it computes; the definitions and their sources are in
+the header of ``oracle.cpp`` and ``decode.cpp``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SO = os.path.join(_HERE, "liboracle.so")
+_SOURCES = [os.path.join(_HERE, "oracle.cpp"), os.path.join(_HERE, "decode.cpp")]
+
+Q8_0, Q4_K, AFFINE4 = 1, 2, 3
+F32, BF16 = 1, 2
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so in place with g++ (-O2, OpenMP, no fp contraction)."""
+    srcs = [s for s in _SOURCES if os.path.exists(s)]
+    newest = max(os.path.getmtime(s) for s in srcs)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < newest:
+        cmd = ["g++", "-std=c++17", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+               "-fPIC", "-shared", "-o", _SO + ".tmp"] + srcs
+        subprocess.run(cmd, check=True)
+        os.replace(_SO + ".tmp", _SO)
+    return _SO
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_SO)
+        P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        L.orc_block_bytes.argtypes = [I]
+        L.orc_block_weights.argtypes = [I]
+        L.orc_half_to_double.argtypes = [ctypes.c_uint16]
+        L.orc_half_to_double.restype = ctypes.c_double
+        for f in (L.orc_double_to_half_rn, L.orc_double_to_half_up, L.orc_double_to_half_down):
+            f.argtypes = [ctypes.c_double]
+            f.restype = ctypes.c_uint16
+        L.orc_unpack_scale_min.argtypes = [P, I, P, P]
+        L.orc_quantize.argtypes = [I, P, I64, I64, P, I]
+        L.orc_dequant.argtypes = [I, P, I64, I64, P]
+        L.orc_gemv.argtypes = [I, P, I, P, I64, I64, I64, P, P, I]
+        L.orc_gemv_sampled.argtypes = [I, P, I, P, I64, I64, I64, I64, P, P, P, P, I]
+        if hasattr(L, "orc_decode_step"):
+            L.orc_decode_step.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I64, I64, I64,
+                                          ctypes.c_double, P, P, I]
+            L.orc_rmsnorm.argtypes = [P, P, I64, I64, ctypes.c_double, P]
+            L.orc_swiglu.argtypes = [P, P, I64, P]
+        _lib = L
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def block_bytes(fmt: int) -> int:
+    return lib().orc_block_bytes(fmt)
+
+
+def block_weights(fmt: int) -> int:
+    return lib().orc_block_weights(fmt)
+
+
+def row_bytes(fmt: int, K: int) -> int:
+    return K // block_weights(fmt) * block_bytes(fmt)
+
+
+def half_to_double(h: int) -> float:
+    return lib().orc_half_to_double(h)
+
+
+def double_to_half_rn(v: float) -> int:
+    return lib().orc_double_to_half_rn(v)
+
+
+def double_to_half_up(v: float) -> int:
+    return lib().orc_double_to_half_up(v)
+
+
+def double_to_half_down(v: float) -> int:
+    return lib().orc_double_to_half_down(v)
+
+
+def unpack_scale_min(sc12: bytes, j: int):
+    a = np.frombuffer(bytes(sc12), dtype=np.uint8).copy()
+    sc, m = ctypes.c_int(), ctypes.c_int()
+    lib().orc_unpack_scale_min(_ptr(a), j, ctypes.byref(sc), ctypes.byref(m))
+    return sc.value, m.value
+
+
+def quantize(fmt: int, w: np.ndarray, nthreads: int = 0) -> np.ndarray:
+    """fp32 N x K -> uint8 N x row_bytes blocks (the oracle's own quantizer)."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    N, K = w.shape
+    out = np.empty((N, row_bytes(fmt, K)), dtype=np.uint8)
+    nt = nthreads or os.cpu_count() or 1
+    if lib().orc_quantize(fmt, _ptr(w), N, K, _ptr(out), nt) != 0:
+        raise ValueError("orc_quantize: bad format or K")
+    return out
+
+
+def dequant(fmt: int, blocks: np.ndarray, N: int, K: int) -> np.ndarray:
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+    out = np.empty((N, K), dtype=np.float64)
+    if lib().orc_dequant(fmt, _ptr(blocks), N, K, _ptr(out)) != 0:
+        raise ValueError("orc_dequant: bad format or K")
+    return out
+
+
+def _x_code(x: np.ndarray):
+    if x.dtype == np.float32:
+        return F32
+    if x.dtype == np.uint16:  # bf16 bit patterns
+        return BF16
+    raise TypeError("x must be float32 or uint16 (bf16 bits)")
+
+
+def gemv(fmt: int, blocks: np.ndarray, x: np.ndarray, N: int, K: int, nthreads: int = 0):
+    """Return (y, absy), both M x N fp64: y = x @ deq(W)^T, absy = |x| @ |deq(W)|^T."""
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+    x = np.ascontiguousarray(x)
+    M = x.shape[0]
+    y = np.empty((M, N), dtype=np.float64)
+    ay = np.empty((M, N), dtype=np.float64)
+    nt = nthreads or os.cpu_count() or 1
+    if lib().orc_gemv(fmt, _ptr(blocks), _x_code(x), _ptr(x), M, N, K, _ptr(y), _ptr(ay), nt) != 0:
+        raise ValueError("orc_gemv: bad arguments")
+    return y, ay
+
+
+def gemv_sampled(fmt: int, blocks: np.ndarray, x: np.ndarray, N: int, K: int, js, ns,
+                 nthreads: int = 0):
+    """(y, absy) at the output coordinates (js[p], ns[p]) only."""
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+    x = np.ascontiguousarray(x)
+    M = x.shape[0]
+    js = np.ascontiguousarray(js, dtype=np.int64)
+    ns = np.ascontiguousarray(ns, dtype=np.int64)
+    y = np.empty(len(js), dtype=np.float64)
+    ay = np.empty(len(js), dtype=np.float64)
+    nt = nthreads or os.cpu_count() or 1
+    rc = lib().orc_gemv_sampled(fmt, _ptr(blocks), _x_code(x), _ptr(x), M, N, K, len(js),
+                                _ptr(js), _ptr(ns), _ptr(y), _ptr(ay), nt)
+    if rc != 0:
+        raise ValueError(f"orc_gemv_sampled: bad arguments ({rc})")
+    return y, ay

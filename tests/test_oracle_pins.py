@@ -1,0 +1,254 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+Each test names what fixes the expected value: a hand-derived closed form, an
+independent library routine (numpy's fp16 conversion, numpy matmul, exact
+rational arithmetic), a worked example in tests/golden, or an invariant of the
+quantization scheme (the round-trip bound). No expected value here comes from
+the CUDA path.
+"""
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from conftest import load_golden
+from quantized_decode_gemv_block_gb300 import inputs
+
+Q8_0, Q4_K, AFFINE4 = 1, 2, 3
+
+
+# ------------------------------------------------------------------- fp16 --
+def test_fp16_decode_exhaustive(orc):
+    """All 65536 binary16 codes decode exactly as numpy's float16 -> float64."""
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = codes.view(np.float16).astype(np.float64)
+    got = np.array([orc.half_to_double(int(c)) for c in codes])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    # signed zeros keep their sign
+    assert math.copysign(1.0, orc.half_to_double(0x8000)) == -1.0
+
+
+def test_fp16_round_trip_all_finite_codes(orc):
+    for c in range(65536):
+        if (c & 0x7C00) == 0x7C00 and (c & 0x3FF):
+            continue  # NaN payloads are canonicalised
+        assert orc.double_to_half_rn(orc.half_to_double(c)) == c
+
+
+def test_fp16_rn_matches_numpy(orc):
+    """Correct rounding from binary64, ties to even, checked against numpy's converter."""
+    rng = np.random.default_rng(7)
+    vals = list(rng.standard_normal(20000) * np.exp2(rng.uniform(-30, 17, 20000)))
+    # exact midpoints between neighbouring fp16 values (ties) and points just off them
+    for c in list(range(0, 0x7BFF, 97)) + [0, 1, 2, 0x3FF, 0x400, 0x401, 0x7BFE]:
+        a, b = orc.half_to_double(c), orc.half_to_double(c + 1)
+        mid = (a + b) / 2
+        vals += [mid, np.nextafter(mid, 0), np.nextafter(mid, np.inf), -mid]
+    vals += [65504.0, 65519.99, 65520.0, 65536.0, 1e300, -1e300, 2.0 ** -25, 2.0 ** -25 * 1.0000001,
+             3 * 2.0 ** -26, 2.0 ** -26, 0.0, -0.0, float("inf"), float("-inf")]
+    for v in vals:
+        ref = int(np.array([v], dtype=np.float64).astype(np.float16).view(np.uint16)[0])
+        assert orc.double_to_half_rn(float(v)) == ref, v
+
+
+def test_fp16_directed_rounding(orc):
+    rng = np.random.default_rng(8)
+    for v in list(rng.uniform(0, 2, 3000) * np.exp2(rng.uniform(-26, 14, 3000))):
+        up, dn = orc.double_to_half_up(v), orc.double_to_half_down(v)
+        vu, vd = orc.half_to_double(up), orc.half_to_double(dn)
+        assert vd <= v <= vu
+        assert vu - vd <= (orc.half_to_double(up + 1) - vu) * 1.0 + 1e-300 or vu == vd
+        if vu != v:  # minimal: the code just below 'up' is already below v
+            assert orc.half_to_double(up - 1) < v
+        if vd != v and dn > 0:
+            assert orc.half_to_double(dn + 1) > v
+
+
+# ----------------------------------------------------------------- layout --
+def test_block_sizes(orc):
+    assert (orc.block_bytes(Q8_0), orc.block_weights(Q8_0)) == (34, 32)
+    assert (orc.block_bytes(Q4_K), orc.block_weights(Q4_K)) == (144, 256)
+    assert (orc.block_bytes(AFFINE4), orc.block_weights(AFFINE4)) == (20, 32)
+    for K in (256, 2048, 2560, 9728):
+        assert orc.row_bytes(Q8_0, K) == K * 17 // 16
+        assert orc.row_bytes(Q4_K, K) == K * 9 // 16
+        assert orc.row_bytes(AFFINE4, K) == K * 5 // 8
+
+
+# --------------------------------------------------------- worked examples --
+def test_q8_0_worked_example(orc):
+    blk, f = load_golden("q8_0_e1.txt")
+    assert len(blk) == 34
+    w = orc.dequant(Q8_0, np.frombuffer(blk, np.uint8).reshape(1, 34), 1, 32)[0]
+    assert np.array_equal(w, 0.5 * (np.arange(32) - 16.0))
+    ones = np.ones((1, 32), np.float32)
+    ramp = np.arange(32, dtype=np.float32)[None]
+    y, ay = orc.gemv(Q8_0, np.frombuffer(blk, np.uint8).reshape(1, 34), ones, 1, 32)
+    assert (y[0, 0], ay[0, 0]) == (-8.0, 128.0)
+    y, ay = orc.gemv(Q8_0, np.frombuffer(blk, np.uint8).reshape(1, 34), ramp, 1, 32)
+    assert (y[0, 0], ay[0, 0]) == (1240.0, 1920.0)
+
+
+def test_q4_k_worked_example(orc):
+    blk, f = load_golden("q4k_e2.txt")
+    assert len(blk) == 144
+    sc = [int(v) for v in f["sc"]]
+    m = [int(v) for v in f["m"]]
+    # the packed 6-bit scales decode to the stated (sc, m) for every sub-block
+    for j in range(8):
+        assert orc.unpack_scale_min(blk[4:16], j) == (sc[j], m[j])
+    w = orc.dequant(Q4_K, np.frombuffer(blk, np.uint8).reshape(1, 144), 1, 256)[0]
+    d, dmin = f["d"][0], f["dmin"][0]
+    expect = np.array([d * sc[i // 32] * ((i + i // 32) % 16) - dmin * m[i // 32] for i in range(256)])
+    assert np.array_equal(w, expect)
+    assert (w[0], w[32], w[255]) == (0.0, -0.5, 377.5)
+    b = np.frombuffer(blk, np.uint8).reshape(1, 144)
+    y, ay = orc.gemv(Q4_K, b, np.ones((1, 256), np.float32), 1, 256)
+    assert y[0, 0] == 240 * sum(sc) - 16 * sum(m) == 38480
+    y, ay = orc.gemv(Q4_K, b, np.arange(256, dtype=np.float32)[None], 1, 256)
+    assert (y[0, 0], ay[0, 0]) == (7768984.0, 7871992.0)
+
+
+def test_affine4_nibble_order(orc):
+    """Hand-built group: s = 2, b = -1, codes byte i = (2i mod 16) | ((2i+1 mod 16) << 4)."""
+    blk = bytes([0x00, 0x40, 0x00, 0xBC]) + bytes(((2 * i) % 16) | ((((2 * i) + 1) % 16) << 4)
+                                                 for i in range(16))
+    w = orc.dequant(AFFINE4, np.frombuffer(blk, np.uint8).reshape(1, 20), 1, 32)[0]
+    assert np.array_equal(w, 2.0 * (np.arange(32) % 16) - 1.0)
+
+
+# --------------------------------------------------- quantizer invariants --
+def _adversarial_blocks(bw, rng):
+    rows = [
+        np.zeros(bw), np.full(bw, 0.013), np.full(bw, -0.02), rng.uniform(0, 1, bw),
+        -rng.uniform(0, 1, bw), np.where(np.arange(bw) == 5, 3.0, 1e-3 * rng.standard_normal(bw)),
+        rng.standard_normal(bw) * 1e-7, rng.standard_normal(bw) * 60.0,
+        np.where(np.arange(bw) % 32 == 0, -0.5, 0.0), np.linspace(-1, 1, bw),
+    ]
+    return np.stack(rows).astype(np.float32)
+
+
+@pytest.mark.parametrize("fmt", [Q8_0, Q4_K, AFFINE4])
+def test_round_trip_bound(orc, fmt):
+    """|w - deq(q(w))| <= step/2 for every block (the quantizer's covering bound)."""
+    bw, bb = orc.block_weights(fmt), orc.block_bytes(fmt)
+    rng = np.random.default_rng(11)
+    w = np.concatenate([inputs.weights(64, 512, seed=3, tensor_id=fmt).reshape(-1, bw),
+                        _adversarial_blocks(bw, rng)]).astype(np.float32)
+    nblk = w.shape[0]
+    # one block per row so each row is one block
+    blocks = orc.quantize(fmt, w)
+    deq = orc.dequant(fmt, blocks, nblk, bw)
+    err = np.abs(w.astype(np.float64) - deq)
+    for r in range(nblk):
+        b = blocks[r]
+        if fmt == Q8_0:
+            d = orc.half_to_double(int(b[0]) | (int(b[1]) << 8))
+            amax = float(np.abs(w[r].astype(np.float64)).max())
+            if d >= 2.0 ** -14:
+                assert err[r].max() <= d / 2 * (1 + 1e-12)
+            else:
+                # fp16 d is subnormal or zero: relative rounding of d is coarse and the
+                # +-127 clamp may bite, so only the covering bound of the clamp holds
+                assert amax / 127 < 2.0 ** -14
+                assert err[r].max() <= max(d / 2, amax - 127 * d) * (1 + 1e-12) + 1e-300
+            q = b[2:].view(np.int8)
+            assert q.min() >= -127
+            assert d == float(np.float16(np.abs(w[r].astype(np.float64)).max() / 127))
+        elif fmt == Q4_K:
+            d = orc.half_to_double(int(b[0]) | (int(b[1]) << 8))
+            dmin = orc.half_to_double(int(b[2]) | (int(b[3]) << 8))
+            for j in range(8):
+                sc, m = orc.unpack_scale_min(bytes(b[4:16]), j)
+                assert 0 <= sc <= 63 and 0 <= m <= 63
+                seg = slice(32 * j, 32 * j + 32)
+                assert err[r, seg].max() <= d * sc / 2 * (1 + 1e-12) + 1e-300
+                # the min covers the most negative weight of the sub-block
+                assert dmin * m >= -min(0.0, float(w[r, seg].min()))
+        else:
+            s = orc.half_to_double(int(b[0]) | (int(b[1]) << 8))
+            bias = orc.half_to_double(int(b[2]) | (int(b[3]) << 8))
+            assert bias <= w[r].min()
+            assert err[r].max() <= s / 2 * (1 + 1e-12) + 1e-300
+
+
+def test_q8_0_codes_match_exact_rounding(orc):
+    """Codes equal round-half-away-from-zero of the exact rational w/d (numpy fp16 for d)."""
+    w = inputs.weights(16, 256, seed=5, tensor_id=2)
+    blocks = orc.quantize(Q8_0, w).reshape(-1, 34)
+    wb = w.reshape(-1, 32)
+    for blk, ws in zip(blocks, wb):
+        d = Fraction(orc.half_to_double(int(blk[0]) | (int(blk[1]) << 8)))
+        for qi, wi in zip(blk[2:].view(np.int8), ws):
+            r = Fraction(float(wi)) / d
+            expect = int(math.floor(abs(r) + Fraction(1, 2))) * (1 if r >= 0 else -1)
+            assert int(qi) == max(-127, min(127, expect))
+
+
+# ------------------------------------------------------------------- gemv --
+@pytest.mark.parametrize("fmt", [Q8_0, Q4_K, AFFINE4])
+@pytest.mark.parametrize("K", [256, 512])
+def test_gemv_brute_force(orc, fmt, K):
+    """Oracle GEMV == numpy dense fp64 matmul of the dequantized matrix (other summation order)."""
+    N, M = 8, 16
+    w = inputs.weights(N, K, seed=1, tensor_id=K + fmt)
+    blocks = orc.quantize(fmt, w)
+    deq = orc.dequant(fmt, blocks, N, K)
+    for xdt in ("f32", "bf16"):
+        xf = inputs.activations_f32(M, K, seed=1, tensor_id=K)
+        x = xf if xdt == "f32" else inputs.to_bf16_bits(xf)
+        xv = xf.astype(np.float64) if xdt == "f32" else inputs.bf16_bits_to_f32(x).astype(np.float64)
+        y, ay = orc.gemv(fmt, blocks, x, N, K)
+        ref = xv @ deq.T
+        aref = np.abs(xv) @ np.abs(deq).T
+        assert np.all(np.abs(y - ref) <= 1e-12 * aref)
+        assert np.allclose(ay, aref, rtol=1e-12, atol=0)
+
+
+def test_gemv_exact_rational(orc):
+    """fp64 oracle result is within K*eps*sum|w x| of the exact rational sum."""
+    N, K, M = 3, 256, 2
+    w = inputs.weights(N, K, seed=2, tensor_id=9)
+    blocks = orc.quantize(Q4_K, w)
+    deq = orc.dequant(Q4_K, blocks, N, K)
+    x = inputs.activations_bf16(M, K, seed=2, tensor_id=10)
+    xv = inputs.bf16_bits_to_f32(x)
+    y, ay = orc.gemv(Q4_K, blocks, x, N, K)
+    for j in range(M):
+        for n in range(N):
+            exact = sum(Fraction(float(deq[n, k])) * Fraction(float(xv[j, k])) for k in range(K))
+            assert abs(Fraction(float(y[j, n])) - exact) <= Fraction(K * 2.0 ** -52) * Fraction(float(ay[j, n]))
+
+
+def test_gemv_sampled_matches_full(orc):
+    N, K, M = 40, 512, 5
+    w = inputs.weights(N, K, seed=4, tensor_id=1)
+    blocks = orc.quantize(Q4_K, w)
+    x = inputs.activations_bf16(M, K, seed=4, tensor_id=2)
+    y, ay = orc.gemv(Q4_K, blocks, x, N, K)
+    js = np.array([0, 4, 2, 3, 1]); ns = np.array([0, 39, 17, 5, 22])
+    ys, ays = orc.gemv_sampled(Q4_K, blocks, x, N, K, js, ns)
+    assert np.array_equal(ys, y[js, ns]) and np.array_equal(ays, ay[js, ns])
+
+
+def test_special_cases(orc):
+    # zero scale -> zero output; NaN scale -> NaN only in that row
+    K = 256
+    w = inputs.weights(4, K, seed=6, tensor_id=3)
+    blocks = orc.quantize(Q4_K, w)
+    blocks[1, 0:2] = 0  # d = 0 and dmin = 0 in row 1's only super-block
+    blocks[1, 2:4] = 0
+    blocks[2, 0:2] = [0x00, 0x7E]  # d = NaN in row 2
+    x = inputs.activations_bf16(3, K, seed=6, tensor_id=4)
+    y, _ = orc.gemv(Q4_K, blocks, x, 4, K)
+    assert np.all(y[:, 1] == 0.0)
+    assert np.all(np.isnan(y[:, 2]))
+    assert np.all(np.isfinite(y[:, [0, 3]]))
+    # all codes equal, x = 1: y = n_blocks * 32 * d * q (Q8_0 closed form)
+    blk = bytes([0x00, 0x34]) + bytes([7]) * 32  # d = 0.25, q = 7
+    b = np.frombuffer(blk * 4, np.uint8).reshape(1, 136)
+    y, _ = orc.gemv(Q8_0, b, np.ones((1, 128), np.float32), 1, 128)
+    assert y[0, 0] == 4 * 32 * 0.25 * 7
