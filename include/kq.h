@@ -1,0 +1,119 @@
+/*
+ * kq -- fused dequantize-and-multiply of block-quantized weights for GB300 (sm_103a).
+ *
+ * What the library computes (engine READMEs this library follows):
+ *  - Kinetic README, "What makes it fast": on a personal computer a decode step is
+ *    bound by memory bandwidth because a dense model reads all of its weights once
+ *    per token; speculative decoding checks every guessed token in one pass over
+ *    the weights; several users can share that pass. kq_gemv is that pass:
+ *        Y[j][n] = sum_k deq(W)[n][k] * X[j][k],   j < M <= 16, n < N, k < K.
+ *  - Same section, last paragraph: every row of a batch is summed in the same
+ *    order as that token would be on its own. kq_gemv guarantees it: row j of Y
+ *    has the same bits for every M in 1..16 and every slot position j.
+ *  - Same section: long prompts run as tiled matrix products so that each weight
+ *    block is unpacked once and used for many tokens. kq_gemm with M > 16 is that
+ *    prefill product, on the tensor cores.
+ *  - Kinetic README, "Switching from llama.cpp": GGUF files work unchanged, so
+ *    Q8_0 and Q4_K blocks use GGUF's byte layouts. Kipp README, "How fast": its
+ *    4-bit scheme is affine (scale + bias) with groups of 32 (layout below).
+ *
+ * Conventions: W is N x K, row-major, the blocks of one row contiguous along K
+ * (GGUF order). X is M x K row-major (fp32 or bf16). Y is M x N fp32 row-major and
+ * is overwritten, never accumulated. All pointers are DEVICE pointers unless a
+ * function says otherwise. The caller owns every buffer; the library allocates
+ * nothing per call and keeps no state besides a thread-local error string.
+ * Every call is asynchronous on `stream` (a cudaStream_t passed as void*, NULL =
+ * the legacy default stream) and never synchronises. There is no CPU fallback:
+ * a call either launches the sm_103a kernels or returns an error.
+ */
+#ifndef KQ_H
+#define KQ_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Block formats.
+ * KQ_Q8_0        34 bytes / 32 weights: fp16 d, int8 q[32];            w = d*q
+ * KQ_Q4_K       144 bytes / 256 weights: fp16 d, fp16 dmin, scales[12] (eight 6-bit
+ *                scales sc_j and mins m_j, GGUF packing), qs[128] (byte 32c+l holds
+ *                weight 64c+l in its low nibble and 64c+32+l in its high nibble);
+ *                w = d*sc_j*q - dmin*m_j for sub-block j = weight/32
+ * KQ_AFFINE4_G32 20 bytes / 32 weights: fp16 s, fp16 b, codes[16] (weight 2i in the
+ *                low nibble of byte i, weight 2i+1 in the high nibble); w = s*q + b */
+enum kq_fmt { KQ_Q8_0 = 1, KQ_Q4_K = 2, KQ_AFFINE4_G32 = 3 };
+
+/* Activation element types. */
+enum kq_dtype { KQ_F32 = 1, KQ_BF16 = 2 };
+
+/* Status codes: 0 on success, negative on failure (text in kq_last_error()). */
+enum kq_status {
+  KQ_OK = 0,
+  KQ_ERR_ARG = -1,         /* null pointer, size out of range, misaligned pointer */
+  KQ_ERR_UNSUPPORTED = -2, /* unknown format or dtype, or a pair with no kernel */
+  KQ_ERR_WORKSPACE = -3,   /* workspace missing or smaller than kq_gemm_workspace_size */
+  KQ_ERR_CUDA = -4,        /* a CUDA launch or runtime call failed */
+  KQ_ERR_TIMEOUT = -5      /* a bounded device-side wait gave up */
+};
+
+/* Bytes and weights per block of `fmt`; 0 for an unknown format. */
+size_t kq_block_bytes(int fmt);
+size_t kq_block_weights(int fmt);
+/* Bytes of one row of K weights; 0 if fmt is unknown or K is not a multiple of the
+ * block's weight count. */
+size_t kq_row_bytes(int fmt, int K);
+
+/* Message for the last failing call on this host thread ("" after a success). The
+ * pointer stays valid until the next kq_* call on the same thread. */
+const char* kq_last_error(void);
+const char* kq_version(void);
+
+/* Quantized GEMV / speculative-verify product (Kinetic README, "What makes it fast").
+ *   fmt       KQ_Q8_0, KQ_Q4_K or KQ_AFFINE4_G32
+ *   w_blocks  N * kq_row_bytes(fmt, K) bytes, 16-byte aligned
+ *   x_dtype   KQ_BF16 (tensor-core path) or KQ_F32 (CUDA-core path)
+ *   x         M x K activations, 16-byte aligned
+ *   y         M x N fp32 output (overwritten), 8-byte aligned
+ *   M         1..16 token rows; 0 returns KQ_OK without launching
+ *   N         output rows, >= 0 (0 is a no-op)
+ *   K         inputs per row, >= 0, a multiple of 256 (keeps every format's rows
+ *             16-byte aligned for vector loads); K == 0 writes zeros
+ * Row j of Y is bit-identical for every M and every position j (the kernel and its
+ * work split are chosen from (fmt, x_dtype, N, K) only; M masks loads and stores).
+ * Errors: KQ_ERR_ARG, KQ_ERR_UNSUPPORTED, KQ_ERR_CUDA. */
+int kq_gemv(int fmt, const void* w_blocks, int x_dtype, const void* x, float* y, int M, int N,
+            int K, void* stream);
+
+/* Quantized GEMM (Kinetic README, "What makes it fast": long prompts as tiled matrix
+ * products, each weight block unpacked once for many tokens).
+ *   M <= 16: identical to kq_gemv (same kernels, same bits); the workspace is unused.
+ *   M  > 16: tensor-core (tcgen05) product for fmt = KQ_Q4_K, x_dtype = KQ_BF16; within
+ *            the documented tolerance of the fp64 result, not bit-identical to kq_gemv.
+ *   workspace/ws_bytes: device scratch of at least kq_gemm_workspace_size() bytes,
+ *            256-byte aligned, owned by the caller; may be NULL when that size is 0.
+ * Other arguments as kq_gemv. Errors: as kq_gemv, plus KQ_ERR_WORKSPACE. */
+int kq_gemm(int fmt, const void* w_blocks, int x_dtype, const void* x, float* y, int M, int N,
+            int K, void* workspace, size_t ws_bytes, void* stream);
+size_t kq_gemm_workspace_size(int fmt, int x_dtype, int M, int N, int K);
+
+/* Quantize an N x K fp32 matrix (device memory) into N rows of blocks of `fmt`, on the
+ * GPU, in fp64 arithmetic, with the same covering scheme in every call:
+ *   Q8_0:    d = fp16_rn(max|w|/127), q = clamp(round_half_away(w/d), -127, 127)
+ *   Q4_K:    per sub-block lo = min(0, min w), hi = max(0, max w);
+ *            dmin = smallest fp16 >= max(-lo)/63, m_j = ceil(-lo_j/dmin);
+ *            t_j = hi_j + dmin*m_j, d = smallest fp16 >= max(t)/945,
+ *            sc_j = ceil(t_j/(15 d)), q = round_half_away((w + dmin*m_j)/(d*sc_j))
+ *   AFFINE4: b = largest fp16 <= min w, s = smallest fp16 >= (max w - b)/15,
+ *            q = clamp(round_half_away((w - b)/s), 0, 15)
+ * These make data for tests and benchmarks (the GEMV never quantizes). K must be a
+ * multiple of the block's weight count; w 4-byte aligned, w_blocks 2-byte aligned.
+ * Errors: KQ_ERR_ARG, KQ_ERR_CUDA. */
+int kq_quantize(int fmt, const float* w, void* w_blocks, int N, int K, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KQ_H */

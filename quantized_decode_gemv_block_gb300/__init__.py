@@ -1,0 +1,146 @@
+"""kq: fused dequantize-and-multiply of block-quantized weights on GB300 (sm_103a).
+
+A thin ctypes binding over the C-ABI library ``libkq.so`` (declared in
+``include/kq.h``). This module only marshals arguments: it passes device pointers
+and the current CUDA stream to the library and raises on a nonzero status. Every
+step of the computation runs in the library's CUDA kernels; there is no CPU or
+PyTorch fallback, and importing fails loudly if ``libkq.so`` has not been built
+(``python -m quantized_decode_gemv_block_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkq.so")
+
+Q8_0, Q4_K, AFFINE4 = 1, 2, 3
+F32, BF16 = 1, 2
+FORMATS = {"q8_0": Q8_0, "q4_k": Q4_K, "affine4": AFFINE4}
+KQ_OK, KQ_ERR_ARG, KQ_ERR_UNSUPPORTED, KQ_ERR_WORKSPACE, KQ_ERR_CUDA, KQ_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
+
+
+class KQError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"kq error {code}: {msg}")
+        self.code = code
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libkq.so and declare its C signatures. Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with "
+                          "`python -m quantized_decode_gemv_block_gb300.build` (needs nvcc)")
+    L = ctypes.CDLL(path)
+    P, I, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    L.kq_block_bytes.argtypes = [I]
+    L.kq_block_bytes.restype = SZ
+    L.kq_block_weights.argtypes = [I]
+    L.kq_block_weights.restype = SZ
+    L.kq_row_bytes.argtypes = [I, I]
+    L.kq_row_bytes.restype = SZ
+    L.kq_last_error.restype = ctypes.c_char_p
+    L.kq_version.restype = ctypes.c_char_p
+    L.kq_gemv.argtypes = [I, P, I, P, P, I, I, I, P]
+    L.kq_gemv.restype = I
+    L.kq_gemm.argtypes = [I, P, I, P, P, I, I, I, P, SZ, P]
+    L.kq_gemm.restype = I
+    L.kq_gemm_workspace_size.argtypes = [I, I, I, I, I]
+    L.kq_gemm_workspace_size.restype = SZ
+    L.kq_quantize.argtypes = [I, P, P, I, I, P]
+    L.kq_quantize.restype = I
+    _lib = L
+    return L
+
+
+def lib():
+    return load_library()
+
+
+def _fmt(fmt) -> int:
+    return FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
+
+
+def _check(rc: int):
+    if rc != KQ_OK:
+        raise KQError(rc, lib().kq_last_error().decode())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def block_bytes(fmt) -> int:
+    return lib().kq_block_bytes(_fmt(fmt))
+
+
+def block_weights(fmt) -> int:
+    return lib().kq_block_weights(_fmt(fmt))
+
+
+def row_bytes(fmt, K: int) -> int:
+    return lib().kq_row_bytes(_fmt(fmt), K)
+
+
+def version() -> str:
+    return lib().kq_version().decode()
+
+
+def _x_dtype(x: torch.Tensor) -> int:
+    if x.dtype == torch.bfloat16:
+        return BF16
+    if x.dtype == torch.float32:
+        return F32
+    raise TypeError("x must be torch.bfloat16 or torch.float32")
+
+
+def gemv(fmt, w: torch.Tensor, x: torch.Tensor, N: int, K: int, y: torch.Tensor | None = None,
+         stream=None) -> torch.Tensor:
+    """Y (M x N fp32) = X (M x K) @ deq(W)^T for M <= 16, through kq_gemv."""
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _check(lib().kq_gemv(_fmt(fmt), w.data_ptr(), _x_dtype(x), x.data_ptr(), y.data_ptr(), M, N, K,
+                         _stream(stream)))
+    return y
+
+
+def gemm_workspace_size(fmt, x_dtype, M: int, N: int, K: int) -> int:
+    xd = x_dtype if isinstance(x_dtype, int) else (BF16 if x_dtype == torch.bfloat16 else F32)
+    return lib().kq_gemm_workspace_size(_fmt(fmt), xd, M, N, K)
+
+
+def gemm(fmt, w: torch.Tensor, x: torch.Tensor, N: int, K: int, y: torch.Tensor | None = None,
+         workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Y = X @ deq(W)^T for any M, through kq_gemm (tensor cores for M > 16)."""
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    need = gemm_workspace_size(fmt, _x_dtype(x), M, N, K)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    wp = workspace.data_ptr() if workspace is not None else None
+    wn = workspace.numel() if workspace is not None else 0
+    _check(lib().kq_gemm(_fmt(fmt), w.data_ptr(), _x_dtype(x), x.data_ptr(), y.data_ptr(), M, N, K,
+                         wp, wn, _stream(stream)))
+    return y
+
+
+def quantize(fmt, w: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """fp32 N x K device matrix -> N x row_bytes uint8 blocks, through kq_quantize."""
+    N, K = w.shape
+    if out is None:
+        out = torch.empty((N, row_bytes(fmt, K)), dtype=torch.uint8, device=w.device)
+    _check(lib().kq_quantize(_fmt(fmt), w.data_ptr(), out.data_ptr(), N, K, _stream(stream)))
+    return out

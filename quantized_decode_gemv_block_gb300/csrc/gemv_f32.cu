@@ -1,0 +1,173 @@
+// CUDA-core GEMV for fp32 activations, M = 1..16.
+//
+// Same product as the tensor-core path, Y[j][n] = sum_k deq(W)[n][k] * X[j][k]
+// (Kinetic README, "What makes it fast"), for callers whose activations are fp32
+// (an fp32 value does not fit a bf16 MMA operand exactly). Each warp owns two rows;
+// lane (gi, q) takes weights 8q..8q+7 of 32-group gi of every 256-weight unit. Per
+// 8-weight slice it forms P = sum code*x and S = sum x in fp32 and promotes with
+// acc = fma(scale, P, acc) and acc = fma(offset, S, acc); the 32 lane partials are
+// added by a fixed butterfly. Each token's chain of operations is the same for every
+// M (the kernel is instantiated for 1, 2, 4, 8 or 16 token slots and M only masks),
+// so a row's bits do not depend on the batch.
+#include "kq_device.cuh"
+#include "kq_internal.h"
+
+namespace kq {
+namespace {
+
+constexpr int kThreadsF = 256;
+constexpr int kRowsPerWarp = 2;
+constexpr int kRowsPerCtaF = 8 * kRowsPerWarp;
+
+__device__ __forceinline__ uint32_t ldg16(const void* p) {
+  unsigned short v;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+template <int FMT>
+__device__ __forceinline__ void decode_slice(const uint8_t* unit, int gi, int q, float (&c)[8],
+                                             float& scale, float& offset) {
+  if (FMT == FMT_Q4_K) {
+    const uint4 h = ldg128(unit);
+    const int ch = gi >> 1;
+    const uint2 b = ldg64(unit + 16 + 32 * ch + 8 * q);
+    const uint32_t s0 = h.y, s1 = h.z, s2 = h.w;
+    uint32_t scw, mw;
+    if (gi < 4) {
+      scw = s0 & 0x3F3F3F3Fu;
+      mw = s1 & 0x3F3F3F3Fu;
+    } else {
+      scw = (s2 & 0x0F0F0F0Fu) | ((s0 >> 2) & 0x30303030u);
+      mw = ((s2 >> 4) & 0x0F0F0F0Fu) | ((s1 >> 2) & 0x30303030u);
+    }
+    const int sh = 8 * (gi & 3);
+    const float sc = static_cast<float>((scw >> sh) & 0xFFu);
+    const float m = static_cast<float>((mw >> sh) & 0xFFu);
+    const float d = half_bits_to_float(h.x), dmin = half_bits_to_float(h.x >> 16);
+    scale = d * sc;      // exact: 11-bit x 6-bit
+    offset = -dmin * m;  // exact
+    const int nsh = (gi & 1) ? 4 : 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      c[k] = static_cast<float>((b.x >> (8 * k + nsh)) & 15u);
+      c[4 + k] = static_cast<float>((b.y >> (8 * k + nsh)) & 15u);
+    }
+  } else if (FMT == FMT_Q8_0) {
+    const uint8_t* blk = unit + 34 * gi;
+    scale = half_bits_to_float(ldg16(blk));
+    offset = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t v = ldg16(blk + 2 + 8 * q + 2 * k);
+      c[2 * k] = static_cast<float>(static_cast<int8_t>(v & 0xFFu));
+      c[2 * k + 1] = static_cast<float>(static_cast<int8_t>(v >> 8));
+    }
+  } else {
+    const uint8_t* grp = unit + 20 * gi;
+    const uint32_t sb = ldg32(grp);
+    const uint32_t cw = ldg32(grp + 4 + 4 * q);
+    scale = half_bits_to_float(sb);
+    offset = half_bits_to_float(sb >> 16);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      c[2 * k] = static_cast<float>((cw >> (8 * k)) & 15u);
+      c[2 * k + 1] = static_cast<float>((cw >> (8 * k + 4)) & 15u);
+    }
+  }
+}
+
+template <int FMT>
+constexpr int unit_bytes() {
+  return FMT == FMT_Q4_K ? 144 : (FMT == FMT_Q8_0 ? 272 : 160);
+}
+
+template <int FMT, int MT>
+__global__ void __launch_bounds__(kThreadsF) gemv_f32_kernel(const uint8_t* __restrict__ w,
+                                                             const float* __restrict__ x,
+                                                             float* __restrict__ y, int M, int N,
+                                                             int K, long long row_bytes) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gi = lane >> 2, q = lane & 3;
+  const int nbase = (blockIdx.x * 8 + warp) * kRowsPerWarp;
+  float acc[kRowsPerWarp][MT];
+#pragma unroll
+  for (int i = 0; i < kRowsPerWarp; ++i)
+#pragma unroll
+    for (int j = 0; j < MT; ++j) acc[i][j] = 0.f;
+
+  const int units = K / 256;
+  for (int u = 0; u < units; ++u) {
+    float c[kRowsPerWarp][8], sc[kRowsPerWarp], off[kRowsPerWarp];
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+      const int row = min(nbase + i, N - 1);
+      decode_slice<FMT>(w + row * row_bytes + (long long)u * unit_bytes<FMT>(), gi, q, c[i], sc[i],
+                        off[i]);
+    }
+#pragma unroll
+    for (int j = 0; j < MT; ++j) {
+      if (j < M) {
+        const float* xp = x + (long long)j * K + u * 256 + 32 * gi + 8 * q;
+        const uint4 v0 = ldg128(xp), v1 = ldg128(xp + 4);
+        const float xv[8] = {__uint_as_float(v0.x), __uint_as_float(v0.y), __uint_as_float(v0.z),
+                             __uint_as_float(v0.w), __uint_as_float(v1.x), __uint_as_float(v1.y),
+                             __uint_as_float(v1.z), __uint_as_float(v1.w)};
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) s = __fadd_rn(s, xv[k]);
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i) {
+          float p = 0.f;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) p = __fmaf_rn(c[i][k], xv[k], p);
+          acc[i][j] = __fmaf_rn(sc[i], p, acc[i][j]);
+          if (FMT != FMT_Q8_0) acc[i][j] = __fmaf_rn(off[i], s, acc[i][j]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kRowsPerWarp; ++i) {
+#pragma unroll
+    for (int j = 0; j < MT; ++j) {
+      float v = acc[i][j];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+      if (lane == 0 && j < M && nbase + i < N) y[(long long)j * N + nbase + i] = v;
+    }
+  }
+}
+
+template <int FMT>
+int launch_fmt(const uint8_t* w, const float* x, float* y, int M, int N, int K,
+               long long row_bytes, cudaStream_t s) {
+  const dim3 grid((N + kRowsPerCtaF - 1) / kRowsPerCtaF), block(kThreadsF);
+  if (M <= 1) gemv_f32_kernel<FMT, 1><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
+  else if (M <= 2) gemv_f32_kernel<FMT, 2><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
+  else if (M <= 4) gemv_f32_kernel<FMT, 4><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
+  else if (M <= 8) gemv_f32_kernel<FMT, 8><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
+  else gemv_f32_kernel<FMT, 16><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
+  return 0;
+}
+
+}  // namespace
+
+int launch_gemv_f32(int fmt, const void* w, const float* x, float* y, int M, int N, int K,
+                    long long row_bytes, cudaStream_t stream, std::string* err) {
+  const uint8_t* wb = static_cast<const uint8_t*>(w);
+  switch (fmt) {
+    case FMT_Q4_K: launch_fmt<FMT_Q4_K>(wb, x, y, M, N, K, row_bytes, stream); break;
+    case FMT_Q8_0: launch_fmt<FMT_Q8_0>(wb, x, y, M, N, K, row_bytes, stream); break;
+    case FMT_AFFINE4: launch_fmt<FMT_AFFINE4>(wb, x, y, M, N, K, row_bytes, stream); break;
+    default: *err = "unsupported format"; return -1;
+  }
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    *err = std::string("gemv (fp32 x) launch: ") + cudaGetErrorString(e);
+    return -1;
+  }
+  return 0;
+}
+
+}  // namespace kq

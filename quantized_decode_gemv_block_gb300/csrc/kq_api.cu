@@ -1,0 +1,154 @@
+// C-ABI boundary of libkq: argument checks, error reporting and kernel dispatch.
+// The declarations, their sources and their contracts are in include/kq.h.
+#include <cstdint>
+#include <cstdio>
+#include <string>
+
+#include "../../include/kq.h"
+#include "kq_internal.h"
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const std::string& msg) {
+  g_err = msg;
+  return code;
+}
+int ok() {
+  g_err.clear();
+  return KQ_OK;
+}
+
+bool fmt_known(int fmt) { return fmt == KQ_Q8_0 || fmt == KQ_Q4_K || fmt == KQ_AFFINE4_G32; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int sm_count(std::string* err) {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    *err = std::string("cudaGetDevice: ") + cudaGetErrorString(e);
+    return -1;
+  }
+  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess || n <= 0) {
+    *err = std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e);
+    return -1;
+  }
+  if (dev < 64) cached[dev] = n;
+  return n;
+}
+
+// Shared checks of kq_gemv / kq_gemm; returns KQ_OK or an error (already recorded).
+int check_common(int fmt, const void* w, int x_dtype, const void* x, const float* y, int M, int N,
+                 int K) {
+  if (!fmt_known(fmt)) return fail(KQ_ERR_UNSUPPORTED, "unknown block format " + std::to_string(fmt));
+  if (x_dtype != KQ_F32 && x_dtype != KQ_BF16)
+    return fail(KQ_ERR_UNSUPPORTED, "unknown activation dtype " + std::to_string(x_dtype));
+  if (M < 0 || N < 0 || K < 0) return fail(KQ_ERR_ARG, "M, N and K must be >= 0");
+  if (K % 256 != 0) return fail(KQ_ERR_ARG, "K must be a multiple of 256, got " + std::to_string(K));
+  if (M == 0 || N == 0) return KQ_OK;
+  if (y == nullptr) return fail(KQ_ERR_ARG, "y is NULL");
+  if (!aligned(y, 4)) return fail(KQ_ERR_ARG, "y must be 4-byte aligned");
+  if (K > 0) {
+    if (w == nullptr || x == nullptr) return fail(KQ_ERR_ARG, "w_blocks or x is NULL");
+    if (!aligned(w, 16)) return fail(KQ_ERR_ARG, "w_blocks must be 16-byte aligned");
+    if (!aligned(x, 16)) return fail(KQ_ERR_ARG, "x must be 16-byte aligned");
+  }
+  return KQ_OK;
+}
+
+int gemv_impl(int fmt, const void* w, int x_dtype, const void* x, float* y, int M, int N, int K,
+              cudaStream_t s) {
+  if (M > 16) return fail(KQ_ERR_ARG, "kq_gemv takes M <= 16 token rows, got " + std::to_string(M));
+  int rc = check_common(fmt, w, x_dtype, x, y, M, N, K);
+  if (rc != KQ_OK) return rc;
+  if (M == 0 || N == 0) return ok();
+  if (K == 0) {
+    const cudaError_t e = cudaMemsetAsync(y, 0, sizeof(float) * (size_t)M * (size_t)N, s);
+    if (e != cudaSuccess) return fail(KQ_ERR_CUDA, std::string("cudaMemsetAsync: ") + cudaGetErrorString(e));
+    return ok();
+  }
+  std::string err;
+  const long long row_bytes = (long long)kq_row_bytes(fmt, K);
+  if (x_dtype == KQ_BF16) {
+    const int sms = sm_count(&err);
+    if (sms < 0) return fail(KQ_ERR_CUDA, err);
+    if (kq::launch_gemv_mma(fmt, w, x, y, M, N, K, row_bytes, sms, s, &err) != 0)
+      return fail(KQ_ERR_CUDA, err);
+  } else {
+    if (kq::launch_gemv_f32(fmt, w, static_cast<const float*>(x), y, M, N, K, row_bytes, s, &err) != 0)
+      return fail(KQ_ERR_CUDA, err);
+  }
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kq_block_bytes(int fmt) {
+  switch (fmt) {
+    case KQ_Q8_0: return 34;
+    case KQ_Q4_K: return 144;
+    case KQ_AFFINE4_G32: return 20;
+  }
+  return 0;
+}
+
+size_t kq_block_weights(int fmt) {
+  switch (fmt) {
+    case KQ_Q8_0: return 32;
+    case KQ_Q4_K: return 256;
+    case KQ_AFFINE4_G32: return 32;
+  }
+  return 0;
+}
+
+size_t kq_row_bytes(int fmt, int K) {
+  const size_t bw = kq_block_weights(fmt);
+  if (bw == 0 || K < 0 || (size_t)K % bw != 0) return 0;
+  return (size_t)K / bw * kq_block_bytes(fmt);
+}
+
+const char* kq_last_error(void) { return g_err.c_str(); }
+
+const char* kq_version(void) { return "kq 0.1.0 (sm_103a)"; }
+
+int kq_gemv(int fmt, const void* w_blocks, int x_dtype, const void* x, float* y, int M, int N,
+            int K, void* stream) {
+  return gemv_impl(fmt, w_blocks, x_dtype, x, y, M, N, K, static_cast<cudaStream_t>(stream));
+}
+
+size_t kq_gemm_workspace_size(int fmt, int x_dtype, int M, int N, int K) {
+  (void)fmt; (void)x_dtype; (void)M; (void)N; (void)K;
+  return 0;
+}
+
+int kq_gemm(int fmt, const void* w_blocks, int x_dtype, const void* x, float* y, int M, int N,
+            int K, void* workspace, size_t ws_bytes, void* stream) {
+  (void)workspace; (void)ws_bytes;
+  if (M <= 16)
+    return gemv_impl(fmt, w_blocks, x_dtype, x, y, M, N, K, static_cast<cudaStream_t>(stream));
+  return fail(KQ_ERR_UNSUPPORTED, "kq_gemm with M > 16 is not available in this build");
+}
+
+int kq_quantize(int fmt, const float* w, void* w_blocks, int N, int K, void* stream) {
+  if (!fmt_known(fmt)) return fail(KQ_ERR_UNSUPPORTED, "unknown block format " + std::to_string(fmt));
+  if (N < 0 || K < 0) return fail(KQ_ERR_ARG, "N and K must be >= 0");
+  if (kq_row_bytes(fmt, K) == 0 && K != 0)
+    return fail(KQ_ERR_ARG, "K must be a multiple of the block's weight count");
+  if ((long long)N * K == 0) return ok();
+  if (w == nullptr || w_blocks == nullptr) return fail(KQ_ERR_ARG, "w or w_blocks is NULL");
+  if (!aligned(w, 4) || !aligned(w_blocks, 2)) return fail(KQ_ERR_ARG, "misaligned w or w_blocks");
+  std::string err;
+  if (kq::launch_quantize(fmt, w, w_blocks, N, K, static_cast<cudaStream_t>(stream), &err) != 0)
+    return fail(KQ_ERR_CUDA, err);
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,34 @@
+// Internal launch interface between the C-ABI layer (kq_api.cu) and the kernels.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <string>
+
+namespace kq {
+
+constexpr int kMaxGemvSmem = 96 * 1024;
+
+struct GemvPlan {
+  int units = 0;        // K / 256
+  int ks = 1;           // K-split across a cluster
+  int chunk_units = 1;  // activation staging granularity (units)
+  int grid = 0;         // CTAs
+};
+
+// Work split of the tensor-core GEMV: a function of (N, K, SM count) only.
+GemvPlan plan_gemv_mma(int N, int K, int num_sms);
+size_t gemv_mma_smem(const GemvPlan& pl, int M);
+
+// bf16 activations, tensor-core path. Returns 0 or -1 with *err set.
+int launch_gemv_mma(int fmt, const void* w, const void* x, float* y, int M, int N, int K,
+                    long long row_bytes, int num_sms, cudaStream_t stream, std::string* err);
+
+// fp32 activations, CUDA-core path.
+int launch_gemv_f32(int fmt, const void* w, const float* x, float* y, int M, int N, int K,
+                    long long row_bytes, cudaStream_t stream, std::string* err);
+
+// GPU quantizers (fp64 arithmetic).
+int launch_quantize(int fmt, const float* w, void* blocks, int N, int K, cudaStream_t stream,
+                    std::string* err);
+
+}  // namespace kq

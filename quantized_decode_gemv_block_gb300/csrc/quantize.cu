@@ -1,0 +1,220 @@
+// GPU quantizers: fp32 weights -> Q8_0 / Q4_K / affine4 blocks, in fp64.
+//
+// They make synthetic test and benchmark data (the GEMV itself never quantizes).
+// Block layouts follow GGUF (Kinetic README, "Switching from llama.cpp": GGUF files
+// and llama.cpp's Q8_0/Q4_K bytes unchanged) and, for affine4, the scale + bias per
+// 32 weights of the Kipp README ("How fast"). The scales are chosen by a covering
+// scheme with a provable bound |w - deq(q(w))| <= step/2 (not llama.cpp's search):
+//   Q8_0    d = fp16_rn(max|w| / 127); q = clamp(round_half_away(w / d), -127, 127)
+//   Q4_K    per sub-block lo = min(0, min w), hi = max(0, max w), mraw = -lo;
+//           dmin = smallest fp16 >= max(mraw) / 63, m = ceil(mraw / dmin);
+//           t = hi + dmin*m; d = smallest fp16 >= max(t) / 945; sc = ceil(t / (15 d));
+//           q = round_half_away((w + dmin*m) / (d*sc)), which lies in [0, 15]
+//   affine4 b = largest fp16 <= min w; s = smallest fp16 >= (max w - b) / 15;
+//           q = clamp(round_half_away((w - b) / s), 0, 15)
+// Every fp64 operation is an explicitly rounded intrinsic so that no contraction
+// changes a rounding decision. If a rounding step ever pushed a 6-bit scale or
+// min past 63, its fp16 step is raised by one code and the step repeated.
+#include "kq_device.cuh"
+#include "kq_internal.h"
+
+namespace kq {
+namespace {
+
+__device__ __forceinline__ double h2d(uint16_t h) {
+  return static_cast<double>(__half2float(__ushort_as_half(h)));
+}
+__device__ __forceinline__ uint16_t d2h_rn(double v) {
+  return __half_as_ushort(__double2half(v));
+}
+__device__ __forceinline__ uint16_t h_next_up(uint16_t h) {
+  if (h == 0x8000u) return 0x0001u;
+  return (h & 0x8000u) ? static_cast<uint16_t>(h - 1) : static_cast<uint16_t>(h + 1);
+}
+__device__ __forceinline__ uint16_t h_next_down(uint16_t h) {
+  if (h == 0x0000u) return 0x8001u;
+  return (h & 0x8000u) ? static_cast<uint16_t>(h + 1) : static_cast<uint16_t>(h - 1);
+}
+__device__ __forceinline__ uint16_t d2h_up(double t) {
+  uint16_t h = d2h_rn(t);
+  if (h2d(h) < t) h = h_next_up(h);
+  return h;
+}
+__device__ __forceinline__ uint16_t d2h_down(double t) {
+  uint16_t h = d2h_rn(t);
+  if (h2d(h) > t) h = h_next_down(h);
+  return h;
+}
+__device__ __forceinline__ double dmin_of(double a, double b) { return (b < a) ? b : a; }
+__device__ __forceinline__ double dmax_of(double a, double b) { return (a < b) ? b : a; }
+// fp16 codes are written with one aligned 16-bit store (every block offset is even and
+// kq_quantize requires a 2-byte aligned destination). Writing the two bytes of a code
+// taken straight from cvt.rn.f16.f64 separately was measured to drop its low byte.
+__device__ __forceinline__ void put16(uint8_t* p, uint16_t v) {
+  *reinterpret_cast<uint16_t*>(p) = v;
+}
+
+__global__ void quant_q8_0_kernel(const float* __restrict__ w, uint8_t* __restrict__ out,
+                                  long long nblk) {
+  const long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (b >= nblk) return;
+  const float* src = w + b * 32;
+  double amax = 0.0;
+  for (int i = 0; i < 32; ++i) amax = dmax_of(amax, fabs(static_cast<double>(src[i])));
+  const uint16_t d16 = d2h_rn(__ddiv_rn(amax, 127.0));
+  const double d = h2d(d16);
+  uint8_t* dst = out + b * 34;
+  put16(dst, d16);
+  for (int i = 0; i < 32; ++i) {
+    double qv = 0.0;
+    if (d != 0.0) qv = fmin(127.0, fmax(-127.0, round(__ddiv_rn(static_cast<double>(src[i]), d))));
+    dst[2 + i] = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(qv)));
+  }
+}
+
+__global__ void quant_q4_k_kernel(const float* __restrict__ w, uint8_t* __restrict__ out,
+                                  long long nblk) {
+  const long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (b >= nblk) return;
+  const float* src = w + b * 256;
+  double hi[8], mraw[8];
+  double maxm = 0.0;
+  for (int j = 0; j < 8; ++j) {
+    double l = 0.0, h = 0.0;
+    for (int i = 0; i < 32; ++i) {
+      const double v = static_cast<double>(src[32 * j + i]);
+      l = dmin_of(l, v);
+      h = dmax_of(h, v);
+    }
+    hi[j] = h;
+    mraw[j] = -l;
+    maxm = dmax_of(maxm, mraw[j]);
+  }
+  uint16_t dmin16 = 0;
+  int m[8];
+  for (int j = 0; j < 8; ++j) m[j] = 0;
+  if (maxm > 0.0) {
+    dmin16 = d2h_up(__ddiv_rn(maxm, 63.0));
+    for (int guard = 0; guard < 64; ++guard) {
+      const double dm = h2d(dmin16);
+      bool ok = true;
+      for (int j = 0; j < 8; ++j) {
+        m[j] = static_cast<int>(ceil(__ddiv_rn(mraw[j], dm)));
+        if (m[j] > 63) ok = false;
+      }
+      if (ok) break;
+      dmin16 = h_next_up(dmin16);
+    }
+  }
+  const double dmin = h2d(dmin16);
+  double t[8], maxt = 0.0;
+  for (int j = 0; j < 8; ++j) {
+    t[j] = __dadd_rn(hi[j], __dmul_rn(dmin, static_cast<double>(m[j])));
+    maxt = dmax_of(maxt, t[j]);
+  }
+  uint16_t d16 = 0;
+  int sc[8];
+  for (int j = 0; j < 8; ++j) sc[j] = 0;
+  if (maxt > 0.0) {
+    d16 = d2h_up(__ddiv_rn(maxt, 945.0));
+    for (int guard = 0; guard < 64; ++guard) {
+      const double dd = h2d(d16);
+      bool ok = true;
+      for (int j = 0; j < 8; ++j) {
+        sc[j] = static_cast<int>(ceil(__ddiv_rn(t[j], __dmul_rn(15.0, dd))));
+        if (sc[j] > 63) ok = false;
+      }
+      if (ok) break;
+      d16 = h_next_up(d16);
+    }
+  }
+  const double d = h2d(d16);
+  uint8_t* dst = out + b * 144;
+  put16(dst, d16);
+  put16(dst + 2, dmin16);
+  uint8_t scales[12];
+  for (int i = 0; i < 12; ++i) scales[i] = 0;
+  for (int j = 0; j < 4; ++j) {
+    scales[j] = static_cast<uint8_t>(scales[j] | (sc[j] & 63));
+    scales[j + 4] = static_cast<uint8_t>(scales[j + 4] | (m[j] & 63));
+  }
+  for (int j = 4; j < 8; ++j) {
+    scales[j + 4] = static_cast<uint8_t>((sc[j] & 15) | ((m[j] & 15) << 4));
+    scales[j - 4] = static_cast<uint8_t>(scales[j - 4] | ((sc[j] >> 4) << 6));
+    scales[j] = static_cast<uint8_t>(scales[j] | ((m[j] >> 4) << 6));
+  }
+  for (int i = 0; i < 12; ++i) dst[4 + i] = scales[i];
+  for (int c = 0; c < 4; ++c) {
+    for (int l = 0; l < 32; ++l) {
+      int qq[2];
+      for (int hsel = 0; hsel < 2; ++hsel) {
+        const int i = 64 * c + 32 * hsel + l, j = i >> 5;
+        const double step = __dmul_rn(d, static_cast<double>(sc[j]));
+        int qv = 0;
+        if (step != 0.0) {
+          const double r = round(__ddiv_rn(
+              __dadd_rn(static_cast<double>(src[i]), __dmul_rn(dmin, static_cast<double>(m[j]))),
+              step));
+          qv = static_cast<int>(fmin(15.0, fmax(0.0, r)));
+        }
+        qq[hsel] = qv;
+      }
+      dst[16 + 32 * c + l] = static_cast<uint8_t>(qq[0] | (qq[1] << 4));
+    }
+  }
+}
+
+__global__ void quant_affine4_kernel(const float* __restrict__ w, uint8_t* __restrict__ out,
+                                     long long nblk) {
+  const long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (b >= nblk) return;
+  const float* src = w + b * 32;
+  double mn = static_cast<double>(src[0]), mx = mn;
+  for (int i = 1; i < 32; ++i) {
+    const double v = static_cast<double>(src[i]);
+    mn = dmin_of(mn, v);
+    mx = dmax_of(mx, v);
+  }
+  const uint16_t b16 = d2h_down(mn);
+  const double bias = h2d(b16);
+  const double span = __dadd_rn(mx, -bias);
+  const uint16_t s16 = span > 0.0 ? d2h_up(__ddiv_rn(span, 15.0)) : 0;
+  const double s = h2d(s16);
+  uint8_t* dst = out + b * 20;
+  put16(dst, s16);
+  put16(dst + 2, b16);
+  for (int k = 0; k < 16; ++k) {
+    int qq[2];
+    for (int e = 0; e < 2; ++e) {
+      int qv = 0;
+      if (s != 0.0)
+        qv = static_cast<int>(
+            fmin(15.0, fmax(0.0, round(__ddiv_rn(__dadd_rn(static_cast<double>(src[2 * k + e]), -bias), s)))));
+      qq[e] = qv;
+    }
+    dst[4 + k] = static_cast<uint8_t>(qq[0] | (qq[1] << 4));
+  }
+}
+
+}  // namespace
+
+int launch_quantize(int fmt, const float* w, void* blocks, int N, int K, cudaStream_t stream,
+                    std::string* err) {
+  uint8_t* out = static_cast<uint8_t*>(blocks);
+  const int bw = fmt == FMT_Q4_K ? 256 : 32;
+  const long long nblk = (long long)N * (K / bw);
+  if (nblk == 0) return 0;
+  const int threads = 128;
+  const long long grid = (nblk + threads - 1) / threads;
+  if (fmt == FMT_Q8_0) quant_q8_0_kernel<<<(unsigned)grid, threads, 0, stream>>>(w, out, nblk);
+  else if (fmt == FMT_Q4_K) quant_q4_k_kernel<<<(unsigned)grid, threads, 0, stream>>>(w, out, nblk);
+  else quant_affine4_kernel<<<(unsigned)grid, threads, 0, stream>>>(w, out, nblk);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    *err = std::string("quantize launch: ") + cudaGetErrorString(e);
+    return -1;
+  }
+  return 0;
+}
+
+}  // namespace kq

@@ -1,0 +1,90 @@
+"""The C-ABI library loads and exports every entry point that include/kq.h declares.
+
+Runs without a GPU: only size helpers and argument checks that fail before any
+CUDA call are exercised here.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "kq.h")
+
+
+@pytest.fixture(scope="module")
+def kqlib():
+    from quantized_decode_gemv_block_gb300 import build
+    build.build()
+    import quantized_decode_gemv_block_gb300 as kq
+    return kq
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("kq_gemv", "kq_gemm", "kq_gemm_workspace_size", "kq_quantize", "kq_block_bytes",
+              "kq_block_weights", "kq_row_bytes", "kq_last_error", "kq_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(kqlib):
+    L = ctypes.CDLL(kqlib.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_size_helpers(kqlib):
+    assert (kqlib.block_bytes("q8_0"), kqlib.block_weights("q8_0")) == (34, 32)
+    assert (kqlib.block_bytes("q4_k"), kqlib.block_weights("q4_k")) == (144, 256)
+    assert (kqlib.block_bytes("affine4"), kqlib.block_weights("affine4")) == (20, 32)
+    assert kqlib.block_bytes(99) == 0
+    assert kqlib.row_bytes("q4_k", 2560) == 1440
+    assert kqlib.row_bytes("q8_0", 2048) == 2176
+    assert kqlib.row_bytes("affine4", 2560) == 1600
+    assert kqlib.row_bytes("q4_k", 100) == 0
+    assert "sm_103a" in kqlib.version()
+
+
+def test_argument_errors_before_any_cuda_call(kqlib):
+    L = kqlib.lib()
+    fake = 1 << 20  # never dereferenced: every call below fails validation first
+    cases = [
+        ((7, fake, kqlib.BF16, fake, fake, 1, 8, 256, None), kqlib.KQ_ERR_UNSUPPORTED),
+        ((kqlib.Q4_K, fake, 9, fake, fake, 1, 8, 256, None), kqlib.KQ_ERR_UNSUPPORTED),
+        ((kqlib.Q4_K, fake, kqlib.BF16, fake, fake, 17, 8, 256, None), kqlib.KQ_ERR_ARG),
+        ((kqlib.Q4_K, fake, kqlib.BF16, fake, fake, -1, 8, 256, None), kqlib.KQ_ERR_ARG),
+        ((kqlib.Q4_K, fake, kqlib.BF16, fake, fake, 1, 8, 300, None), kqlib.KQ_ERR_ARG),
+        ((kqlib.Q4_K, None, kqlib.BF16, fake, fake, 1, 8, 256, None), kqlib.KQ_ERR_ARG),
+        ((kqlib.Q4_K, fake, kqlib.BF16, None, fake, 1, 8, 256, None), kqlib.KQ_ERR_ARG),
+        ((kqlib.Q4_K, fake, kqlib.BF16, fake, None, 1, 8, 256, None), kqlib.KQ_ERR_ARG),
+        ((kqlib.Q4_K, fake + 8, kqlib.BF16, fake, fake, 1, 8, 256, None), kqlib.KQ_ERR_ARG),
+        ((kqlib.Q4_K, fake, kqlib.BF16, fake + 4, fake, 1, 8, 256, None), kqlib.KQ_ERR_ARG),
+        ((kqlib.Q4_K, fake, kqlib.BF16, fake, fake + 2, 1, 8, 256, None), kqlib.KQ_ERR_ARG),
+    ]
+    for args, code in cases:
+        assert L.kq_gemv(*args) == code, args
+        assert L.kq_last_error().decode() != ""
+    # empty problems succeed without launching anything
+    assert L.kq_gemv(kqlib.Q4_K, None, kqlib.BF16, None, None, 0, 8, 256, None) == 0
+    assert L.kq_gemv(kqlib.Q4_K, None, kqlib.BF16, None, None, 4, 0, 256, None) == 0
+    assert L.kq_last_error().decode() == ""
+    assert L.kq_quantize(kqlib.Q4_K, fake, fake, 4, 100, None) == kqlib.KQ_ERR_ARG
+    assert L.kq_quantize(5, fake, fake, 4, 256, None) == kqlib.KQ_ERR_UNSUPPORTED
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    import quantized_decode_gemv_block_gb300 as kq
+    with pytest.raises(ImportError):
+        kq._lib, saved = None, kq._lib
+        try:
+            kq.load_library(str(tmp_path / "missing.so"))
+        finally:
+            kq._lib = saved
