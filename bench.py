@@ -1,0 +1,403 @@
+#!/usr/bin/env python3
+"""Benchmark: effective weight-read HBM GB/s of the quantized GEMV / verify path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kq|reference] [--workload NAME]
+
+Prints ONE JSON line (rank 0). Workloads (synthetic data, seeded):
+  ffn      (default) Q4_K GEMV of a Qwen3-4B-like FFN pair: W 9728x2560 and 2560x9728,
+           one bf16 activation row each. One step = both GEMVs.
+  verify   Q4_K speculative-verify GEMM, W 12288x4096, M bf16 rows (--m, default 16).
+  q8_0     Q8_0 GEMV, W 1024x1024, one fp32 row.
+Metric: weight block bytes read per step / step time (GB/s). Inputs: rotating copies of
+the weights totalling >= 4x the L2 size, so every launch streams its weights from HBM.
+K steps are captured in one CUDA graph and replayed; a second replay with an event pair
+around every launch gives the per-launch kernel durations for the roofline.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "effective weight-read HBM GB/s (and % of 8 TB/s) for quantized GEMV at M=1..16"
+FMT_ID = {"q8_0": 1, "q4_k": 2, "affine4": 3}
+
+
+def workload_spec(name: str, m: int):
+    if name == "ffn":
+        return dict(name="q4_k ffn gemv 9728x2560 + 2560x9728, M=1 bf16", fmt="q4_k",
+                    mats=[(9728, 2560), (2560, 9728)], M=1, dtype="bf16")
+    if name == "verify":
+        return dict(name=f"q4_k verify 12288x4096, M={m} bf16", fmt="q4_k", mats=[(12288, 4096)],
+                    M=m, dtype="bf16")
+    if name == "q8_0":
+        return dict(name="q8_0 gemv 1024x1024, M=1 fp32", fmt="q8_0", mats=[(1024, 1024)], M=1,
+                    dtype="f32")
+    raise SystemExit(f"unknown workload {name}")
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = ["quantized_decode_gemv_block_gb300/csrc/gemv_mma.cu",
+                  "quantized_decode_gemv_block_gb300/csrc/kq_device.cuh"]
+
+
+def profile_traffic(profile_name: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", profile_name)
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if "=" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split("=", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256") != source_sha(KERNEL_SOURCES):
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the GPU runs our graphs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.dev)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except FileNotFoundError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax.append(float(p[2]))
+                power.append(float(p[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+def cpu_oracle_gbps(spec, budget_s: float, seed: int = 0):
+    """The fp64 oracle on all host cores, over the same workload's matrices (bounded sample)."""
+    import oracle
+    from quantized_decode_gemv_block_gb300 import inputs
+    f = FMT_ID[spec["fmt"]]
+    mats = []
+    for i, (N, K) in enumerate(spec["mats"]):
+        w = inputs.weights(N, K, seed=seed, tensor_id=i)
+        blocks = oracle.quantize(f, w)
+        xf = inputs.activations_f32(spec["M"], K, seed=seed, tensor_id=1000 + i)
+        x = xf if spec["dtype"] == "f32" else inputs.to_bf16_bits(xf)
+        mats.append((blocks, x, N, K))
+    nbytes = sum(b.nbytes for b, _, _, _ in mats)
+    cores = os.cpu_count() or 1
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        for blocks, x, N, K in mats:
+            oracle.gemv(f, blocks, x, N, K, nthreads=cores)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return nbytes * passes / el / 1e9, cores, passes, el
+
+
+def run_reference(args, spec):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from quantized_decode_gemv_block_gb300 import inputs
+    f = FMT_ID[spec["fmt"]]
+    mats = []
+    for i, (N, K) in enumerate(spec["mats"]):
+        w = inputs.weights(N, K, seed=0, tensor_id=i)
+        blocks = oracle.quantize(f, w)
+        xf = inputs.activations_f32(spec["M"], K, seed=0, tensor_id=1000 + i)
+        x = xf if spec["dtype"] == "f32" else inputs.to_bf16_bits(xf)
+        mats.append((blocks, x, N, K))
+    nbytes = sum(b.nbytes for b, _, _, _ in mats)
+    cores = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        for blocks, x, N, K in mats:
+            oracle.gemv(f, blocks, x, N, K, nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for blocks, x, N, K in mats:
+            oracle.gemv(f, blocks, x, N, K, nthreads=cores)
+    el = time.perf_counter() - t0
+    v = nbytes * args.steps / el / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": spec["name"], "M": spec["M"]},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": f"full workload per step ({nbytes} weight bytes), fp64 scalar oracle, "
+                                       f"OpenMP over output rows"},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="kq", choices=["kq", "reference"])
+    ap.add_argument("--workload", default="ffn", choices=["ffn", "verify", "q8_0"])
+    ap.add_argument("--m", type=int, default=16)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    spec = workload_spec(args.workload, args.m)
+    if args.impl == "reference":
+        run_reference(args, spec)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import quantized_decode_gemv_block_gb300 as kq
+    from quantized_decode_gemv_block_gb300 import build, inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    if rank == 0 or not os.path.exists(kq.LIB_PATH):
+        build.build()
+    if world > 1:
+        dist.barrier()
+    kq.load_library()
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 129 * 2**20) or 129 * 2**20
+
+    # ---- inputs: quantized weights (rotating copies), activations, outputs
+    fmt, M = spec["fmt"], spec["M"]
+    xdt = torch.bfloat16 if spec["dtype"] == "bf16" else torch.float32
+    base = []
+    for i, (N, K) in enumerate(spec["mats"]):
+        w32 = inputs.weights_cuda(N, K, seed=rank, tensor_id=i, device=str(dev))
+        base.append(kq.quantize(fmt, w32))
+        del w32
+    step_bytes = sum(b.numel() for b in base)
+    copies = max(2, math.ceil(4 * l2 / step_bytes))
+    wsets = [[b.clone() for b in base] for _ in range(copies)]
+    xs = [inputs.activations_cuda(M, K, seed=rank, tensor_id=1000 + i, dtype=xdt, device=str(dev))
+          for i, (N, K) in enumerate(spec["mats"])]
+    ys = [torch.empty((M, N), dtype=torch.float32, device=dev) for (N, K) in spec["mats"]]
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def launch_step(s, events=None):
+        ws = wsets[s % copies]
+        for i, (N, K) in enumerate(spec["mats"]):
+            if events is not None:
+                events[s][i][0].record()
+            kq.gemv(fmt, ws[i], xs[i], N, K, y=ys[i])
+            if events is not None:
+                events[s][i][1].record()
+
+    def capture(nsteps, events=None):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            launch_step(0)  # untimed eager launch before capture (lazy init)
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for s in range(nsteps):
+                    launch_step(s, events)
+        return g
+
+    K_ = args.steps
+    g_warm = capture(args.warmup)
+    g_main = capture(K_)
+    def timing_event():
+        # external=True makes a captured record a real timestamp at replay time
+        return torch.cuda.Event(enable_timing=True, external=True)
+
+    ev = [[[timing_event(), timing_event()] for _ in spec["mats"]] for _ in range(K_)]
+    g_inst = capture(K_, ev)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        g_warm.replay()
+    stream.synchronize()
+
+    # ---- timed region: exactly K steps
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record()
+        g_main.replay()
+        t1.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms_total = t0.elapsed_time(t1)
+
+    # ---- per-launch durations (same K steps, event pair around each launch)
+    with torch.cuda.stream(stream):
+        g_inst.replay()
+    torch.cuda.synchronize()
+    durs = [[ev[s][i][0].elapsed_time(ev[s][i][1]) for i in range(len(spec["mats"]))] for s in range(K_)]
+    # keep the GPU busy with the same graph for ~1.5 s more so the clock sampler sees load
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < 1.5:
+        with torch.cuda.stream(stream):
+            g_main.replay()
+        stream.synchronize()
+    clocks = sampler.stop()
+
+    # ---- e2e through the public API with host buffers (H2D of x, D2H of y, every step)
+    xh = [x.cpu().pin_memory() for x in xs]
+    yh = [torch.empty(y.shape, dtype=torch.float32).pin_memory() for y in ys]
+    xd = [torch.empty_like(x) for x in xs]
+    h2d = sum(x.numel() * x.element_size() for x in xh)
+    d2h = sum(y.numel() * 4 for y in yh)
+    e2e_steps = min(K_, 100)
+    for s in range(3):
+        for i, (N, K) in enumerate(spec["mats"]):
+            xd[i].copy_(xh[i], non_blocking=True)
+            kq.gemv(fmt, wsets[s % copies][i], xd[i], N, K, y=ys[i])
+            yh[i].copy_(ys[i], non_blocking=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for s in range(e2e_steps):
+        for i, (N, K) in enumerate(spec["mats"]):
+            xd[i].copy_(xh[i], non_blocking=True)
+            kq.gemv(fmt, wsets[s % copies][i], xd[i], N, K, y=ys[i])
+            yh[i].copy_(ys[i], non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    # ---- reduce over ranks (max time)
+    t = torch.tensor([ms_total, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_total, e2e_ms = float(t[0]), float(t[1])
+    ms_step = ms_total / K_
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+
+    flat = np.array(durs).reshape(K_, -1)
+    launch_ms = float(flat.mean())
+    achieved = step_bytes / len(spec["mats"]) / (launch_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    traffic = profile_traffic(f"gemv_mma_{args.workload}.md")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, passes, el = cpu_oracle_gbps(spec, args.cpu_budget)
+        cpu = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"{passes} passes over the full workload ({step_bytes} weight bytes each) in "
+                         f"{el:.1f} s, fp64 scalar oracle, OpenMP over output rows"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K_,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": spec["dtype"], "data": "synthetic",
+            "config": {"workload": spec["name"], "M": M, "weight_bytes_per_step": step_bytes,
+                       "l2": f"rotating weight copies: {copies} x {step_bytes} B >= 4x L2 ({l2} B)",
+                       "parallelism": "replicas" if world > 1 else "single gpu",
+                       "pct_of_8tbs": value / world / 8000.0},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": f"{peak_kind} hbm_gbs", "kernel": "gemv_mma_kernel",
+                         "launch_us": launch_ms * 1e3},
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "note": "eager kq.gemv calls from Python, pinned-host x in, y out, every step"},
+            "gpu_launches": K_ * len(spec["mats"]),
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -70,6 +70,12 @@ size_t kq_row_bytes(int fmt, int K);
 const char* kq_last_error(void);
 const char* kq_version(void);
 
+/* Reads and clears the device error word of the current device; synchronises the device.
+ * Every wait inside a kernel is bounded: if one gives up, the kernel records bit 0 here,
+ * skips the rest of its work (its output is then invalid) and returns instead of hanging.
+ * Returns the bits (0 = nothing recorded) or KQ_ERR_CUDA if the word cannot be read. */
+int kq_device_errors(void);
+
 /* Quantized GEMV / speculative-verify product (Kinetic README, "What makes it fast").
  *   fmt       KQ_Q8_0, KQ_Q4_K or KQ_AFFINE4_G32
  *   w_blocks  N * kq_row_bytes(fmt, K) bytes, 16-byte aligned
@@ -85,6 +91,20 @@ const char* kq_version(void);
  * Errors: KQ_ERR_ARG, KQ_ERR_UNSUPPORTED, KQ_ERR_CUDA. */
 int kq_gemv(int fmt, const void* w_blocks, int x_dtype, const void* x, float* y, int M, int N,
             int K, void* stream);
+
+/* Flags of kq_gemv_ex. */
+enum kq_flags {
+  /* The kernel launched just before this call on `stream` does not write w_blocks (for
+   * example the previous layer's GEMV). The GEMV may then start streaming its weights
+   * before that kernel finishes (programmatic dependent launch); it still waits for it
+   * before reading x or writing y. Only the tensor-core path (KQ_BF16) uses it. */
+  KQ_OVERLAP_PREVIOUS = 1u
+};
+
+/* kq_gemv with flags (0 gives exactly kq_gemv). Unknown flag bits: KQ_ERR_ARG. Results are
+ * identical with and without KQ_OVERLAP_PREVIOUS. */
+int kq_gemv_ex(int fmt, const void* w_blocks, int x_dtype, const void* x, float* y, int M, int N,
+               int K, unsigned flags, void* stream);
 
 /* Quantized GEMM (Kinetic README, "What makes it fast": long prompts as tiled matrix
  * products, each weight block unpacked once for many tokens).

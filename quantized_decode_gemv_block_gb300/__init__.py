@@ -52,12 +52,15 @@ def load_library(path: str = LIB_PATH):
     L.kq_version.restype = ctypes.c_char_p
     L.kq_gemv.argtypes = [I, P, I, P, P, I, I, I, P]
     L.kq_gemv.restype = I
+    L.kq_gemv_ex.argtypes = [I, P, I, P, P, I, I, I, ctypes.c_uint, P]
+    L.kq_gemv_ex.restype = I
     L.kq_gemm.argtypes = [I, P, I, P, P, I, I, I, P, SZ, P]
     L.kq_gemm.restype = I
     L.kq_gemm_workspace_size.argtypes = [I, I, I, I, I]
     L.kq_gemm_workspace_size.restype = SZ
     L.kq_quantize.argtypes = [I, P, P, I, I, P]
     L.kq_quantize.restype = I
+    L.kq_device_errors.restype = I
     _lib = L
     return L
 
@@ -105,14 +108,25 @@ def _x_dtype(x: torch.Tensor) -> int:
     raise TypeError("x must be torch.bfloat16 or torch.float32")
 
 
+KQ_OVERLAP_PREVIOUS = 1
+
+
 def gemv(fmt, w: torch.Tensor, x: torch.Tensor, N: int, K: int, y: torch.Tensor | None = None,
-         stream=None) -> torch.Tensor:
-    """Y (M x N fp32) = X (M x K) @ deq(W)^T for M <= 16, through kq_gemv."""
+         stream=None, overlap: bool = False) -> torch.Tensor:
+    """Y (M x N fp32) = X (M x K) @ deq(W)^T for M <= 16, through kq_gemv / kq_gemv_ex.
+
+    overlap=True passes KQ_OVERLAP_PREVIOUS: the previous kernel on the stream must not
+    write w (it may still be running while this one streams w)."""
     M = x.shape[0]
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=x.device)
-    _check(lib().kq_gemv(_fmt(fmt), w.data_ptr(), _x_dtype(x), x.data_ptr(), y.data_ptr(), M, N, K,
-                         _stream(stream)))
+    if overlap:
+        rc = lib().kq_gemv_ex(_fmt(fmt), w.data_ptr(), _x_dtype(x), x.data_ptr(), y.data_ptr(), M, N, K,
+                              KQ_OVERLAP_PREVIOUS, _stream(stream))
+    else:
+        rc = lib().kq_gemv(_fmt(fmt), w.data_ptr(), _x_dtype(x), x.data_ptr(), y.data_ptr(), M, N, K,
+                           _stream(stream))
+    _check(rc)
     return y
 
 
@@ -135,6 +149,14 @@ def gemm(fmt, w: torch.Tensor, x: torch.Tensor, N: int, K: int, y: torch.Tensor 
     _check(lib().kq_gemm(_fmt(fmt), w.data_ptr(), _x_dtype(x), x.data_ptr(), y.data_ptr(), M, N, K,
                          wp, wn, _stream(stream)))
     return y
+
+
+def device_errors() -> int:
+    """Read and clear the device error word (bit 0: a bounded in-kernel wait gave up)."""
+    rc = lib().kq_device_errors()
+    if rc < 0:
+        _check(rc)
+    return rc
 
 
 def quantize(fmt, w: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:

@@ -1,0 +1,531 @@
+// Per-format pieces of the tensor-core GEMV: how a warp reads one 256-weight unit of
+// 16 rows (rows g and g+8 per thread), turns the codes into exact bf16 MMA A fragments,
+// and promotes each 32-weight group's fp32 MMA result by its scale and min/bias.
+// Included by gemv_mma.cu only.
+#pragma once
+#include "kq_device.cuh"
+
+namespace kq {
+namespace gemv {
+
+constexpr uint32_t kBf16Magic = 0x43434343u;  // bf16 0x43nn = 128 + nn for nn < 128
+constexpr uint32_t kBf16x2_128 = 0x43004300u;
+
+struct LdGlobal {
+  __device__ static uint4 v128(const void* p) { return ldg128(p); }
+  __device__ static uint2 v64(const void* p) { return ldg64(p); }
+  __device__ static uint32_t v32(const void* p) { return ldg32(p); }
+};
+struct LdShared {  // plain loads: the compiler may combine and schedule them (the stage's
+                  // mbarrier wait carries a memory clobber, so none moves above it)
+  __device__ static uint4 v128(const void* p) { return *static_cast<const uint4*>(p); }
+  __device__ static uint2 v64(const void* p) { return *static_cast<const uint2*>(p); }
+  __device__ static uint32_t v32(const void* p) { return *static_cast<const uint32_t*>(p); }
+};
+// ------------------------------------------------------------------ Q4_K --
+// One unit = one 144-byte super-block. Thread (g, q) of a warp handles rows g and
+// g+8 of the warp's 16 rows; for each 32-byte chunk c of codes it loads the 8 bytes
+// 8q..8q+7, i.e. weights 8q..8q+7 of sub-block 2c (low nibbles) and of sub-block
+// 2c+1 (high nibbles).
+struct FmtQ4K {
+  static constexpr bool kHalfX = false;
+  static constexpr int kUnitBytes = 144;
+  static constexpr bool kPerm0213 = false;
+  static constexpr bool kNeedsSum = true;
+  struct Raw {
+    uint4 h[2];
+    uint2 qs[2][4];
+  };
+  template <class Ld>
+  __device__ static void load(Raw& r, const uint8_t* pa, const uint8_t* pb, int q) {
+    r.h[0] = Ld::v128(pa);
+    r.h[1] = Ld::v128(pb);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      r.qs[0][c] = Ld::v64(pa + 16 + 32 * c + 8 * q);
+      r.qs[1][c] = Ld::v64(pb + 16 + 32 * c + 8 * q);
+    }
+  }
+  // 4-bit codes -> bf16 pairs: slots (2q, 2q+1) <- bytes (0,1), (2q+8, 2q+9) <- bytes (2,3).
+  template <int NT>
+  __device__ static void compute(const Raw& r, float (&acc)[NT][4], const uint16_t* xs_unit,
+                                 int xstride, const float* s_unit, int lane, int M) {
+    constexpr int T = 8 * NT;
+    const int g = lane >> 2, q = lane & 3;
+    uint32_t sc_lo[2], sc_hi[2], m_lo[2], m_hi[2];
+    float d[2], nd[2], dmin[2], pdmin[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint32_t s0 = r.h[i].y, s1 = r.h[i].z, s2 = r.h[i].w;
+      sc_lo[i] = s0 & 0x3F3F3F3Fu;
+      m_lo[i] = s1 & 0x3F3F3F3Fu;
+      sc_hi[i] = (s2 & 0x0F0F0F0Fu) | ((s0 >> 2) & 0x30303030u);
+      m_hi[i] = ((s2 >> 4) & 0x0F0F0F0Fu) | ((s1 >> 2) & 0x30303030u);
+      d[i] = half_bits_to_float(r.h[i].x);
+      dmin[i] = half_bits_to_float(r.h[i].x >> 16);
+      nd[i] = -8388608.f * d[i];
+      pdmin[i] = 8388608.f * dmin[i];
+    }
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const int c = b >> 1;
+      uint32_t a0[4], a1[4];
+      float ds[2], ndm[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint32_t w0 = r.qs[i][c].x, w1 = r.qs[i][c].y;
+        const uint32_t n0 = (b & 1) ? ((w0 >> 4) & 0x0F0F0F0Fu) : (w0 & 0x0F0F0F0Fu);
+        const uint32_t n1 = (b & 1) ? ((w1 >> 4) & 0x0F0F0F0Fu) : (w1 & 0x0F0F0F0Fu);
+        a0[i] = bf16x2_sub(prmt(n0, kBf16Magic, 0x4140u), kBf16x2_128);
+        a0[i + 2] = bf16x2_sub(prmt(n0, kBf16Magic, 0x4342u), kBf16x2_128);
+        a1[i] = bf16x2_sub(prmt(n1, kBf16Magic, 0x4140u), kBf16x2_128);
+        a1[i + 2] = bf16x2_sub(prmt(n1, kBf16Magic, 0x4342u), kBf16x2_128);
+        const uint32_t scw = (b < 4) ? sc_lo[i] : sc_hi[i];
+        const uint32_t mw = (b < 4) ? m_lo[i] : m_hi[i];
+        ds[i] = scaled_byte(scw, b & 3, d[i], nd[i]);          //  d * sc_b (exact)
+        ndm[i] = scaled_byte(mw, b & 3, -dmin[i], pdmin[i]);   // -dmin * m_b (exact)
+      }
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int tok = 8 * t + g;
+        uint4 xb = make_uint4(0u, 0u, 0u, 0u);
+        if (tok < M) xb = lds128(xs_unit + tok * xstride + 32 * b + 8 * q);
+        const float z[4] = {0.f, 0.f, 0.f, 0.f};
+        float p[4];
+        mma_bf16_16816(p, a0, xb.x, xb.y, z);
+        mma_bf16_16816(p, a1, xb.z, xb.w, p);
+        const float2 sv = lds_f2(s_unit + b * T + 8 * t + 2 * q);
+        acc[t][0] = __fmaf_rn(ndm[0], sv.x, __fmaf_rn(ds[0], p[0], acc[t][0]));
+        acc[t][1] = __fmaf_rn(ndm[0], sv.y, __fmaf_rn(ds[0], p[1], acc[t][1]));
+        acc[t][2] = __fmaf_rn(ndm[1], sv.x, __fmaf_rn(ds[1], p[2], acc[t][2]));
+        acc[t][3] = __fmaf_rn(ndm[1], sv.y, __fmaf_rn(ds[1], p[3], acc[t][3]));
+      }
+    }
+  }
+};
+
+// ------------------------------------------------------------------ Q8_0 --
+// One unit = 8 blocks of 34 bytes = 272 bytes, read as 4 pairs of 68 bytes. The
+// even block of a pair starts on a 4-byte boundary (its codes 2 bytes after it),
+// the odd block's codes start on one. Thread q takes codes 8q..8q+7 of each block.
+// The fp16 scale of the even block sits in the first word of thread 0's window
+// and that of the odd block in the last word of thread 3's; they are broadcast in
+// the quad with shuffles.
+struct FmtQ8_0 {
+  static constexpr bool kHalfX = false;
+  static constexpr int kUnitBytes = 272;
+  static constexpr bool kPerm0213 = true;
+  static constexpr bool kNeedsSum = false;
+  struct Raw {
+    uint32_t w[2][4][5];
+  };
+  template <class Ld>
+  __device__ static void load(Raw& r, const uint8_t* pa, const uint8_t* pb, int q) {
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+#pragma unroll
+      for (int k = 0; k < 3; ++k) {
+        r.w[0][p][k] = Ld::v32(pa + 68 * p + 8 * q + 4 * k);
+        r.w[1][p][k] = Ld::v32(pb + 68 * p + 8 * q + 4 * k);
+      }
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        r.w[0][p][3 + k] = Ld::v32(pa + 68 * p + 36 + 8 * q + 4 * k);
+        r.w[1][p][3 + k] = Ld::v32(pb + 68 * p + 36 + 8 * q + 4 * k);
+      }
+    }
+  }
+  // int8 pair (bytes 0 and 2, or 1 and 3) -> exact bf16 pair: (128 + (q & 127)) - (128 or 256).
+  __device__ static uint32_t i8pair(uint32_t v) {
+    return bf16x2_sub(and_or(v, 0x007F007Fu, kBf16x2_128), and_or(v, 0x00800080u, kBf16x2_128));
+  }
+  template <int NT>
+  __device__ static void compute(const Raw& r, float (&acc)[NT][4], const uint16_t* xs_unit,
+                                 int xstride, const float* /*s_unit*/, int lane, int M) {
+    const int g = lane >> 2, q = lane & 3;
+    const int quad = lane & ~3;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+#pragma unroll
+      for (int odd = 0; odd < 2; ++odd) {
+        const int b = 2 * p + odd;
+        uint32_t a0[4], a1[4];
+        float dsc[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          uint32_t c0, c1;
+          if (!odd) {
+            c0 = prmt(r.w[i][p][0], r.w[i][p][1], 0x5432u);
+            c1 = prmt(r.w[i][p][1], r.w[i][p][2], 0x5432u);
+          } else {
+            c0 = r.w[i][p][3];
+            c1 = r.w[i][p][4];
+          }
+          const uint32_t dw = __shfl_sync(0xFFFFFFFFu, odd ? r.w[i][p][2] : r.w[i][p][0],
+                                          quad | (odd ? 3 : 0));
+          dsc[i] = half_bits_to_float(odd ? (dw >> 16) : dw);
+          a0[i] = i8pair(c0);
+          a0[i + 2] = i8pair(c0 >> 8);
+          a1[i] = i8pair(c1);
+          a1[i + 2] = i8pair(c1 >> 8);
+        }
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const int tok = 8 * t + g;
+          uint4 xb = make_uint4(0u, 0u, 0u, 0u);
+          if (tok < M) xb = lds128(xs_unit + tok * xstride + 32 * b + 8 * q);
+          const float z[4] = {0.f, 0.f, 0.f, 0.f};
+          float pr[4];
+          mma_bf16_16816(pr, a0, xb.x, xb.y, z);
+          mma_bf16_16816(pr, a1, xb.z, xb.w, pr);
+          acc[t][0] = __fmaf_rn(dsc[0], pr[0], acc[t][0]);
+          acc[t][1] = __fmaf_rn(dsc[0], pr[1], acc[t][1]);
+          acc[t][2] = __fmaf_rn(dsc[1], pr[2], acc[t][2]);
+          acc[t][3] = __fmaf_rn(dsc[1], pr[3], acc[t][3]);
+        }
+      }
+    }
+  }
+};
+
+// --------------------------------------------------------------- affine4 --
+// One unit = 8 groups of 20 bytes = 160 bytes. Group g: word 0 = (s, b) fp16, then
+// 16 code bytes; thread q takes code bytes 4q..4q+3 (weights 8q..8q+7; even weight in
+// the low nibble).
+struct FmtAffine4 {
+  static constexpr bool kHalfX = false;
+  static constexpr int kUnitBytes = 160;
+  static constexpr bool kPerm0213 = true;
+  static constexpr bool kNeedsSum = true;
+  struct Raw {
+    uint32_t sb[2][8];
+    uint32_t cw[2][8];
+  };
+  template <class Ld>
+  __device__ static void load(Raw& r, const uint8_t* pa, const uint8_t* pb, int q) {
+#pragma unroll
+    for (int gi = 0; gi < 8; ++gi) {
+      r.sb[0][gi] = Ld::v32(pa + 20 * gi);
+      r.sb[1][gi] = Ld::v32(pb + 20 * gi);
+      r.cw[0][gi] = Ld::v32(pa + 20 * gi + 4 + 4 * q);
+      r.cw[1][gi] = Ld::v32(pb + 20 * gi + 4 + 4 * q);
+    }
+  }
+  template <int NT>
+  __device__ static void compute(const Raw& r, float (&acc)[NT][4], const uint16_t* xs_unit,
+                                 int xstride, const float* s_unit, int lane, int M) {
+    constexpr int T = 8 * NT;
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int gi = 0; gi < 8; ++gi) {
+      uint32_t a0[4], a1[4];
+      float s[2], bias[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint32_t cw = r.cw[i][gi];
+        const uint32_t lo = cw & 0x0F0F0F0Fu, hi = (cw >> 4) & 0x0F0F0F0Fu;
+        a0[i] = bf16x2_sub(prmt(lo, kBf16Magic, 0x4140u), kBf16x2_128);      // w0, w2
+        a0[i + 2] = bf16x2_sub(prmt(hi, kBf16Magic, 0x4140u), kBf16x2_128);  // w1, w3
+        a1[i] = bf16x2_sub(prmt(lo, kBf16Magic, 0x4342u), kBf16x2_128);      // w4, w6
+        a1[i + 2] = bf16x2_sub(prmt(hi, kBf16Magic, 0x4342u), kBf16x2_128);  // w5, w7
+        s[i] = half_bits_to_float(r.sb[i][gi]);
+        bias[i] = half_bits_to_float(r.sb[i][gi] >> 16);
+      }
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int tok = 8 * t + g;
+        uint4 xb = make_uint4(0u, 0u, 0u, 0u);
+        if (tok < M) xb = lds128(xs_unit + tok * xstride + 32 * gi + 8 * q);
+        const float z[4] = {0.f, 0.f, 0.f, 0.f};
+        float p[4];
+        mma_bf16_16816(p, a0, xb.x, xb.y, z);
+        mma_bf16_16816(p, a1, xb.z, xb.w, p);
+        const float2 sv = lds_f2(s_unit + gi * T + 8 * t + 2 * q);
+        acc[t][0] = __fmaf_rn(bias[0], sv.x, __fmaf_rn(s[0], p[0], acc[t][0]));
+        acc[t][1] = __fmaf_rn(bias[0], sv.y, __fmaf_rn(s[0], p[1], acc[t][1]));
+        acc[t][2] = __fmaf_rn(bias[1], sv.x, __fmaf_rn(s[1], p[2], acc[t][2]));
+        acc[t][3] = __fmaf_rn(bias[1], sv.y, __fmaf_rn(s[1], p[3], acc[t][3]));
+      }
+    }
+  }
+};
+
+template <int FMT> struct FmtOf;
+template <> struct FmtOf<FMT_Q4_K> { using type = FmtQ4K; };
+template <> struct FmtOf<FMT_Q8_0> { using type = FmtQ8_0; };
+template <> struct FmtOf<FMT_AFFINE4> { using type = FmtAffine4; };
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+
+// ------------------------------------------------------- Q4_K, fp16 path --
+// The streaming kernel's Q4_K variant. Each thread of a quad owns whole sub-blocks:
+// thread q reads the 32 code bytes 32q..32q+31 of its two rows' super-block, i.e. all
+// of sub-block 2q (low nibbles) and sub-block 2q+1 (high nibbles). The 6-bit scale is
+// folded into the fp16 A operand (sc*q <= 945 is exact in fp16), so one MMA may mix
+// the four threads' sub-blocks and the fp32 result needs one promotion by d per
+// super-block. The min term sum_b dmin*m_b*S_b(x) is one more MMA per super-block with
+// A = m_b (exact) and B = S_b/64 split into an fp16 high and low part.
+//
+// The activations are staged as fp16 after an exact per-token power-of-two scale
+// 2^e (max |x| of the CTA's slice lands in [2^14, 2^15)); every bf16 value within a
+// factor 2^28 of that maximum converts exactly. The scale is removed when a partial
+// is emitted (exact power-of-two multiply).
+//
+// MMA m (0..15) of a super-block takes, for thread q, weights 64q + 4m + {0,2 | 1,3}
+// (m < 8, low nibbles of code word m) or 64q + 32 + 4(m-8) + {0,2 | 1,3} (m >= 8,
+// high nibbles of word m-8): slots (2q, 2q+1) get the pair (+0, +2), slots (2q+8,
+// 2q+9) the pair (+1, +3). The staged x of each thread's 64 positions is permuted the
+// same way within groups of four, so B fragments are plain 16-byte loads.
+struct FmtQ4KH {
+  static constexpr bool kHalfX = true;
+  static constexpr bool kPerm0213 = false;
+  static constexpr bool kNeedsSum = false;
+  static constexpr int kUnitBytes = 144;
+  struct Raw {
+    uint4 h[2];
+    uint4 c[2][2];
+  };
+  template <class Ld>
+  __device__ static void load(Raw& r, const uint8_t* pa, const uint8_t* pb, int q) {
+    r.h[0] = Ld::v128(pa);
+    r.h[1] = Ld::v128(pb);
+    r.c[0][0] = Ld::v128(pa + 16 + 32 * q);
+    r.c[0][1] = Ld::v128(pa + 32 + 32 * q);
+    r.c[1][0] = Ld::v128(pb + 16 + 32 * q);
+    r.c[1][1] = Ld::v128(pb + 32 + 32 * q);
+  }
+  // Byte offset, within one token's 512-byte super-block slot, of the 16-byte chunk i
+  // (0..7) of thread q: the quad's four chunks i sit side by side (64 bytes), and tokens
+  // are 64 bytes apart modulo 128, so a quarter-warp's loads hit 32 distinct banks.
+  __device__ static int chunk_off(int q, int i) { return 64 * i + 16 * q; }
+
+  // xh_unit: token 0's slot of this super-block; xts: token stride (bytes).
+  // s2_unit: token 0's min-term operands of this super-block; s2ts: their token stride.
+  // The fp32 sums of one super-block: ps = sum (sc*q)*x per (row, token) and mn = sum m*S/64.
+  // xo[t] / so[t]: byte offsets of this thread's token row in tile t within the staged x
+  // and min-term operands (absent tokens point at the zero row), 16q / 8q included.
+  template <int NT>
+  __device__ static void sums(const Raw& r, const uint8_t* xh_unit, const int (&xo)[NT],
+                              const uint8_t* s2_unit, const int (&so)[NT], int lane,
+                              float (&ps)[NT][4], float (&mnv)[NT][4], float (&d)[2], float (&dmin)[2]) {
+    const int g = lane >> 2, q = lane & 3;
+    const uint32_t kMagic = 0x64006400u;   // fp16 1024 in both halves
+    uint32_t sa[2], nsa[2], sb16[2], nsb64[2], ma[2], mb[2];
+    // Thread q needs sub-blocks j = 2q and 2q+1. For j < 4 (q < 2): sc = scales[j] & 63,
+    // m = scales[j+4] & 63. For j >= 4 (q >= 2): sc = (scales[j+4] & 15) | (scales[j-4] >> 6) << 4,
+    // m = (scales[j+4] >> 4) | (scales[j] >> 6) << 4. One permute gathers, per thread,
+    // bytes (sc_a, sc_b, m_a, m_b) of the low form and one the high-bit sources.
+    const uint32_t ja = static_cast<uint32_t>((2 * q) & 3);
+    // low form: q < 2 -> [s0.ja, s0.ja+1, s1.ja, s1.ja+1]; q >= 2 -> [s2.ja, s2.ja+1, s2.ja, s2.ja+1]
+    const uint32_t sel_lo = q < 2 ? (ja | ((ja + 1) << 4) | ((ja + 4) << 8) | ((ja + 5) << 12))
+                                  : (ja | ((ja + 1) << 4) | (ja << 8) | ((ja + 1) << 12));
+    // high bits (q >= 2): [s0.ja, s0.ja+1, s1.ja, s1.ja+1] >> 6 << 4
+    const uint32_t sel_hi = ja | ((ja + 1) << 4) | ((ja + 4) << 8) | ((ja + 5) << 12);
+    const uint32_t pa_sel = 0x4040u, pb_sel = 0x4141u, pma_sel = 0x4242u, pmb_sel = 0x4343u;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint32_t s0 = r.h[i].y, s1 = r.h[i].z, s2 = r.h[i].w;
+      // bytes: sc_2q, sc_2q+1, m_2q, m_2q+1 (both forms computed, one selected: no branch)
+      const uint32_t v6 = prmt(s0, s1, sel_lo) & 0x3F3F3F3Fu;
+      const uint32_t lo = prmt(s2, s2, sel_lo);
+      const uint32_t hb = (prmt(s0, s1, sel_hi) >> 2) & 0x30303030u;
+      const uint32_t v4 = (((lo & 0x0000FFFFu) | ((lo >> 4) & 0x0F0F0000u)) & 0x0F0F0F0Fu) | hb;
+      const uint32_t v = q < 2 ? v6 : v4;
+      sa[i] = h2_sub(prmt(v, 0x64646464u, pa_sel), kMagic);               // (sc_2q, sc_2q)
+      nsa[i] = h2_mul(sa[i], 0xE400E400u);                                 // -1024 * sc_2q
+      const uint32_t sb = h2_sub(prmt(v, 0x64646464u, pb_sel), kMagic);   // sc_2q+1
+      sb16[i] = h2_mul(sb, 0x2C002C00u);                                   // sc_2q+1 / 16
+      nsb64[i] = h2_mul(sb, 0xD400D400u);                                  // -64 * sc_2q+1
+      ma[i] = h2_sub(prmt(v, 0x64646464u, pma_sel), kMagic);              // (m_2q, m_2q)
+      mb[i] = h2_sub(prmt(v, 0x64646464u, pmb_sel), kMagic);              // (m_2q+1, m_2q+1)
+      d[i] = half_bits_to_float(r.h[i].x);
+      dmin[i] = half_bits_to_float(r.h[i].x >> 16);
+    }
+    // four independent accumulation chains (word parity x low/high nibbles), added in a
+    // fixed order at the end: the MMAs of one super-block overlap instead of queueing
+    float p[NT][4][4];
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) p[t][c][0] = p[t][c][1] = p[t][c][2] = p[t][c][3] = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {  // code word k: MMA k (low nibbles) and MMA 8+k (high nibbles)
+      uint32_t alo[4], ahi[4];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint4 cv = r.c[i][k >> 2];
+        const uint32_t w = (k & 3) == 0 ? cv.x : (k & 3) == 1 ? cv.y : (k & 3) == 2 ? cv.z : cv.w;
+        const uint32_t w8 = w >> 8;
+        alo[i] = h2_fma(and_or(w, 0x000F000Fu, kMagic), sa[i], nsa[i]);
+        alo[i + 2] = h2_fma(and_or(w8, 0x000F000Fu, kMagic), sa[i], nsa[i]);
+        ahi[i] = h2_fma(and_or(w, 0x00F000F0u, kMagic), sb16[i], nsb64[i]);
+        ahi[i + 2] = h2_fma(and_or(w8, 0x00F000F0u, kMagic), sb16[i], nsb64[i]);
+      }
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int tok = 8 * t + g;
+        // chunk i = k/2 holds MMAs 2i, 2i+1 of the low half; chunk 4 + k/2 of the high half
+        const uint8_t* base = xh_unit + xo[t];
+        const uint4 xlo = *reinterpret_cast<const uint4*>(base + 64 * (k >> 1));
+        const uint4 xhi = *reinterpret_cast<const uint4*>(base + 64 * (4 + (k >> 1)));
+        const uint32_t bl0 = (k & 1) ? xlo.z : xlo.x, bl1 = (k & 1) ? xlo.w : xlo.y;
+        const uint32_t bh0 = (k & 1) ? xhi.z : xhi.x, bh1 = (k & 1) ? xhi.w : xhi.y;
+        const int c = 2 * (k & 1);
+        mma_f16_16816(p[t][c], alo, bl0, bl1, p[t][c]);
+        mma_f16_16816(p[t][c + 1], ahi, bh0, bh1, p[t][c + 1]);
+      }
+    }
+    // min term: A2 slots (2q, 2q+1) = m_2q, (2q+8, 2q+9) = m_2q+1; B2 = S/64 hi/lo parts
+    const uint32_t a2[4] = {ma[0], ma[1], mb[0], mb[1]};
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const int tok = 8 * t + g;
+      const uint2 b2 = *reinterpret_cast<const uint2*>(s2_unit + so[t]);
+      const float z[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_f16_16816(mnv[t], a2, b2.x, b2.y, z);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) ps[t][e] = (p[t][0][e] + p[t][1][e]) + (p[t][2][e] + p[t][3][e]);
+    }
+  }
+
+  // acc += d*ps - 64*dmin*mn, rows g (elements 0, 1) and g+8 (elements 2, 3)
+  template <int NT>
+  __device__ static void promote(float (&acc)[NT][4], const float (&ps)[NT][4], const float (&mnv)[NT][4],
+                                 const float (&d)[2], const float (&dmin)[2]) {
+    const float nd0 = -64.f * dmin[0], nd1 = -64.f * dmin[1];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      acc[t][0] = __fmaf_rn(nd0, mnv[t][0], __fmaf_rn(d[0], ps[t][0], acc[t][0]));
+      acc[t][1] = __fmaf_rn(nd0, mnv[t][1], __fmaf_rn(d[0], ps[t][1], acc[t][1]));
+      acc[t][2] = __fmaf_rn(nd1, mnv[t][2], __fmaf_rn(d[1], ps[t][2], acc[t][2]));
+      acc[t][3] = __fmaf_rn(nd1, mnv[t][3], __fmaf_rn(d[1], ps[t][3], acc[t][3]));
+    }
+  }
+
+  template <int NT>
+  __device__ static void compute(const Raw& r, float (&acc)[NT][4], const uint8_t* xh_unit,
+                                 const int (&xo)[NT], const uint8_t* s2_unit, const int (&so)[NT],
+                                 int lane) {
+    float ps[NT][4], mnv[NT][4], d[2], dmin[2];
+    sums<NT>(r, xh_unit, xo, s2_unit, so, lane, ps, mnv, d, dmin);
+    promote<NT>(acc, ps, mnv, d, dmin);
+  }
+
+  // Two consecutive super-blocks (x and min-term operands of the second 512 and 32 bytes
+  // further on); the same arithmetic, in the same order, as two compute() calls.
+  template <int NT>
+  __device__ static void compute2(const Raw& r0, const Raw& r1, float (&acc)[NT][4],
+                                  const uint8_t* xh_unit, const int (&xo)[NT], const uint8_t* s2_unit,
+                                  const int (&so)[NT], int lane) {
+    float ps0[NT][4], mn0[NT][4], d0[2], dm0[2], ps1[NT][4], mn1[NT][4], d1[2], dm1[2];
+    sums<NT>(r0, xh_unit, xo, s2_unit, so, lane, ps0, mn0, d0, dm0);
+    sums<NT>(r1, xh_unit + 512, xo, s2_unit + 32, so, lane, ps1, mn1, d1, dm1);
+    promote<NT>(acc, ps0, mn0, d0, dm0);
+    promote<NT>(acc, ps1, mn1, d1, dm1);
+  }
+};
+
+// Stage the activations of one CTA's K-slice for FmtQ4KH (all threads of the CTA take
+// part; two __syncthreads inside). x: M x K bf16. Slice = units [k0, k0+S).
+// smax/inv: T-entry scratch in shared memory (max |x| bits, then 2^-e per token).
+// Per-token power-of-two scale 2^e with max|x| * 2^e in [2^14, 2^15), from the bits of
+// max|x| (an fp32 pattern); zero, Inf and NaN keep 2^0.
+__device__ __forceinline__ float token_scale(uint32_t mb) {
+  const int E = static_cast<int>(mb >> 23);
+  int e = 0;
+  if (mb != 0u && E < 255) {
+    e = 14 - (E == 0 ? -126 : E - 127);
+    e = max(-126, min(127, e));
+  }
+  return __int_as_float((e + 127) << 23);
+}
+
+// Activation staging for FmtQ4KH in two phases, so the loads of x leave before the
+// weight copies flood the memory system: load() reads this thread's items into
+// registers (and clears the zero row and the maxima); finish() reduces the per-token
+// maxima, converts, stores, and writes the min-term operands. The caller places one
+// __syncthreads between them (and one after finish()).
+// Rows 0..M-1 of the staged x hold the tokens, row M zeros (absent token slots read it).
+template <int NTHREADS>
+struct StageQ4KH {
+  static constexpr int kItems = 5;  // 16 tokens x 10 units x 8 groups / 256 threads
+  uint4 u[kItems][4];
+
+  __device__ void load(const uint16_t* x, int M, int K, int k0, int S, uint8_t* xh, int xts, uint8_t* s2,
+                       int s2ts, unsigned int* smax) {
+    const int items = M * S * 8;
+#pragma unroll
+    for (int it = 0; it < kItems; ++it) {
+      const int idx = threadIdx.x + it * NTHREADS;
+      if (idx < items) {
+        const int tok = idx / (S * 8), grp = idx - tok * (S * 8);
+        const uint16_t* src = x + (long long)tok * K + (long long)k0 * 256 + grp * 32;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) u[it][v] = ldg128(src + 8 * v);
+      }
+    }
+    for (int i = threadIdx.x; i < S * 32; i += NTHREADS)
+      *reinterpret_cast<uint4*>(xh + M * xts + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = threadIdx.x; i < S * 4; i += NTHREADS)
+      *reinterpret_cast<uint2*>(s2 + M * s2ts + 8 * i) = make_uint2(0u, 0u);
+    for (int t = threadIdx.x; t < M; t += NTHREADS) smax[t] = 0u;
+  }
+
+  __device__ void finish(int M, int S, uint8_t* xh, int xts, uint8_t* s2, int s2ts, unsigned int* smax,
+                         float* inv) {
+    const int items = M * S * 8;
+#pragma unroll
+    for (int it = 0; it < kItems; ++it) {
+      const int idx = threadIdx.x + it * NTHREADS;
+      if (idx < items) {
+        const int tok = idx / (S * 8);
+        uint32_t best = 0u;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const uint32_t w4[4] = {u[it][v].x, u[it][v].y, u[it][v].z, u[it][v].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) best = max(best, max((w4[k] & 0x7FFFu) << 16, w4[k] & 0x7FFF0000u));
+        }
+        atomicMax(&smax[tok], best);
+      }
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < M; t += NTHREADS) inv[t] = 1.0f / token_scale(smax[t]);
+#pragma unroll
+    for (int it = 0; it < kItems; ++it) {
+      const int idx = threadIdx.x + it * NTHREADS;
+      if (idx < items) {
+        const int tok = idx / (S * 8), grp = idx - tok * (S * 8);
+        const int ul = grp >> 3, j = grp & 7, q = j >> 1, half = j & 1;
+        const float sc = token_scale(smax[tok]);
+        float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const uint4 w = u[it][v];
+          const float f0 = __uint_as_float(w.x << 16) * sc, f1 = __uint_as_float(w.x & 0xFFFF0000u) * sc;
+          const float f2 = __uint_as_float(w.y << 16) * sc, f3 = __uint_as_float(w.y & 0xFFFF0000u) * sc;
+          const float f4 = __uint_as_float(w.z << 16) * sc, f5 = __uint_as_float(w.z & 0xFFFF0000u) * sc;
+          const float f6 = __uint_as_float(w.w << 16) * sc, f7 = __uint_as_float(w.w & 0xFFFF0000u) * sc;
+          const uint4 o = make_uint4(f2_to_h2(f0, f2), f2_to_h2(f1, f3), f2_to_h2(f4, f6), f2_to_h2(f5, f7));
+          *reinterpret_cast<uint4*>(xh + tok * xts + ul * 512 + FmtQ4KH::chunk_off(q, 4 * half + v)) = o;
+          // the sum of what the MMA will see (the fp16 values), four partial sums in a fixed order
+          const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            a[k] += half_bits_to_float(ow[k]);
+            a[k] += half_bits_to_float(ow[k] >> 16);
+          }
+        }
+        const float hs = ((a[0] + a[1]) + (a[2] + a[3])) * 0.015625f;  // S / 64
+        const uint32_t hh = f2_to_h2(hs, 0.f) & 0xFFFFu;
+        const uint32_t hl = f2_to_h2(hs - h_lo_to_f(hh), 0.f) & 0xFFFFu;
+        *reinterpret_cast<uint32_t*>(s2 + tok * s2ts + ul * 32 + 8 * q + 4 * half) = hh | (hl << 16);
+      }
+    }
+  }
+};
+
+}  // namespace gemv
+}  // namespace kq

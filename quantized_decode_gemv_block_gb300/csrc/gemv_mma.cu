@@ -29,14 +29,19 @@
 // activation loads (absent tokens read as zero) and the stores, and the column
 // tile count (1 or 2) leaves tile 0 unchanged.
 #include <cooperative_groups.h>
+#include <cuda.h>
+
+#include <algorithm>
 
 #include "kq_device.cuh"
 #include "kq_internal.h"
+#include "gemv_formats.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace kq {
 namespace {
+using namespace gemv;
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
@@ -44,8 +49,6 @@ constexpr int kRowsPerCta = 16 * kWarps;
 constexpr int kUnit = 256;       // weights per K-unit (one Q4_K super-block, 8 Q8_0 / affine4 blocks)
 constexpr int kChunkUnits = 8;   // K-units of activations staged in shared memory at a time
 constexpr int kDepth = 2;        // K-units each warp keeps in flight
-constexpr uint32_t kBf16Magic = 0x43434343u;  // bf16 0x43nn = 128 + nn for nn < 128
-constexpr uint32_t kBf16x2_128 = 0x43004300u;
 
 struct Params {
   const uint8_t* w;
@@ -59,244 +62,15 @@ struct Params {
   long long row_bytes;
 };
 
-// ------------------------------------------------------------------ Q4_K --
-// One unit = one 144-byte super-block. Thread (g, q) of a warp handles rows g and
-// g+8 of the warp's 16 rows; for each 32-byte chunk c of codes it loads the 8 bytes
-// 8q..8q+7, i.e. weights 8q..8q+7 of sub-block 2c (low nibbles) and of sub-block
-// 2c+1 (high nibbles).
-struct FmtQ4K {
-  static constexpr int kUnitBytes = 144;
-  static constexpr bool kPerm0213 = false;
-  static constexpr bool kNeedsSum = true;
-  struct Raw {
-    uint4 h[2];
-    uint2 qs[2][4];
-  };
-  __device__ static void load(Raw& r, const uint8_t* pa, const uint8_t* pb, int q) {
-    r.h[0] = ldg128(pa);
-    r.h[1] = ldg128(pb);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      r.qs[0][c] = ldg64(pa + 16 + 32 * c + 8 * q);
-      r.qs[1][c] = ldg64(pb + 16 + 32 * c + 8 * q);
-    }
-  }
-  // 4-bit codes -> bf16 pairs: slots (2q, 2q+1) <- bytes (0,1), (2q+8, 2q+9) <- bytes (2,3).
-  template <int NT>
-  __device__ static void compute(const Raw& r, float (&acc)[NT][4], const uint16_t* xs_unit,
-                                 int xstride, const float* s_unit, int lane, int M) {
-    constexpr int T = 8 * NT;
-    const int g = lane >> 2, q = lane & 3;
-    uint32_t sc_lo[2], sc_hi[2], m_lo[2], m_hi[2];
-    float d[2], nd[2], dmin[2], pdmin[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const uint32_t s0 = r.h[i].y, s1 = r.h[i].z, s2 = r.h[i].w;
-      sc_lo[i] = s0 & 0x3F3F3F3Fu;
-      m_lo[i] = s1 & 0x3F3F3F3Fu;
-      sc_hi[i] = (s2 & 0x0F0F0F0Fu) | ((s0 >> 2) & 0x30303030u);
-      m_hi[i] = ((s2 >> 4) & 0x0F0F0F0Fu) | ((s1 >> 2) & 0x30303030u);
-      d[i] = half_bits_to_float(r.h[i].x);
-      dmin[i] = half_bits_to_float(r.h[i].x >> 16);
-      nd[i] = -8388608.f * d[i];
-      pdmin[i] = 8388608.f * dmin[i];
-    }
-#pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      const int c = b >> 1;
-      uint32_t a0[4], a1[4];
-      float ds[2], ndm[2];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const uint32_t w0 = r.qs[i][c].x, w1 = r.qs[i][c].y;
-        const uint32_t n0 = (b & 1) ? ((w0 >> 4) & 0x0F0F0F0Fu) : (w0 & 0x0F0F0F0Fu);
-        const uint32_t n1 = (b & 1) ? ((w1 >> 4) & 0x0F0F0F0Fu) : (w1 & 0x0F0F0F0Fu);
-        a0[i] = bf16x2_sub(prmt(n0, kBf16Magic, 0x4140u), kBf16x2_128);
-        a0[i + 2] = bf16x2_sub(prmt(n0, kBf16Magic, 0x4342u), kBf16x2_128);
-        a1[i] = bf16x2_sub(prmt(n1, kBf16Magic, 0x4140u), kBf16x2_128);
-        a1[i + 2] = bf16x2_sub(prmt(n1, kBf16Magic, 0x4342u), kBf16x2_128);
-        const uint32_t scw = (b < 4) ? sc_lo[i] : sc_hi[i];
-        const uint32_t mw = (b < 4) ? m_lo[i] : m_hi[i];
-        ds[i] = scaled_byte(scw, b & 3, d[i], nd[i]);          //  d * sc_b (exact)
-        ndm[i] = scaled_byte(mw, b & 3, -dmin[i], pdmin[i]);   // -dmin * m_b (exact)
-      }
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const int tok = 8 * t + g;
-        uint4 xb = make_uint4(0u, 0u, 0u, 0u);
-        if (tok < M) xb = lds128(xs_unit + tok * xstride + 32 * b + 8 * q);
-        const float z[4] = {0.f, 0.f, 0.f, 0.f};
-        float p[4];
-        mma_bf16_16816(p, a0, xb.x, xb.y, z);
-        mma_bf16_16816(p, a1, xb.z, xb.w, p);
-        const float2 sv = lds_f2(s_unit + b * T + 8 * t + 2 * q);
-        acc[t][0] = __fmaf_rn(ndm[0], sv.x, __fmaf_rn(ds[0], p[0], acc[t][0]));
-        acc[t][1] = __fmaf_rn(ndm[0], sv.y, __fmaf_rn(ds[0], p[1], acc[t][1]));
-        acc[t][2] = __fmaf_rn(ndm[1], sv.x, __fmaf_rn(ds[1], p[2], acc[t][2]));
-        acc[t][3] = __fmaf_rn(ndm[1], sv.y, __fmaf_rn(ds[1], p[3], acc[t][3]));
-      }
-    }
-  }
-};
-
-// ------------------------------------------------------------------ Q8_0 --
-// One unit = 8 blocks of 34 bytes = 272 bytes, read as 4 pairs of 68 bytes. The
-// even block of a pair starts on a 4-byte boundary (its codes 2 bytes after it),
-// the odd block's codes start on one. Thread q takes codes 8q..8q+7 of each block.
-// The fp16 scale of the even block sits in the first word of thread 0's window
-// and that of the odd block in the last word of thread 3's; they are broadcast in
-// the quad with shuffles.
-struct FmtQ8_0 {
-  static constexpr int kUnitBytes = 272;
-  static constexpr bool kPerm0213 = true;
-  static constexpr bool kNeedsSum = false;
-  struct Raw {
-    uint32_t w[2][4][5];
-  };
-  __device__ static void load(Raw& r, const uint8_t* pa, const uint8_t* pb, int q) {
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-#pragma unroll
-      for (int k = 0; k < 3; ++k) {
-        r.w[0][p][k] = ldg32(pa + 68 * p + 8 * q + 4 * k);
-        r.w[1][p][k] = ldg32(pb + 68 * p + 8 * q + 4 * k);
-      }
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        r.w[0][p][3 + k] = ldg32(pa + 68 * p + 36 + 8 * q + 4 * k);
-        r.w[1][p][3 + k] = ldg32(pb + 68 * p + 36 + 8 * q + 4 * k);
-      }
-    }
-  }
-  // int8 pair (bytes 0 and 2, or 1 and 3) -> exact bf16 pair: (128 + (q & 127)) - (128 or 256).
-  __device__ static uint32_t i8pair(uint32_t v) {
-    return bf16x2_sub(and_or(v, 0x007F007Fu, kBf16x2_128), and_or(v, 0x00800080u, kBf16x2_128));
-  }
-  template <int NT>
-  __device__ static void compute(const Raw& r, float (&acc)[NT][4], const uint16_t* xs_unit,
-                                 int xstride, const float* /*s_unit*/, int lane, int M) {
-    const int g = lane >> 2, q = lane & 3;
-    const int quad = lane & ~3;
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-#pragma unroll
-      for (int odd = 0; odd < 2; ++odd) {
-        const int b = 2 * p + odd;
-        uint32_t a0[4], a1[4];
-        float dsc[2];
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          uint32_t c0, c1;
-          if (!odd) {
-            c0 = prmt(r.w[i][p][0], r.w[i][p][1], 0x5432u);
-            c1 = prmt(r.w[i][p][1], r.w[i][p][2], 0x5432u);
-          } else {
-            c0 = r.w[i][p][3];
-            c1 = r.w[i][p][4];
-          }
-          const uint32_t dw = __shfl_sync(0xFFFFFFFFu, odd ? r.w[i][p][2] : r.w[i][p][0],
-                                          quad | (odd ? 3 : 0));
-          dsc[i] = half_bits_to_float(odd ? (dw >> 16) : dw);
-          a0[i] = i8pair(c0);
-          a0[i + 2] = i8pair(c0 >> 8);
-          a1[i] = i8pair(c1);
-          a1[i + 2] = i8pair(c1 >> 8);
-        }
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          const int tok = 8 * t + g;
-          uint4 xb = make_uint4(0u, 0u, 0u, 0u);
-          if (tok < M) xb = lds128(xs_unit + tok * xstride + 32 * b + 8 * q);
-          const float z[4] = {0.f, 0.f, 0.f, 0.f};
-          float pr[4];
-          mma_bf16_16816(pr, a0, xb.x, xb.y, z);
-          mma_bf16_16816(pr, a1, xb.z, xb.w, pr);
-          acc[t][0] = __fmaf_rn(dsc[0], pr[0], acc[t][0]);
-          acc[t][1] = __fmaf_rn(dsc[0], pr[1], acc[t][1]);
-          acc[t][2] = __fmaf_rn(dsc[1], pr[2], acc[t][2]);
-          acc[t][3] = __fmaf_rn(dsc[1], pr[3], acc[t][3]);
-        }
-      }
-    }
-  }
-};
-
-// --------------------------------------------------------------- affine4 --
-// One unit = 8 groups of 20 bytes = 160 bytes. Group g: word 0 = (s, b) fp16, then
-// 16 code bytes; thread q takes code bytes 4q..4q+3 (weights 8q..8q+7; even weight in
-// the low nibble).
-struct FmtAffine4 {
-  static constexpr int kUnitBytes = 160;
-  static constexpr bool kPerm0213 = true;
-  static constexpr bool kNeedsSum = true;
-  struct Raw {
-    uint32_t sb[2][8];
-    uint32_t cw[2][8];
-  };
-  __device__ static void load(Raw& r, const uint8_t* pa, const uint8_t* pb, int q) {
-#pragma unroll
-    for (int gi = 0; gi < 8; ++gi) {
-      r.sb[0][gi] = ldg32(pa + 20 * gi);
-      r.sb[1][gi] = ldg32(pb + 20 * gi);
-      r.cw[0][gi] = ldg32(pa + 20 * gi + 4 + 4 * q);
-      r.cw[1][gi] = ldg32(pb + 20 * gi + 4 + 4 * q);
-    }
-  }
-  template <int NT>
-  __device__ static void compute(const Raw& r, float (&acc)[NT][4], const uint16_t* xs_unit,
-                                 int xstride, const float* s_unit, int lane, int M) {
-    constexpr int T = 8 * NT;
-    const int g = lane >> 2, q = lane & 3;
-#pragma unroll
-    for (int gi = 0; gi < 8; ++gi) {
-      uint32_t a0[4], a1[4];
-      float s[2], bias[2];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const uint32_t cw = r.cw[i][gi];
-        const uint32_t lo = cw & 0x0F0F0F0Fu, hi = (cw >> 4) & 0x0F0F0F0Fu;
-        a0[i] = bf16x2_sub(prmt(lo, kBf16Magic, 0x4140u), kBf16x2_128);      // w0, w2
-        a0[i + 2] = bf16x2_sub(prmt(hi, kBf16Magic, 0x4140u), kBf16x2_128);  // w1, w3
-        a1[i] = bf16x2_sub(prmt(lo, kBf16Magic, 0x4342u), kBf16x2_128);      // w4, w6
-        a1[i + 2] = bf16x2_sub(prmt(hi, kBf16Magic, 0x4342u), kBf16x2_128);  // w5, w7
-        s[i] = half_bits_to_float(r.sb[i][gi]);
-        bias[i] = half_bits_to_float(r.sb[i][gi] >> 16);
-      }
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const int tok = 8 * t + g;
-        uint4 xb = make_uint4(0u, 0u, 0u, 0u);
-        if (tok < M) xb = lds128(xs_unit + tok * xstride + 32 * gi + 8 * q);
-        const float z[4] = {0.f, 0.f, 0.f, 0.f};
-        float p[4];
-        mma_bf16_16816(p, a0, xb.x, xb.y, z);
-        mma_bf16_16816(p, a1, xb.z, xb.w, p);
-        const float2 sv = lds_f2(s_unit + gi * T + 8 * t + 2 * q);
-        acc[t][0] = __fmaf_rn(bias[0], sv.x, __fmaf_rn(s[0], p[0], acc[t][0]));
-        acc[t][1] = __fmaf_rn(bias[0], sv.y, __fmaf_rn(s[0], p[1], acc[t][1]));
-        acc[t][2] = __fmaf_rn(bias[1], sv.x, __fmaf_rn(s[1], p[2], acc[t][2]));
-        acc[t][3] = __fmaf_rn(bias[1], sv.y, __fmaf_rn(s[1], p[3], acc[t][3]));
-      }
-    }
-  }
-};
-
-template <int FMT> struct FmtOf;
-template <> struct FmtOf<FMT_Q4_K> { using type = FmtQ4K; };
-template <> struct FmtOf<FMT_Q8_0> { using type = FmtQ8_0; };
-template <> struct FmtOf<FMT_AFFINE4> { using type = FmtAffine4; };
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
 // Stage X[0:M][uc*256 : (uc+nun)*256] into shared memory (B-fragment order) and, when the
 // format has a min or bias term, the fp32 sum of each 32-group of every token.
 template <class F, int T>
-__device__ void stage_x(const Params& p, uint16_t* xs, float* ss, int uc, int nun) {
+__device__ void stage_x(const uint16_t* xg, int M, int K, int xstride, uint16_t* xs, float* ss,
+                        int uc, int nun) {
   const int per_tok = nun * 32;  // 16-byte vectors per token
-  for (int idx = threadIdx.x; idx < p.M * per_tok; idx += kThreads) {
+  for (int idx = threadIdx.x; idx < M * per_tok; idx += kThreads) {
     const int tok = idx / per_tok, v = idx - tok * per_tok;
-    uint4 val = ldg128(p.x + (long long)tok * p.K + (long long)uc * kUnit + v * 8);
+    uint4 val = ldg128(xg + (long long)tok * K + (long long)uc * kUnit + v * 8);
     if (F::kPerm0213) {  // (e0 e1 e2 e3) -> (e0 e2 e1 e3) within each group of four
       const uint4 o = val;
       val.x = prmt(o.x, o.y, 0x5410u);
@@ -304,14 +78,14 @@ __device__ void stage_x(const Params& p, uint16_t* xs, float* ss, int uc, int nu
       val.z = prmt(o.z, o.w, 0x5410u);
       val.w = prmt(o.z, o.w, 0x7632u);
     }
-    *reinterpret_cast<uint4*>(xs + tok * p.xstride + v * 8) = val;
+    *reinterpret_cast<uint4*>(xs + tok * xstride + v * 8) = val;
   }
   if (F::kNeedsSum) {
     for (int idx = threadIdx.x; idx < T * nun * 8; idx += kThreads) {
       const int grp = idx / T, tok = idx - grp * T;
       float s = 0.f;
-      if (tok < p.M) {
-        const uint16_t* src = p.x + (long long)tok * p.K + (long long)uc * kUnit + grp * 32;
+      if (tok < M) {
+        const uint16_t* src = xg + (long long)tok * K + (long long)uc * kUnit + grp * 32;
         float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
@@ -327,10 +101,10 @@ __device__ void stage_x(const Params& p, uint16_t* xs, float* ss, int uc, int nu
 }
 
 template <int FMT, int NT>
-__global__ void __launch_bounds__(kThreads, 2) gemv_mma_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, 2) gemv_chunked_kernel(const Params p) {
   using F = typename FmtOf<FMT>::type;
   constexpr int T = 8 * NT;
-  extern __shared__ __align__(16) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem[];
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
   float* ss = reinterpret_cast<float*>(smem + (size_t)T * p.xstride * 2);
   float* red = ss + p.chunk_units * 8 * T;
@@ -357,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_mma_kernel(const Params p) {
 #pragma unroll
   for (int i = 0; i < kDepth; ++i)
     if (u0 + i < u1)
-      F::load(raw[i], wa + (long long)(u0 + i) * F::kUnitBytes,
+      F::template load<LdGlobal>(raw[i], wa + (long long)(u0 + i) * F::kUnitBytes,
               wb + (long long)(u0 + i) * F::kUnitBytes, q);
 
   int chunk0 = u0;
@@ -369,14 +143,14 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_mma_kernel(const Params p) {
         if ((uu - u0) % p.chunk_units == 0) {  // uniform over the CTA
           chunk0 = uu;
           __syncthreads();
-          stage_x<F, T>(p, xs, ss, uu, min(p.chunk_units, u1 - uu));
+          stage_x<F, T>(p.x, p.M, p.K, p.xstride, xs, ss, uu, min(p.chunk_units, u1 - uu));
           __syncthreads();
         }
         const int ul = uu - chunk0;
         F::template compute<NT>(raw[i], acc, xs + ul * kUnit, p.xstride, ss + ul * 8 * T, lane,
                                 p.M);
         if (uu + kDepth < u1)
-          F::load(raw[i], wa + (long long)(uu + kDepth) * F::kUnitBytes,
+          F::template load<LdGlobal>(raw[i], wa + (long long)(uu + kDepth) * F::kUnitBytes,
                   wb + (long long)(uu + kDepth) * F::kUnitBytes, q);
       }
     }
@@ -424,8 +198,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_mma_kernel(const Params p) {
 }
 
 template <int FMT, int NT>
-int launch_one(const Params& prm, size_t smem, cudaStream_t stream, std::string* err) {
-  auto kern = gemv_mma_kernel<FMT, NT>;
+int launch_chunked(const Params& prm, size_t smem, cudaStream_t stream, std::string* err) {
+  auto kern = gemv_chunked_kernel<FMT, NT>;
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -462,7 +236,499 @@ int launch_one(const Params& prm, size_t smem, cudaStream_t stream, std::string*
   return 0;
 }
 
+
+// ============================================================================
+// Streaming kernel: one CTA per SM, weights brought in by 2-D tensor copies (TMA).
+//
+// The N rows are cut into 16-row tiles and K into 256-weight units. A cluster of C
+// CTAs owns a contiguous range of tiles; CTA rank r owns K-slice r of those tiles.
+// The CTA's (tile, unit) work list, tile-major, is cut into 8 contiguous pieces, one
+// per warp, so every warp streams the same number of units. Each warp keeps a
+// private ring of `depth` stages in shared memory; one stage holds up to `su`
+// consecutive units of one tile for its 16 rows and is filled by ONE tensor copy (a
+// 16-row box, rows past N arriving as zeros) completing on the stage's mbarrier. The
+// whole ring is requested before the activations are staged.
+//
+// A tile whose units one warp covers entirely is finished by that warp. A tile cut
+// between warps leaves one partial per warp, added at the end in warp order (= K
+// order). With C > 1 the CTAs' tile results meet in distributed shared memory and
+// are added in rank order (= K order). Every cut depends on (N, K, SM count) only.
+// ============================================================================
+constexpr int kMaxSliceUnits = 10;     // K-units of activations a CTA stages
+constexpr int kMaxClusterTiles = 32;   // tiles per cluster when partials meet across CTAs
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded waits give up after 2 s
+
+__device__ unsigned int g_device_errors = 0;  // bit 0: a bounded wait gave up
+
+struct TmaParams {
+  const uint16_t* x;
+  float* y;
+  int M, N, K;
+  int units, tiles, C, G;
+  int su, depth, row_stride, unit_bytes, xstride, max_tiles;
+  int off_ss, off_ring, off_bar, off_pb, off_res, off_aux;
+  int xts, s2ts;  // fp16 path: row strides (bytes) of the staged x and min-term operands
+};
+
+template <class F, int NT>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemv_tma_kernel(const __grid_constant__ CUtensorMap tmap, const TmaParams p) {
+  constexpr int T = 8 * NT;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
+  float* ss = reinterpret_cast<float*>(smem + p.off_ss);
+  uint8_t* ring = smem + p.off_ring;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
+  float* pbuf = reinterpret_cast<float*>(smem + p.off_pb);  // [warp][2][16][T]
+  float* res = reinterpret_cast<float*>(smem + p.off_res);  // [tile][16][T], C > 1
+  unsigned int* smax = reinterpret_cast<unsigned int*>(smem + p.off_aux);
+  float* inv = reinterpret_cast<float*>(smem + p.off_aux + 64);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, q = lane & 3;
+  if (threadIdx.x == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap) : "memory");
+  int rank = 0;
+  if (p.C > 1) rank = static_cast<int>(cg::this_cluster().block_rank());
+  // all index math in 32-bit unsigned (every product below stays under 2^31)
+  const unsigned cid = blockIdx.x / static_cast<unsigned>(p.C);
+  const unsigned ug = static_cast<unsigned>(p.G), uc = static_cast<unsigned>(p.C);
+  const int t0 = static_cast<int>(cid * static_cast<unsigned>(p.tiles) / ug);
+  const int t1 = static_cast<int>((cid + 1u) * static_cast<unsigned>(p.tiles) / ug);
+  const int k0 = static_cast<int>(static_cast<unsigned>(rank) * static_cast<unsigned>(p.units) / uc);
+  const int k1 = static_cast<int>(static_cast<unsigned>(rank + 1) * static_cast<unsigned>(p.units) / uc);
+  const int S = k1 - k0;
+  const int nt = t1 - t0;
+  const int ltot = nt * S;
+  const int l0 = warp * ltot / kWarps, l1 = (warp + 1) * ltot / kWarps;
+
+  // Barriers first: their release fence would otherwise wait for the activation loads.
+  uint8_t* myring = ring + (size_t)warp * p.depth * 16 * p.row_stride;
+  uint64_t* mybar = bars + warp * p.depth;
+  if (lane == 0) {
+    for (int s = 0; s < p.depth; ++s) mbar_init(&mybar[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  // Programmatic dependent launch: a following launch may begin now (it still waits for
+  // this grid to finish before it reads anything this grid writes).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  // Producer (lane 0): stage sequence over [l0, l1), never crossing a tile boundary.
+  const int fdiv = S > 0 ? S : 1;
+  int lp = l0, ptl = l0 / fdiv, pul = l0 - ptl * S;
+  const uint32_t stage_bytes = 16u * static_cast<uint32_t>(p.row_stride);
+  const int ucol = p.unit_bytes / 4;  // tensor map elements are 4-byte words
+  auto issue = [&](int slot) {
+    const int nu = min(p.su, min(l1 - lp, S - pul));
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&mybar[slot], stage_bytes);
+      tma_load_2d(myring + (size_t)slot * 16 * p.row_stride, &tmap, (k0 + pul) * ucol,
+                  (t0 + ptl) * 16, &mybar[slot]);
+    }
+    lp += nu;
+    pul += nu;
+    if (pul == S) { pul = 0; ++ptl; }
+  };
+  for (int s = 0; s < p.depth && lp < l1; ++s) issue(s);
+
+  // The weights may stream before the previous grid in the stream has finished (when this
+  // launch was allowed to overlap it); the activations it produced may not: wait here.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  [[maybe_unused]] StageQ4KH<kThreads> stq;
+  if constexpr (F::kHalfX) {
+    if (S > 0) stq.load(p.x, p.M, p.K, k0, S, smem, p.xts, smem + p.off_ss, p.s2ts, smax);
+  }
+
+  // This warp's first and last tile, and whether each is partial (kept for the combine).
+  int* meta = reinterpret_cast<int*>(smem + p.off_aux + 128);  // [warp][4]
+  const int w_first = l0 / fdiv, w_last = l1 > l0 ? (l1 - 1) / fdiv : -1;
+  if (lane == 0) {
+    meta[warp * 4 + 0] = l1 > l0 ? w_first : -1;
+    meta[warp * 4 + 1] = w_last;
+    meta[warp * 4 + 2] = (l1 > l0) && !(w_first * S >= l0 && (w_first + 1) * S <= l1);  // first partial
+    meta[warp * 4 + 3] = (l1 > l0) && !(w_last * S >= l0 && (w_last + 1) * S <= l1);    // last partial
+  }
+
+  int xo[NT], so[NT];  // this thread's token rows in the staged activations (fp16 path)
+  if constexpr (F::kHalfX) {
+    __syncthreads();
+    if (S > 0) stq.finish(p.M, S, smem, p.xts, smem + p.off_ss, p.s2ts, smax, inv);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const int tok = 8 * t + g, row = tok < p.M ? tok : p.M;
+      xo[t] = row * p.xts + 16 * q;
+      so[t] = row * p.s2ts + 8 * q;
+    }
+  } else {
+    if (S > 0) stage_x<F, T>(p.x, p.M, p.K, p.xstride, xs, ss, k0, S);
+  }
+  __syncthreads();
+
+  float acc[NT][4];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+
+  // a finished CTA partial of local tile tl (fp16 path: still in 2^e-scaled units)
+  auto emit = [&](int tl, float (&a)[NT][4]) {
+    if constexpr (F::kHalfX) {
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int j0 = 8 * t + 2 * q;
+        const float i0 = j0 < p.M ? inv[j0] : 0.f, i1 = j0 + 1 < p.M ? inv[j0 + 1] : 0.f;
+        a[t][0] *= i0;
+        a[t][1] *= i1;
+        a[t][2] *= i0;
+        a[t][3] *= i1;
+      }
+    }
+    if (p.C == 1) {
+      const int na = (t0 + tl) * 16 + g, nb = na + 8;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int j0 = 8 * t + 2 * q;
+        if (j0 < p.M) {
+          if (na < p.N) p.y[(long long)j0 * p.N + na] = a[t][0];
+          if (nb < p.N) p.y[(long long)j0 * p.N + nb] = a[t][2];
+        }
+        if (j0 + 1 < p.M) {
+          if (na < p.N) p.y[(long long)(j0 + 1) * p.N + na] = a[t][1];
+          if (nb < p.N) p.y[(long long)(j0 + 1) * p.N + nb] = a[t][3];
+        }
+      }
+    } else {
+      float* r = res + (size_t)tl * 16 * T;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int j0 = 8 * t + 2 * q;
+        r[g * T + j0] = a[t][0];
+        r[g * T + j0 + 1] = a[t][1];
+        r[(g + 8) * T + j0] = a[t][2];
+        r[(g + 8) * T + j0 + 1] = a[t][3];
+      }
+    }
+  };
+
+  bool ok = true;
+  int lc = l0, stage = 0, ctl = w_first, cul = l0 - w_first * S;
+  while (lc < l1) {
+    const int tl = ctl, ul = cul;
+    const int nu = min(p.su, min(l1 - lc, S - ul));
+    const int slot = stage % p.depth;
+    const uint32_t parity = static_cast<uint32_t>(stage / p.depth) & 1u;
+    if (ok && !mbar_wait_bounded(&mybar[slot], parity, kWaitLimitNs)) {
+      ok = false;
+      if (lane == 0) atomicOr(&g_device_errors, 1u);
+    }
+    if (ok) {
+      const uint8_t* sa = myring + ((size_t)slot * 16 + g) * p.row_stride;
+      const uint8_t* sb = sa + (size_t)8 * p.row_stride;
+      int i = 0;
+      if constexpr (F::kHalfX) {
+        // two super-blocks per step: independent MMA chains the scheduler can interleave
+        for (; i + 1 < nu; i += 2) {
+          typename F::Raw r0, r1;
+          F::template load<LdShared>(r0, sa + i * p.unit_bytes, sb + i * p.unit_bytes, q);
+          F::template load<LdShared>(r1, sa + (i + 1) * p.unit_bytes, sb + (i + 1) * p.unit_bytes, q);
+          F::template compute2<NT>(r0, r1, acc, smem + (ul + i) * 512, xo,
+                                   smem + p.off_ss + (ul + i) * 32, so, lane);
+        }
+      }
+      for (; i < nu; ++i) {
+        typename F::Raw raw;
+        F::template load<LdShared>(raw, sa + i * p.unit_bytes, sb + i * p.unit_bytes, q);
+        if constexpr (F::kHalfX)
+          F::template compute<NT>(raw, acc, smem + (ul + i) * 512, xo, smem + p.off_ss + (ul + i) * 32,
+                                  so, lane);
+        else
+          F::template compute<NT>(raw, acc, xs + (ul + i) * kUnit, p.xstride, ss + (ul + i) * 8 * T,
+                                  lane, p.M);
+      }
+    }
+    __syncwarp();
+    lc += nu;
+    cul += nu;
+    ++stage;
+    if (lc == l1 || cul == S) {  // leaving tile tl
+      const bool whole = tl * S >= l0 && (tl + 1) * S <= l1;
+      if (whole) {
+        emit(tl, acc);
+      } else {
+        float* pb = pbuf + ((size_t)(warp * 2 + (tl == w_first ? 0 : 1)) * 16) * T;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const int j0 = 8 * t + 2 * q;
+          pb[g * T + j0] = acc[t][0];
+          pb[g * T + j0 + 1] = acc[t][1];
+          pb[(g + 8) * T + j0] = acc[t][2];
+          pb[(g + 8) * T + j0 + 1] = acc[t][3];
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+    }
+    if (cul == S) { cul = 0; ++ctl; }
+    if (ok && lp < l1) {
+      fence_proxy_async_smem();
+      issue(slot);
+    }
+  }
+  if (!ok) {  // let this warp's copies in flight land before the CTA can exit
+    for (int s2 = stage; s2 < stage + p.depth; ++s2)
+      mbar_wait_bounded(&mybar[s2 % p.depth], static_cast<uint32_t>(s2 / p.depth) & 1u, kWaitLimitNs);
+  }
+  __syncthreads();
+
+  // Tiles cut between warps. A cut tile's last unit lies in exactly one warp's range, and
+  // for that warp the tile is its first tile and a partial one: that warp adds the
+  // partials of every warp touching the tile, in warp order (empty warps skipped).
+  if (l1 > l0 && meta[warp * 4 + 2] && (w_first + 1) * S <= l1) {
+    const int t = w_first;
+    int wa = warp;
+    for (int ww = warp - 1; ww >= 0; --ww) {
+      if (meta[ww * 4 + 0] < 0) continue;  // empty range
+      if (meta[ww * 4 + 1] != t) break;
+      wa = ww;
+    }
+    for (int e = lane; e < 16 * p.M; e += 32) {
+      const int row = e / p.M, tok = e - row * p.M;
+      float v = 0.f;
+      for (int ww = wa; ww <= warp; ++ww) {
+        if (meta[ww * 4 + 0] < 0) continue;
+        const int slot = meta[ww * 4 + 0] == t ? 0 : 1;
+        v += pbuf[((size_t)(ww * 2 + slot) * 16 + row) * T + tok];
+      }
+      if constexpr (F::kHalfX) v *= inv[tok];
+      if (p.C == 1) {
+        const int n = (t0 + t) * 16 + row;
+        if (n < p.N) p.y[(long long)tok * p.N + n] = v;
+      } else {
+        res[((size_t)t * 16 + row) * T + tok] = v;
+      }
+    }
+  }
+  if (p.C == 1) return;
+
+  // K-split across the cluster: add the ranks' tile results in rank order.
+  cg::cluster_group cluster = cg::this_cluster();
+  __syncthreads();
+  cluster.sync();
+  const int total = nt * 16 * p.M;
+  const int e0 = (int)((long long)rank * total / p.C), e1 = (int)((long long)(rank + 1) * total / p.C);
+  for (int e = e0 + threadIdx.x; e < e1; e += kThreads) {
+    const int tok = e % p.M, rt = e / p.M;  // rt = tile * 16 + row
+    float v = 0.f;
+    for (int r = 0; r < p.C; ++r) v += cluster.map_shared_rank(res, r)[(size_t)rt * T + tok];
+    const int n = t0 * 16 + rt;
+    if (n < p.N) p.y[(long long)tok * p.N + n] = v;
+  }
+  cluster.sync();
+}
+
+template <class F, int NT>
+int launch_tma(const CUtensorMap& tm, const TmaParams& prm, size_t smem, int grid, cudaStream_t stream,
+               bool overlap, std::string* err) {
+  auto kern = gemv_tma_kernel<F, NT>;
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemCap);
+    if (e != cudaSuccess) {
+      *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
+      return -1;
+    }
+    attr_done[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (prm.C > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = prm.C;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (overlap) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tm, prm);
+  if (e != cudaSuccess) {
+    *err = std::string("gemv (stream) launch: ") + cudaGetErrorString(e);
+    return -1;
+  }
+  return 0;
+}
+
+int unit_bytes_of(int fmt) { return fmt == FMT_Q4_K ? 144 : (fmt == FMT_Q8_0 ? 272 : 160); }
+// Units per stage: one tensor copy brings 16 rows of >= 544 bytes each (row-strided copies
+// below ~576 bytes per row measured well under the HBM rate).
+int stage_units_of(int fmt) { return fmt == FMT_Q8_0 ? 2 : 4; }
+
+// Shared-memory layout of the streaming kernel for a plan and M tokens. The stage is the
+// largest (units per row) that leaves a ring of >= 2 stages per warp. A row of a stage is
+// `row_stride` bytes: the units plus a pad that puts consecutive rows in distinct banks
+// for the fragment loads (the box reads the pad bytes from the next unit, or zeros past
+// the end of the row). Returns false if nothing fits.
+bool tma_layout(int fmt, const TmaPlan& pl, int M, TmaParams* prm, size_t* smem) {
+  auto al = [](size_t v) { return (v + 127) & ~size_t(127); };
+  const int T = M > 8 ? 16 : 8;
+  const int ub = unit_bytes_of(fmt);
+  const bool half_x = fmt == FMT_Q4_K;
+  const int smax = (pl.units + pl.C - 1) / pl.C;
+  int xstride = 0, xts = 0, s2ts = 0;
+  size_t xbytes = 0, sbytes = 0;
+  if (half_x) {  // M token rows + one zero row
+    xts = smax * 512 + 64;
+    s2ts = 32 * ((smax & 1) ? smax : smax + 1);
+    xbytes = (size_t)(M + 1) * xts;
+    sbytes = (size_t)(M + 1) * s2ts;
+  } else {
+    xstride = smax * kUnit + 32;
+    xbytes = (size_t)T * xstride * 2;
+    sbytes = (size_t)smax * 8 * T * 4;
+  }
+  size_t off = al(xbytes);
+  const size_t off_ss = off;
+  off = al(off + sbytes);
+  const size_t off_aux = off;
+  off = al(off + 64 + 64 + 128);
+  const size_t off_pb = off;
+  off = al(off + (size_t)kWarps * 2 * 16 * T * 4);
+  const size_t off_res = off;
+  if (pl.C > 1) off = al(off + (size_t)pl.max_tiles * 16 * T * 4);
+  const size_t off_bar = off;
+  off = al(off + (size_t)kWarps * 8 * 8);
+  const size_t off_ring = off;
+  for (int su = stage_units_of(fmt); su >= 1; --su) {
+    int stride = su * ub;
+    if (half_x) {  // quad loads of 16 bytes at 16 + 32q: rows must differ by 16 mod 32 bytes
+      while (stride % 32 != 16) stride += 16;
+    } else {       // 8-byte loads of 4 rows per phase: rows must differ by 32 or 96 mod 128
+      while (stride % 128 != 32 && stride % 128 != 96) stride += 16;
+    }
+    if (stride / 4 > 256) continue;  // tensor-map box limit (256 elements)
+    const size_t per_stage = (size_t)kWarps * 16 * stride;
+    if (off + 2 * per_stage > (size_t)kSmemCap) continue;
+    const int depth = (int)std::min<size_t>(8, ((size_t)kSmemCap - off) / per_stage);
+    prm->su = su;
+    prm->depth = depth;
+    prm->row_stride = stride;
+    prm->unit_bytes = ub;
+    prm->xstride = xstride;
+    prm->xts = xts;
+    prm->s2ts = s2ts;
+    prm->off_ss = (int)off_ss;
+    prm->off_aux = (int)off_aux;
+    prm->off_pb = (int)off_pb;
+    prm->off_res = (int)off_res;
+    prm->off_bar = (int)off_bar;
+    prm->off_ring = (int)off_ring;
+    *smem = off + (size_t)depth * per_stage;
+    return true;
+  }
+  return false;
+}
+
+// Max co-resident clusters of C CTAs for the streaming kernel of `fmt` at `smem` bytes of
+// shared memory per CTA. Cached per device, format and C. Returns 0 if the query fails.
+int max_clusters(int fmt, int C, size_t smem) {
+  static int cache[64][4][5];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return 0;
+  int ci = 0;
+  while ((1 << ci) < C) ++ci;
+  int& slot = cache[dev][fmt & 3][ci];
+  if (slot > 0) return slot;
+  const void* fn = nullptr;
+  if (fmt == FMT_Q4_K) fn = (const void*)gemv_tma_kernel<FmtQ4KH, 2>;
+  else if (fmt == FMT_Q8_0) fn = (const void*)gemv_tma_kernel<FmtQ8_0, 2>;
+  else fn = (const void*)gemv_tma_kernel<FmtAffine4, 2>;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemCap) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  slot = n;
+  return n;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
+            cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
 }  // namespace
+
+TmaPlan plan_gemv_tma(int fmt, int N, int K, int num_sms) {
+  TmaPlan best;
+  best.ok = false;
+  const int U = K / kUnit, tiles = (N + 15) / 16;
+  long long best_work = -1;
+  for (int C = 1; C <= 8; C *= 2) {
+    if (C > U) break;
+    const int smax = (U + C - 1) / C;
+    if (smax > kMaxSliceUnits) continue;
+    // every launch of this kernel holds more than half an SM's shared memory, so the
+    // co-resident cluster count depends on C only; query it at the full allowance
+    int G = max_clusters(fmt, C, (size_t)kSmemCap);
+    if (G <= 0) G = num_sms / C;
+    if (G <= 0) break;
+    if (G > tiles) G = tiles;
+    const int ntmax = (tiles + G - 1) / G;
+    if (C > 1 && ntmax > kMaxClusterTiles) continue;
+    TmaPlan pl;
+    pl.ok = true;
+    pl.units = U;
+    pl.tiles = tiles;
+    pl.C = C;
+    pl.G = G;
+    pl.max_tiles = ntmax;
+    TmaParams tmp;
+    size_t sm16 = 0;
+    if (!tma_layout(fmt, pl, 16, &tmp, &sm16)) continue;  // must fit for every M
+    const long long work = ((long long)ntmax * smax + kWarps - 1) / kWarps;
+    if (best_work < 0 || work < best_work) {
+      best = pl;
+      best_work = work;
+    }
+  }
+  return best;
+}
 
 GemvPlan plan_gemv_mma(int N, int K, int num_sms) {
   GemvPlan pl;
@@ -486,7 +752,56 @@ size_t gemv_mma_smem(const GemvPlan& pl, int M) {
 }
 
 int launch_gemv_mma(int fmt, const void* w, const void* x, float* y, int M, int N, int K,
-                    long long row_bytes, int num_sms, cudaStream_t stream, std::string* err) {
+                    long long row_bytes, int num_sms, cudaStream_t stream, bool overlap, std::string* err) {
+  const bool two = M > 8;
+  const TmaPlan tp = plan_gemv_tma(fmt, N, K, num_sms);
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (tp.ok && enc) {
+    TmaParams prm;
+    prm.x = static_cast<const uint16_t*>(x);
+    prm.y = y;
+    prm.M = M;
+    prm.N = N;
+    prm.K = K;
+    prm.units = tp.units;
+    prm.tiles = tp.tiles;
+    prm.C = tp.C;
+    prm.G = tp.G;
+    prm.max_tiles = tp.max_tiles;
+    size_t smem = 0;
+    if (!tma_layout(fmt, tp, M, &prm, &smem)) {
+      *err = "internal: streaming plan does not fit shared memory";
+      return -1;
+    }
+    // W as a 2-D tensor of 4-byte words: rows of row_bytes, box = 16 rows x row_stride bytes
+    CUtensorMap tm;
+    const cuuint64_t gdim[2] = {(cuuint64_t)(row_bytes / 4), (cuuint64_t)N};
+    const cuuint64_t gstride[1] = {(cuuint64_t)row_bytes};
+    const cuuint32_t box[2] = {(cuuint32_t)(prm.row_stride / 4), 16u};
+    const cuuint32_t estride[2] = {1u, 1u};
+    const CUresult cr = enc(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(w), gdim, gstride, box,
+                            estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) {
+      *err = "cuTensorMapEncodeTiled failed (" + std::to_string((int)cr) + ")";
+      return -1;
+    }
+    const int grid = tp.G * tp.C;
+    switch (fmt) {
+      case FMT_Q4_K:
+        return two ? launch_tma<FmtQ4KH, 2>(tm, prm, smem, grid, stream, overlap, err)
+                   : launch_tma<FmtQ4KH, 1>(tm, prm, smem, grid, stream, overlap, err);
+      case FMT_Q8_0:
+        return two ? launch_tma<FmtQ8_0, 2>(tm, prm, smem, grid, stream, overlap, err)
+                   : launch_tma<FmtQ8_0, 1>(tm, prm, smem, grid, stream, overlap, err);
+      case FMT_AFFINE4:
+        return two ? launch_tma<FmtAffine4, 2>(tm, prm, smem, grid, stream, overlap, err)
+                   : launch_tma<FmtAffine4, 1>(tm, prm, smem, grid, stream, overlap, err);
+    }
+    *err = "unsupported format";
+    return -1;
+  }
+  // K too long for one CTA's activation slice: register-streaming kernel with chunked staging.
   const GemvPlan pl = plan_gemv_mma(N, K, num_sms);
   Params prm;
   prm.w = static_cast<const uint8_t*>(w);
@@ -501,20 +816,30 @@ int launch_gemv_mma(int fmt, const void* w, const void* x, float* y, int M, int 
   prm.xstride = pl.chunk_units * kUnit + 32;
   prm.row_bytes = row_bytes;
   const size_t smem = gemv_mma_smem(pl, M);
-  const bool two = M > 8;
   switch (fmt) {
     case FMT_Q4_K:
-      return two ? launch_one<FMT_Q4_K, 2>(prm, smem, stream, err)
-                 : launch_one<FMT_Q4_K, 1>(prm, smem, stream, err);
+      return two ? launch_chunked<FMT_Q4_K, 2>(prm, smem, stream, err)
+                 : launch_chunked<FMT_Q4_K, 1>(prm, smem, stream, err);
     case FMT_Q8_0:
-      return two ? launch_one<FMT_Q8_0, 2>(prm, smem, stream, err)
-                 : launch_one<FMT_Q8_0, 1>(prm, smem, stream, err);
+      return two ? launch_chunked<FMT_Q8_0, 2>(prm, smem, stream, err)
+                 : launch_chunked<FMT_Q8_0, 1>(prm, smem, stream, err);
     case FMT_AFFINE4:
-      return two ? launch_one<FMT_AFFINE4, 2>(prm, smem, stream, err)
-                 : launch_one<FMT_AFFINE4, 1>(prm, smem, stream, err);
+      return two ? launch_chunked<FMT_AFFINE4, 2>(prm, smem, stream, err)
+                 : launch_chunked<FMT_AFFINE4, 1>(prm, smem, stream, err);
   }
   *err = "unsupported format";
   return -1;
+}
+
+unsigned int take_device_errors(std::string* err) {
+  unsigned int v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_errors, sizeof(v));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_device_errors, &zero, sizeof(zero));
+  if (e != cudaSuccess) {
+    *err = std::string("reading the device error word: ") + cudaGetErrorString(e);
+    return 0xFFFFFFFFu;
+  }
+  return v;
 }
 
 }  // namespace kq

@@ -4,7 +4,7 @@
 #include <cstdio>
 #include <string>
 
-#include "../../include/kq.h"
+#include "kq.h"
 #include "kq_internal.h"
 
 namespace {
@@ -63,7 +63,9 @@ int check_common(int fmt, const void* w, int x_dtype, const void* x, const float
 }
 
 int gemv_impl(int fmt, const void* w, int x_dtype, const void* x, float* y, int M, int N, int K,
-              cudaStream_t s) {
+              cudaStream_t s, unsigned flags = 0) {
+  if (flags & ~static_cast<unsigned>(KQ_OVERLAP_PREVIOUS))
+    return fail(KQ_ERR_ARG, "unknown flag bits " + std::to_string(flags));
   if (M > 16) return fail(KQ_ERR_ARG, "kq_gemv takes M <= 16 token rows, got " + std::to_string(M));
   int rc = check_common(fmt, w, x_dtype, x, y, M, N, K);
   if (rc != KQ_OK) return rc;
@@ -78,7 +80,8 @@ int gemv_impl(int fmt, const void* w, int x_dtype, const void* x, float* y, int 
   if (x_dtype == KQ_BF16) {
     const int sms = sm_count(&err);
     if (sms < 0) return fail(KQ_ERR_CUDA, err);
-    if (kq::launch_gemv_mma(fmt, w, x, y, M, N, K, row_bytes, sms, s, &err) != 0)
+    if (kq::launch_gemv_mma(fmt, w, x, y, M, N, K, row_bytes, sms, s, (flags & KQ_OVERLAP_PREVIOUS) != 0,
+                            &err) != 0)
       return fail(KQ_ERR_CUDA, err);
   } else {
     if (kq::launch_gemv_f32(fmt, w, static_cast<const float*>(x), y, M, N, K, row_bytes, s, &err) != 0)
@@ -119,9 +122,24 @@ const char* kq_last_error(void) { return g_err.c_str(); }
 
 const char* kq_version(void) { return "kq 0.1.0 (sm_103a)"; }
 
+int kq_device_errors(void) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail(KQ_ERR_CUDA, std::string("cudaDeviceSynchronize: ") + cudaGetErrorString(e));
+  std::string err;
+  const unsigned int v = kq::take_device_errors(&err);
+  if (v == 0xFFFFFFFFu) return fail(KQ_ERR_CUDA, err);
+  ok();
+  return static_cast<int>(v & 0x7FFFFFFFu);
+}
+
 int kq_gemv(int fmt, const void* w_blocks, int x_dtype, const void* x, float* y, int M, int N,
             int K, void* stream) {
   return gemv_impl(fmt, w_blocks, x_dtype, x, y, M, N, K, static_cast<cudaStream_t>(stream));
+}
+
+int kq_gemv_ex(int fmt, const void* w_blocks, int x_dtype, const void* x, float* y, int M, int N,
+               int K, unsigned flags, void* stream) {
+  return gemv_impl(fmt, w_blocks, x_dtype, x, y, M, N, K, static_cast<cudaStream_t>(stream), flags);
 }
 
 size_t kq_gemm_workspace_size(int fmt, int x_dtype, int M, int N, int K) {

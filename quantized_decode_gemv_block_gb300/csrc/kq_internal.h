@@ -7,6 +7,7 @@
 namespace kq {
 
 constexpr int kMaxGemvSmem = 96 * 1024;
+constexpr int kSmemCap = 227 * 1024;  // opt-in shared memory per CTA on sm_103a
 
 struct GemvPlan {
   int units = 0;        // K / 256
@@ -17,11 +18,26 @@ struct GemvPlan {
 
 // Work split of the tensor-core GEMV: a function of (N, K, SM count) only.
 GemvPlan plan_gemv_mma(int N, int K, int num_sms);
+
+// Work split of the streaming (bulk-copy) GEMV; ok == false when K is too long for it.
+struct TmaPlan {
+  bool ok = false;
+  int units = 0, tiles = 0;  // K / 256, ceil(N / 16)
+  int C = 1;                 // CTAs per cluster = K-split
+  int G = 0;                 // clusters
+  int max_tiles = 0;         // tiles per cluster (upper bound)
+};
+TmaPlan plan_gemv_tma(int fmt, int N, int K, int num_sms);
+
+// Reads and clears the device error word (bit 0: a bounded wait in a kernel gave up).
+unsigned int take_device_errors(std::string* err);
 size_t gemv_mma_smem(const GemvPlan& pl, int M);
 
 // bf16 activations, tensor-core path. Returns 0 or -1 with *err set.
+// overlap: launch with programmatic stream serialization (the caller guarantees the
+// previous kernel in the stream does not write w).
 int launch_gemv_mma(int fmt, const void* w, const void* x, float* y, int M, int N, int K,
-                    long long row_bytes, int num_sms, cudaStream_t stream, std::string* err);
+                    long long row_bytes, int num_sms, cudaStream_t stream, bool overlap, std::string* err);
 
 // fp32 activations, CUDA-core path.
 int launch_gemv_f32(int fmt, const void* w, const float* x, float* y, int M, int N, int K,

@@ -75,7 +75,7 @@ def test_quantizer_bytes_match_oracle(kq, orc, fmt):
 
 
 # ------------------------------------------------------------------ gemv --
-SHAPES = [(1, 256), (37, 512), (300, 2560), (1000, 1024), (129, 4096)]
+SHAPES = [(1, 256), (37, 512), (300, 2560), (1000, 1024), (129, 4096), (700, 3072), (90, 20736)]
 
 
 @pytest.mark.parametrize("fmt", list(FMTS))
@@ -154,6 +154,10 @@ def test_nan_scale_stays_in_its_row(kq, orc, dtype):
     assert_close(np.delete(y, 11, axis=1), np.delete(yref, 11, axis=1), np.delete(ay, 11, axis=1))
 
 
+def test_no_device_errors_recorded(kq):
+    assert kq.device_errors() == 0
+
+
 def test_errors_reported(kq):
     w = torch.zeros(1024, dtype=torch.uint8, device="cuda")
     x = torch.zeros((17, 256), dtype=torch.bfloat16, device="cuda")
@@ -201,3 +205,46 @@ def test_full_q4_k_ffn_gemv(kq, orc, N, K):
 
 def test_full_q4_k_verify_12288x4096(kq, orc):
     sampled_check(kq, orc, 2, "q4_k", 12288, 4096, [1, 2, 4, 8, 16], "bf16", seed=0)
+
+
+def test_overlap_flag_gives_identical_results_in_a_chain(kq, orc):
+    """KQ_OVERLAP_PREVIOUS (programmatic dependent launch): a chain of GEMVs where each reads
+    the previous one's output gives the same bits as the plain chain, and matches the oracle."""
+    dims = [2048, 3072, 1024, 2048]
+    blocks = [orc.quantize(2, inputs.weights(dims[i + 1], dims[i], seed=40 + i, tensor_id=2))
+              for i in range(len(dims) - 1)]
+    wd = [dev(b) for b in blocks]
+    x0 = make_x(4, dims[0], "bf16", seed=41)
+
+    def chain(overlap):
+        x = x_tensor(x0, "bf16")
+        outs = []
+        for i, w in enumerate(wd):
+            y = kq.gemv("q4_k", w, x, dims[i + 1], dims[i], overlap=overlap)
+            outs.append(y)
+            x = y.to(torch.bfloat16)
+        torch.cuda.synchronize()
+        return [o.cpu().numpy() for o in outs]
+
+    plain, over = chain(False), chain(True)
+    for a, b in zip(plain, over):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    # the first link against the oracle
+    yref, ay = orc.gemv(2, blocks[0], x0, dims[1], dims[0])
+    assert_close(over[0].astype(np.float64), yref, ay, "chain link 0")
+    # back-to-back GEMVs on the same input with overlap, in a CUDA graph
+    x = x_tensor(x0, "bf16")
+    ys = [torch.empty((4, dims[1]), device="cuda") for _ in range(6)]
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        kq.gemv("q4_k", wd[0], x, dims[1], dims[0], y=ys[0], overlap=True)
+        s.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            for y in ys:
+                kq.gemv("q4_k", wd[0], x, dims[1], dims[0], y=y, overlap=True)
+    g.replay()
+    torch.cuda.synchronize()
+    for y in ys:
+        assert np.array_equal(y.cpu().numpy().view(np.uint32), plain[0].view(np.uint32))
+    assert kq.device_errors() == 0
