@@ -45,6 +45,9 @@ def workload_spec(name: str, m: int):
     if name == "q8_0":
         return dict(name="q8_0 gemv 1024x1024, M=1 fp32", fmt="q8_0", mats=[(1024, 1024)], M=1,
                     dtype="f32")
+    if name == "head":
+        return dict(name=f"q8_0 lm head 151936x2048, M={m} bf16", fmt="q8_0", mats=[(151936, 2048)],
+                    M=m, dtype="bf16")
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -67,6 +70,7 @@ def source_sha(files):
 
 
 KERNEL_SOURCES = ["quantized_decode_gemv_block_gb300/csrc/gemv_mma.cu",
+                  "quantized_decode_gemv_block_gb300/csrc/gemv_formats.cuh",
                   "quantized_decode_gemv_block_gb300/csrc/kq_device.cuh"]
 
 
@@ -211,7 +215,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="kq", choices=["kq", "reference"])
-    ap.add_argument("--workload", default="ffn", choices=["ffn", "verify", "q8_0"])
+    ap.add_argument("--workload", default="ffn", choices=["ffn", "verify", "q8_0", "head"])
     ap.add_argument("--m", type=int, default=16)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -266,7 +270,9 @@ def main():
         for i, (N, K) in enumerate(spec["mats"]):
             if events is not None:
                 events[s][i][0].record()
-            kq.gemv(fmt, ws[i], xs[i], N, K, y=ys[i])
+            # weights are never written inside the step: each launch may stream its
+            # weights while the previous one finishes (programmatic dependent launch)
+            kq.gemv(fmt, ws[i], xs[i], N, K, y=ys[i], overlap=(spec["dtype"] == "bf16"))
             if events is not None:
                 events[s][i][1].record()
 
@@ -364,7 +370,7 @@ def main():
     launch_ms = float(flat.mean())
     achieved = step_bytes / len(spec["mats"]) / (launch_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
-    traffic = profile_traffic(f"gemv_mma_{args.workload}.md")
+    traffic = profile_traffic(f"gemv_tma_{args.workload}.md")
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -384,7 +390,7 @@ def main():
                        "pct_of_8tbs": value / world / 8000.0},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": f"{peak_kind} hbm_gbs", "kernel": "gemv_mma_kernel",
+                         "peak_source": f"{peak_kind} hbm_gbs", "kernel": "gemv_tma_kernel" if spec["dtype"] == "bf16" else "gemv_f32_kernel",
                          "launch_us": launch_ms * 1e3},
             "cpu_baseline": cpu,
             "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
