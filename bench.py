@@ -45,6 +45,9 @@ def workload_spec(name: str, m: int):
     if name == "q8_0":
         return dict(name="q8_0 gemv 1024x1024, M=1 fp32", fmt="q8_0", mats=[(1024, 1024)], M=1,
                     dtype="f32")
+    if name == "decode":
+        return dict(name=f"decode step dense 28 layers hidden 2048 ffn 6144 vocab 151936, M={m}",
+                    fmt="q4_k", mats=[], M=m, dtype="bf16", decode=True)
     if name == "head":
         return dict(name=f"q8_0 lm head 151936x2048, M={m} bf16", fmt="q8_0", mats=[(151936, 2048)],
                     M=m, dtype="bf16")
@@ -209,13 +212,149 @@ def run_reference(args, spec):
     print(json.dumps(line), flush=True)
 
 
+def run_decode(args, spec):
+    """The dense 28-layer decode step (kq_decode_step) as one CUDA graph, replayed K times."""
+    import torch
+    import torch.distributed as dist
+
+    import quantized_decode_gemv_block_gb300 as kq
+    from quantized_decode_gemv_block_gb300 import build
+    from quantized_decode_gemv_block_gb300 import decode as kqd
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    if rank == 0 or not os.path.exists(kq.LIB_PATH):
+        build.build()
+    if world > 1:
+        dist.barrier()
+    kq.load_library()
+    dev = torch.device("cuda", local)
+    M = spec["M"]
+    d = kqd.DENSE_28L
+    model = kqd.random_model(d, seed=rank, device=str(dev))
+    wbytes = kqd.weight_bytes(model)
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 129 * 2**20) or 129 * 2**20
+    g = kqd.GraphStep(model, M)
+    g.x.copy_(torch.randn((M, d["hidden"]), device=dev).to(torch.bfloat16))
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(g.stream):
+        t0.record()
+    for _ in range(args.steps):
+        g.replay()
+    with torch.cuda.stream(g.stream):
+        t1.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms_step = t0.elapsed_time(t1) / args.steps
+    # roofline: every GEMV of the step once, an event pair around each launch
+    mats = []
+    for lay in model.layers:
+        for (nm, N, K), w in zip(kqd.matrix_shapes(d), lay):
+            mats.append((d["layer_fmt"], w, N, K))
+    mats.append((d["head_fmt"], model.head, d["vocab"], d["hidden"]))
+    xs_ = {K: torch.randn((M, K), device=dev).to(torch.bfloat16) for (_, _, _, K) in mats}
+    yout = torch.empty((M, d["vocab"]), device=dev)
+    ev = [(torch.cuda.Event(enable_timing=True, external=True),
+           torch.cuda.Event(enable_timing=True, external=True)) for _ in mats]
+    gi = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(g.stream):
+        for (fmt, w, N, K) in mats:  # untimed eager pass: lazy set-up
+            kq.gemv(fmt, w, xs_[K], N, K, y=yout[:, :N])
+        g.stream.synchronize()
+        with torch.cuda.graph(gi, stream=g.stream):
+            for (fmt, w, N, K), (a, b) in zip(mats, ev):
+                a.record()
+                kq.gemv(fmt, w, xs_[K], N, K, y=yout[:, :N])
+                b.record()
+    for _ in range(2):
+        with torch.cuda.stream(g.stream):
+            gi.replay()
+        torch.cuda.synchronize()
+    gemv_ms = sum(a.elapsed_time(b) for a, b in ev)
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < 1.0:
+        g.replay()
+        torch.cuda.synchronize()
+    clocks = sampler.stop()
+    # e2e: pinned host x in, logits out, every step, through the graph of the public step
+    xh = g.x.cpu().pin_memory()
+    lh = torch.empty(g.logits.shape, dtype=torch.float32).pin_memory()
+    n_e2e = min(args.steps, 50)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(g.stream):
+        e0.record()
+        for _ in range(n_e2e):
+            g.x.copy_(xh, non_blocking=True)
+            g.graph.replay()
+            lh.copy_(g.logits, non_blocking=True)
+        e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    t = torch.tensor([ms_step, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_step, e2e_ms = float(t[0]), float(t[1])
+    peak, peak_kind = measured_peaks()
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, passes, el = cpu_oracle_gbps(
+            dict(fmt="q4_k", mats=[(N, K) for _, N, K in kqd.matrix_shapes(d)], M=M, dtype="bf16"),
+            args.cpu_budget)
+        cpu = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"{passes} passes over one layer's four Q4_K matrices (fp64 scalar oracle GEMV, "
+                         f"OpenMP over rows, M={M}) in {el:.1f} s"}
+    if rank == 0:
+        value = world * wbytes / (ms_step * 1e-3) / 1e9
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": spec["name"], "M": M, "weight_bytes_per_step": wbytes,
+                       "tokens_per_s_equivalent": world * M / (ms_step * 1e-3),
+                       "l2": f"weights per step {wbytes} B > 4x L2 ({l2} B): every step streams from HBM",
+                       "launches_per_step": 8 * d["n_layers"] + 2,
+                       "parallelism": "replicas" if world > 1 else "single gpu",
+                       "pct_of_8tbs": value / world / 8000.0},
+            "roofline": {"bound": "hbm", "achieved": wbytes / (gemv_ms * 1e-3) / 1e9, "peak": peak,
+                         "unit": "GB/s", "frac": wbytes / (gemv_ms * 1e-3) / 1e9 / peak, "traffic": None,
+                         "peak_source": f"{peak_kind} hbm_gbs", "kernel": "gemv_tma_kernel (all GEMVs of one step)",
+                         "gemv_ms_per_step_isolated": gemv_ms},
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * wbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": xh.numel() * 2, "d2h_bytes_per_step": lh.numel() * 4,
+                    "note": "pinned-host x copied in, graph of kq_decode_step, logits copied out, every step"},
+            "gpu_launches": args.steps * (8 * d["n_layers"] + 2),
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="kq", choices=["kq", "reference"])
-    ap.add_argument("--workload", default="ffn", choices=["ffn", "verify", "q8_0", "head"])
+    ap.add_argument("--workload", default="ffn", choices=["ffn", "verify", "q8_0", "head", "decode"])
     ap.add_argument("--m", type=int, default=16)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -223,7 +362,12 @@ def main():
     args.warmup = max(args.warmup, 3)
     spec = workload_spec(args.workload, args.m)
     if args.impl == "reference":
+        if spec.get("decode"):
+            spec = dict(spec, fmt="q4_k", mats=[(3072, 2048), (2048, 2048), (12288, 2048), (2048, 6144)])
         run_reference(args, spec)
+        return
+    if spec.get("decode"):
+        run_decode(args, spec)
         return
 
     import torch

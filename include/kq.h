@@ -132,6 +132,47 @@ size_t kq_gemm_workspace_size(int fmt, int x_dtype, int M, int N, int K);
  * Errors: KQ_ERR_ARG, KQ_ERR_CUDA. */
 int kq_quantize(int fmt, const float* w, void* w_blocks, int N, int K, void* stream);
 
+/* ---- Decode step (composition of the GEMVs; Kinetic README, "What makes it fast": a
+ * decode step is hundreds of small kernels replayed with one launch per token, and a
+ * dense model reads all of its weights once per token). ----
+ * Per layer: x = RMSNorm(h); [q k v] = x Wqkv^T; attention stand-in: each token attends
+ * only to itself (a context of one), so query head hq outputs v of kv head
+ * hq / (q_dim/kv_dim); h += o Wo^T with o that expanded v; x = RMSNorm(h);
+ * [g u] = x Wgu^T; h += (silu(g) * u) Wd^T. Then logits = RMSNorm(h) Whead^T.
+ * RMSNorm has unit weight: x = h / sqrt(mean(h^2) + rms_eps). Every GEMV input is rounded
+ * to bf16 (nearest even); h and every GEMV output are fp32. Rows are independent, so a
+ * token's logits are bit-identical for every M.
+ * Weight matrices (device memory, rows of blocks as for kq_gemv):
+ *   w_qkv[l]     (q_dim + 2*kv_dim) x hidden   rows q, then k, then v
+ *   w_o[l]       hidden x q_dim
+ *   w_gate_up[l] (2*ffn) x hidden              rows gate, then up
+ *   w_down[l]    hidden x ffn
+ *   w_head       vocab x hidden
+ * The struct and the four pointer arrays live in HOST memory; the pointers in them are
+ * device pointers. hidden, q_dim and ffn are multiples of 256. */
+typedef struct kq_decode_model {
+  int n_layers, hidden, q_dim, kv_dim, head_dim, ffn, vocab;
+  int layer_fmt; /* format of every layer matrix */
+  int head_fmt;  /* format of w_head */
+  float rms_eps;
+  const void* const* w_qkv;
+  const void* const* w_o;
+  const void* const* w_gate_up;
+  const void* const* w_down;
+  const void* w_head;
+} kq_decode_model;
+
+/* Device workspace bytes kq_decode_step needs for M tokens (0 on invalid arguments). */
+size_t kq_decode_workspace_size(const kq_decode_model* model, int M);
+
+/* One decode step for M (1..16) token rows: x = M x hidden bf16 (device), logits =
+ * M x vocab fp32 (device, overwritten). workspace: >= kq_decode_workspace_size bytes of
+ * device memory, 256-byte aligned, owned by the caller (the library allocates nothing).
+ * Asynchronous on stream; can be captured in a CUDA graph. Errors: KQ_ERR_ARG,
+ * KQ_ERR_UNSUPPORTED, KQ_ERR_WORKSPACE, KQ_ERR_CUDA. */
+int kq_decode_step(const kq_decode_model* model, const void* x, float* logits, int M, void* workspace,
+                   size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

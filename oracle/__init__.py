@@ -56,11 +56,11 @@ def lib():
         L.orc_dequant.argtypes = [I, P, I64, I64, P]
         L.orc_gemv.argtypes = [I, P, I, P, I64, I64, I64, P, P, I]
         L.orc_gemv_sampled.argtypes = [I, P, I, P, I64, I64, I64, I64, P, P, P, P, I]
-        if hasattr(L, "orc_decode_step"):
-            L.orc_decode_step.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I64, I64, I64,
-                                          ctypes.c_double, P, P, I]
-            L.orc_rmsnorm.argtypes = [P, P, I64, I64, ctypes.c_double, P]
-            L.orc_swiglu.argtypes = [P, P, I64, P]
+        L.orc_double_to_bf16_rn.argtypes = [ctypes.c_double]
+        L.orc_double_to_bf16_rn.restype = ctypes.c_uint16
+        L.orc_rmsnorm.argtypes = [P, P, I64, I64, ctypes.c_double]
+        L.orc_decode_step.argtypes = [I, I, I, I, I, I, I, I, I, ctypes.c_double, P, P, P, P, P, P, I64,
+                                      P, I, P]
         _lib = L
     return _lib
 
@@ -161,3 +161,41 @@ def gemv_sampled(fmt: int, blocks: np.ndarray, x: np.ndarray, N: int, K: int, js
     if rc != 0:
         raise ValueError(f"orc_gemv_sampled: bad arguments ({rc})")
     return y, ay
+
+
+def double_to_bf16_rn(v: float) -> int:
+    return lib().orc_double_to_bf16_rn(v)
+
+
+def rmsnorm_bf16(h: np.ndarray, eps: float) -> np.ndarray:
+    """bf16 bits of h / sqrt(mean(h^2) + eps), row by row (fp64 arithmetic)."""
+    h = np.ascontiguousarray(h, dtype=np.float64)
+    M, D = h.shape
+    out = np.empty((M, D), dtype=np.uint16)
+    lib().orc_rmsnorm(_ptr(h), _ptr(out), M, D, eps)
+    return out
+
+
+def decode_step(dims: dict, layers: list, head: np.ndarray, x_bf16: np.ndarray, nthreads: int = 0,
+                return_head_input: bool = False):
+    """Logits (M x vocab, fp64) of one decode step (definition in decode.cpp); optionally
+    also the head's input (bf16 bits of the final RMSNorm).
+
+    dims: n_layers, hidden, q_dim, kv_dim, head_dim, ffn, vocab, layer_fmt, head_fmt, eps.
+    layers: per layer (w_qkv, w_o, w_gate_up, w_down) blocks (uint8 arrays); head: blocks."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    M = x.shape[0]
+    keep = [np.ascontiguousarray(a, dtype=np.uint8) for lay in layers for a in lay]
+    ptrs = [[keep[4 * l + i].ctypes.data for l in range(len(layers))] for i in range(4)]
+    arrs = [(ctypes.c_void_p * max(1, len(layers)))(*p) for p in ptrs]
+    headb = np.ascontiguousarray(head, dtype=np.uint8)
+    out = np.empty((M, dims["vocab"]), dtype=np.float64)
+    xf = np.empty((M, dims["hidden"]), dtype=np.uint16)
+    nt = nthreads or os.cpu_count() or 1
+    rc = lib().orc_decode_step(dims["n_layers"], dims["hidden"], dims["q_dim"], dims["kv_dim"],
+                               dims["head_dim"], dims["ffn"], dims["vocab"], dims["layer_fmt"],
+                               dims["head_fmt"], dims["eps"], *[ctypes.cast(a, ctypes.c_void_p) for a in arrs],
+                               _ptr(headb), _ptr(x), M, _ptr(out), nt, _ptr(xf))
+    if rc != 0:
+        raise ValueError("orc_decode_step failed")
+    return (out, xf) if return_head_input else out

@@ -29,6 +29,16 @@ class KQError(RuntimeError):
         self.code = code
 
 
+class DecodeModelC(ctypes.Structure):
+    """Mirror of kq_decode_model (include/kq.h)."""
+    _fields_ = [("n_layers", ctypes.c_int), ("hidden", ctypes.c_int), ("q_dim", ctypes.c_int),
+                ("kv_dim", ctypes.c_int), ("head_dim", ctypes.c_int), ("ffn", ctypes.c_int),
+                ("vocab", ctypes.c_int), ("layer_fmt", ctypes.c_int), ("head_fmt", ctypes.c_int),
+                ("rms_eps", ctypes.c_float), ("w_qkv", ctypes.POINTER(ctypes.c_void_p)),
+                ("w_o", ctypes.POINTER(ctypes.c_void_p)), ("w_gate_up", ctypes.POINTER(ctypes.c_void_p)),
+                ("w_down", ctypes.POINTER(ctypes.c_void_p)), ("w_head", ctypes.c_void_p)]
+
+
 _lib = None
 
 
@@ -61,6 +71,10 @@ def load_library(path: str = LIB_PATH):
     L.kq_quantize.argtypes = [I, P, P, I, I, P]
     L.kq_quantize.restype = I
     L.kq_device_errors.restype = I
+    L.kq_decode_workspace_size.argtypes = [ctypes.POINTER(DecodeModelC), I]
+    L.kq_decode_workspace_size.restype = SZ
+    L.kq_decode_step.argtypes = [ctypes.POINTER(DecodeModelC), P, P, I, P, SZ, P]
+    L.kq_decode_step.restype = I
     _lib = L
     return L
 
@@ -166,3 +180,36 @@ def quantize(fmt, w: torch.Tensor, out: torch.Tensor | None = None, stream=None)
         out = torch.empty((N, row_bytes(fmt, K)), dtype=torch.uint8, device=w.device)
     _check(lib().kq_quantize(_fmt(fmt), w.data_ptr(), out.data_ptr(), N, K, _stream(stream)))
     return out
+
+
+class DecodeModel:
+    """A dense decoder whose weights are block-quantized device tensors (kq_decode_step).
+
+    layers: list of (w_qkv, w_o, w_gate_up, w_down) uint8 CUDA tensors; head: uint8 CUDA tensor.
+    The model struct and pointer arrays are kept alive by this object."""
+
+    def __init__(self, n_layers, hidden, q_dim, kv_dim, head_dim, ffn, vocab, layers, head,
+                 layer_fmt="q4_k", head_fmt="q8_0", eps=1e-6):
+        self.layers, self.head = layers, head
+        n = max(1, n_layers)
+        self._arrs = [(ctypes.c_void_p * n)(*[lay[i].data_ptr() for lay in layers]) for i in range(4)]
+        self.c = DecodeModelC(n_layers, hidden, q_dim, kv_dim, head_dim, ffn, vocab, _fmt(layer_fmt),
+                              _fmt(head_fmt), eps,
+                              *[ctypes.cast(a, ctypes.POINTER(ctypes.c_void_p)) for a in self._arrs],
+                              head.data_ptr())
+        self.hidden, self.vocab = hidden, vocab
+
+    def workspace_size(self, M: int) -> int:
+        return lib().kq_decode_workspace_size(ctypes.byref(self.c), M)
+
+    def step(self, x: torch.Tensor, logits: torch.Tensor | None = None,
+             workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """logits (M x vocab fp32) for M bf16 token rows x (M x hidden)."""
+        M = x.shape[0]
+        if logits is None:
+            logits = torch.empty((M, self.vocab), dtype=torch.float32, device=x.device)
+        if workspace is None:
+            workspace = torch.empty(self.workspace_size(M), dtype=torch.uint8, device=x.device)
+        _check(lib().kq_decode_step(ctypes.byref(self.c), x.data_ptr(), logits.data_ptr(), M,
+                                    workspace.data_ptr(), workspace.numel(), _stream(stream)))
+        return logits

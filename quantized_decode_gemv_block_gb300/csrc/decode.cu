@@ -1,0 +1,215 @@
+// Decode step of a dense transformer on block-quantized weights (the composition of the
+// GEMVs; Kinetic README, "What makes it fast": a decode step is hundreds of small kernels,
+// recorded once and replayed with one launch per token; all of a dense model's weights
+// are read once per token).
+//
+// Model (per layer): x = RMSNorm(h) -> [q k v] = x Wqkv^T -> attention stand-in (each row
+// attends only to itself, so the output of head hq is v of kv head hq / (n_q / n_kv)) ->
+// h += o Wo^T -> x = RMSNorm(h) -> [g u] = x Wgu^T -> a = silu(g) * u -> h += a Wd^T.
+// Then logits = RMSNorm(h) Whead^T. RMSNorm has unit weight. Activations entering a GEMV
+// are rounded to bf16 (round to nearest even); the residual stream h and every GEMV
+// output stay fp32.
+//
+// Every kernel here takes part in programmatic dependent launch: it lets the next launch
+// begin at once and waits for the previous grid before touching what that grid wrote.
+// The GEMVs are launched with KQ_OVERLAP_PREVIOUS (no kernel of the step writes weights),
+// so each one streams its weights while the glue before it still runs.
+#include <cuda_bf16.h>
+
+#include <vector>
+
+#include "kq.h"
+#include "kq_device.cuh"
+#include "kq_internal.h"
+
+namespace kq {
+namespace {
+
+constexpr int kGlueThreads = 256;
+
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ uint16_t f2bf(float v) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+// Fixed-order block sum (same tree for every launch): warp butterflies, then warp 0.
+__device__ float block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    v = lane < (kGlueThreads / 32) ? red[lane] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    if (lane == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float r = red[0];
+  __syncthreads();
+  return r;
+}
+
+// h[j] = x[j] (bf16 -> fp32) if x != null; then, if add != null, h[j] += add[j]; then
+// out[j] = bf16(h[j] / sqrt(mean(h[j]^2) + eps)). One CTA per token.
+__global__ void __launch_bounds__(kGlueThreads) add_rmsnorm_kernel(float* __restrict__ h,
+                                                                   const uint16_t* __restrict__ x,
+                                                                   const float* __restrict__ add,
+                                                                   uint16_t* __restrict__ out, int D,
+                                                                   float eps) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float red[kGlueThreads / 32];
+  const int j = blockIdx.x;
+  float* hj = h + (long long)j * D;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < D; i += kGlueThreads) {
+    float v = x ? __uint_as_float((uint32_t)x[(long long)j * D + i] << 16) : hj[i];
+    if (add) v = v + add[(long long)j * D + i];
+    hj[i] = v;
+    ss = __fmaf_rn(v, v, ss);
+  }
+  const float tot = block_sum(ss, red);
+  const float inv = 1.0f / sqrtf(tot / (float)D + eps);
+  for (int i = threadIdx.x; i < D; i += kGlueThreads) out[(long long)j * D + i] = f2bf(hj[i] * inv);
+}
+
+// out[j][hq*hd + d] = bf16(qkv[j][q_dim + kv_dim + (hq / group)*hd + d]): the attention
+// stand-in with a context of one token (softmax weight 1 on the token's own value).
+__global__ void __launch_bounds__(kGlueThreads) gqa_expand_kernel(const float* __restrict__ qkv,
+                                                                  uint16_t* __restrict__ out, int M,
+                                                                  int q_dim, int kv_dim, int hd,
+                                                                  int group) {
+  pdl_trigger();
+  pdl_wait();
+  const int qkv_dim = q_dim + 2 * kv_dim;
+  const long long total = (long long)M * q_dim;
+  for (long long e = blockIdx.x * (long long)kGlueThreads + threadIdx.x; e < total;
+       e += (long long)gridDim.x * kGlueThreads) {
+    const int j = (int)(e / q_dim), c = (int)(e - (long long)j * q_dim);
+    const int hq = c / hd, d = c - hq * hd;
+    out[e] = f2bf(qkv[(long long)j * qkv_dim + q_dim + kv_dim + (hq / group) * hd + d]);
+  }
+}
+
+// out[j][i] = bf16(silu(gu[j][i]) * gu[j][F + i]), silu(g) = g / (1 + exp(-g)).
+__global__ void __launch_bounds__(kGlueThreads) swiglu_kernel(const float* __restrict__ gu,
+                                                              uint16_t* __restrict__ out, int M, int F) {
+  pdl_trigger();
+  pdl_wait();
+  const long long total = (long long)M * F;
+  for (long long e = blockIdx.x * (long long)kGlueThreads + threadIdx.x; e < total;
+       e += (long long)gridDim.x * kGlueThreads) {
+    const int j = (int)(e / F), i = (int)(e - (long long)j * F);
+    const float g = gu[(long long)j * 2 * F + i], u = gu[(long long)j * 2 * F + F + i];
+    const float s = g / (1.0f + expf(-g));
+    out[e] = f2bf(s * u);
+  }
+}
+
+template <class... Args>
+cudaError_t launch_pdl(void (*kern)(Args...), int grid, cudaStream_t s, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kGlueThreads, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
+
+struct Ws {  // workspace carve-up
+  float* h;     // M x hidden      residual stream
+  uint16_t* x;  // M x max(hidden, q_dim, ffn) bf16 GEMV input
+  float* qkv;   // M x (q_dim + 2 kv_dim)
+  float* y;     // M x hidden      o / down outputs
+  float* gu;    // M x 2 ffn
+  size_t bytes;
+};
+
+Ws carve(const kq_decode_model* m, int M, void* base) {
+  Ws w;
+  const int xw = std::max(m->hidden, std::max(m->q_dim, m->ffn));
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    void* p = base ? static_cast<uint8_t*>(base) + off : nullptr;
+    off = al256(off + bytes);
+    return p;
+  };
+  w.h = static_cast<float*>(take(sizeof(float) * (size_t)M * m->hidden));
+  w.x = static_cast<uint16_t*>(take(sizeof(uint16_t) * (size_t)M * xw));
+  w.qkv = static_cast<float*>(take(sizeof(float) * (size_t)M * (m->q_dim + 2 * m->kv_dim)));
+  w.y = static_cast<float*>(take(sizeof(float) * (size_t)M * m->hidden));
+  w.gu = static_cast<float*>(take(sizeof(float) * (size_t)M * 2 * m->ffn));
+  w.bytes = off;
+  return w;
+}
+
+}  // namespace
+
+int decode_check(const kq_decode_model* m, int M, std::string* err) {
+  if (!m) { *err = "model is NULL"; return -1; }
+  if (m->n_layers < 0 || m->hidden <= 0 || m->q_dim <= 0 || m->kv_dim <= 0 || m->head_dim <= 0 ||
+      m->ffn <= 0 || m->vocab <= 0) { *err = "model dimensions must be positive"; return -1; }
+  if (m->q_dim % m->head_dim || m->kv_dim % m->head_dim) { *err = "q_dim and kv_dim must be multiples of head_dim"; return -1; }
+  if ((m->q_dim / m->head_dim) % (m->kv_dim / m->head_dim)) { *err = "query heads must be a multiple of kv heads"; return -1; }
+  if (m->hidden % 256 || m->q_dim % 256 || m->ffn % 256) { *err = "hidden, q_dim and ffn must be multiples of 256"; return -1; }
+  if (M < 1 || M > 16) { *err = "M must be in 1..16"; return -1; }
+  if (m->n_layers > 0 && (!m->w_qkv || !m->w_o || !m->w_gate_up || !m->w_down)) { *err = "layer weight arrays are NULL"; return -1; }
+  if (!m->w_head) { *err = "w_head is NULL"; return -1; }
+  return 0;
+}
+
+size_t decode_workspace_size(const kq_decode_model* m, int M) { return carve(m, M, nullptr).bytes; }
+
+int decode_step(const kq_decode_model* m, const uint16_t* x, float* logits, int M, void* ws, int num_sms,
+                cudaStream_t s, std::string* err) {
+  const Ws w = carve(m, M, ws);
+  const int qkv_dim = m->q_dim + 2 * m->kv_dim;
+  const int group = (m->q_dim / m->head_dim) / (m->kv_dim / m->head_dim);
+  auto rowb = [](int fmt, int K) { return (long long)kq_row_bytes(fmt, K); };
+  auto ew_grid = [&](long long n) { return (int)std::min<long long>(4 * (long long)num_sms, (n + kGlueThreads - 1) / kGlueThreads); };
+  auto ck = [&](cudaError_t e, const char* what) {
+    if (e != cudaSuccess) { *err = std::string(what) + ": " + cudaGetErrorString(e); return -1; }
+    return 0;
+  };
+  auto gemv = [&](int fmt, const void* wt, const uint16_t* xin, float* y, int N, int K) {
+    return launch_gemv_mma(fmt, wt, xin, y, M, N, K, rowb(fmt, K), num_sms, s, true, err);
+  };
+  // h = x (bf16 -> fp32); x_norm = RMSNorm(h)
+  if (ck(launch_pdl(add_rmsnorm_kernel, M, s, false, w.h, x, (const float*)nullptr, w.x, m->hidden, m->rms_eps),
+         "add_rmsnorm"))
+    return -1;
+  for (int l = 0; l < m->n_layers; ++l) {
+    if (gemv(m->layer_fmt, m->w_qkv[l], w.x, w.qkv, qkv_dim, m->hidden)) return -1;
+    if (ck(launch_pdl(gqa_expand_kernel, ew_grid((long long)M * m->q_dim), s, true, (const float*)w.qkv, w.x, M,
+                      m->q_dim, m->kv_dim, m->head_dim, group),
+           "gqa_expand"))
+      return -1;
+    if (gemv(m->layer_fmt, m->w_o[l], w.x, w.y, m->hidden, m->q_dim)) return -1;
+    if (ck(launch_pdl(add_rmsnorm_kernel, M, s, true, w.h, (const uint16_t*)nullptr, (const float*)w.y, w.x,
+                      m->hidden, m->rms_eps),
+           "add_rmsnorm"))
+      return -1;
+    if (gemv(m->layer_fmt, m->w_gate_up[l], w.x, w.gu, 2 * m->ffn, m->hidden)) return -1;
+    if (ck(launch_pdl(swiglu_kernel, ew_grid((long long)M * m->ffn), s, true, (const float*)w.gu, w.x, M, m->ffn),
+           "swiglu"))
+      return -1;
+    if (gemv(m->layer_fmt, m->w_down[l], w.x, w.y, m->hidden, m->ffn)) return -1;
+    if (ck(launch_pdl(add_rmsnorm_kernel, M, s, true, w.h, (const uint16_t*)nullptr, (const float*)w.y, w.x,
+                      m->hidden, m->rms_eps),
+           "add_rmsnorm"))
+      return -1;
+  }
+  return gemv(m->head_fmt, m->w_head, w.x, logits, m->vocab, m->hidden);
+}
+
+}  // namespace kq

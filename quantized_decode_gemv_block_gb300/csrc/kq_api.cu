@@ -155,6 +155,37 @@ int kq_gemm(int fmt, const void* w_blocks, int x_dtype, const void* x, float* y,
   return fail(KQ_ERR_UNSUPPORTED, "kq_gemm with M > 16 is not available in this build");
 }
 
+size_t kq_decode_workspace_size(const kq_decode_model* model, int M) {
+  std::string err;
+  if (kq::decode_check(model, M, &err) != 0) return 0;
+  return kq::decode_workspace_size(model, M);
+}
+
+int kq_decode_step(const kq_decode_model* model, const void* x, float* logits, int M, void* workspace,
+                   size_t ws_bytes, void* stream) {
+  std::string err;
+  if (kq::decode_check(model, M, &err) != 0) return fail(KQ_ERR_ARG, err);
+  if (!fmt_known(model->layer_fmt) || !fmt_known(model->head_fmt))
+    return fail(KQ_ERR_UNSUPPORTED, "unknown weight format in the model");
+  if (!x || !logits) return fail(KQ_ERR_ARG, "x or logits is NULL");
+  if (!aligned(x, 16) || !aligned(logits, 4)) return fail(KQ_ERR_ARG, "misaligned x or logits");
+  const size_t need = kq::decode_workspace_size(model, M);
+  if (!workspace || ws_bytes < need || !aligned(workspace, 256))
+    return fail(KQ_ERR_WORKSPACE, "workspace must be >= " + std::to_string(need) + " bytes, 256-byte aligned");
+  for (int l = 0; l < model->n_layers; ++l) {
+    const void* ps[4] = {model->w_qkv[l], model->w_o[l], model->w_gate_up[l], model->w_down[l]};
+    for (const void* p : ps)
+      if (!p || !aligned(p, 16)) return fail(KQ_ERR_ARG, "layer " + std::to_string(l) + ": NULL or misaligned weights");
+  }
+  if (!aligned(model->w_head, 16)) return fail(KQ_ERR_ARG, "misaligned w_head");
+  const int sms = sm_count(&err);
+  if (sms < 0) return fail(KQ_ERR_CUDA, err);
+  if (kq::decode_step(model, static_cast<const uint16_t*>(x), logits, M, workspace, sms,
+                      static_cast<cudaStream_t>(stream), &err) != 0)
+    return fail(KQ_ERR_CUDA, err);
+  return ok();
+}
+
 int kq_quantize(int fmt, const float* w, void* w_blocks, int N, int K, void* stream) {
   if (!fmt_known(fmt)) return fail(KQ_ERR_UNSUPPORTED, "unknown block format " + std::to_string(fmt));
   if (N < 0 || K < 0) return fail(KQ_ERR_ARG, "N and K must be >= 0");

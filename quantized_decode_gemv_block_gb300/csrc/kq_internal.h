@@ -2,7 +2,11 @@
 #pragma once
 #include <cuda_runtime.h>
 
+#include <cstdint>
+
 #include <string>
+
+#include "kq.h"
 
 namespace kq {
 
@@ -42,6 +46,12 @@ int launch_gemv_mma(int fmt, const void* w, const void* x, float* y, int M, int 
 // fp32 activations, CUDA-core path.
 int launch_gemv_f32(int fmt, const void* w, const float* x, float* y, int M, int N, int K,
                     long long row_bytes, cudaStream_t stream, std::string* err);
+
+// Decode step (decode.cu).
+int decode_check(const kq_decode_model* m, int M, std::string* err);
+size_t decode_workspace_size(const kq_decode_model* m, int M);
+int decode_step(const kq_decode_model* m, const uint16_t* x, float* logits, int M, void* ws, int num_sms,
+                cudaStream_t s, std::string* err);
 
 // GPU quantizers (fp64 arithmetic).
 int launch_quantize(int fmt, const float* w, void* blocks, int N, int K, cudaStream_t stream,

@@ -1,0 +1,96 @@
+"""GPU decode step (kq_decode_step) against the fp64 oracle step, and batch invariance.
+
+Tolerance (derived in the design doc): every GEMV input is rounded to bf16, and the GPU (fp32
+arithmetic) and the oracle (fp64) round an activation lying within the GEMV's ~1e-6
+relative error of a bf16 rounding boundary to neighbouring bf16 values (about 1e-6 / 2^-8,
+i.e. 2.6e-4 of the elements at each rounding point). One flip in the head's input moves a
+logit by at most 2^-8 |w_k x_k|; flips upstream move the residual stream by a similar
+relative amount and accumulate over layers. Per logit the test allows 1e-2 * sum_k |w_k x_k|
+(sum over the head row, x = the oracle's final activations) and a median of 1e-5 per layer
+of depth (2 layers: 2e-5; 28 layers: 2.8e-4).
+"""
+import numpy as np
+import pytest
+import torch
+
+import quantized_decode_gemv_block_gb300 as kq
+from quantized_decode_gemv_block_gb300 import decode as kqd
+from quantized_decode_gemv_block_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+FMT = {"q4_k": 2, "q8_0": 1, "affine4": 3}
+
+
+@pytest.fixture(scope="module")
+def built():
+    from quantized_decode_gemv_block_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+def make(orc, d, seed):
+    """Weights from numpy, quantized by the oracle; the same blocks go to the GPU."""
+    host_layers, dev_layers, tid = [], [], 0
+    for _ in range(d["n_layers"]):
+        hl = []
+        for _, N, K in kqd.matrix_shapes(d):
+            hl.append(orc.quantize(FMT[d["layer_fmt"]], inputs.weights(N, K, seed=seed, tensor_id=tid)))
+            tid += 1
+        host_layers.append(tuple(hl))
+        dev_layers.append(tuple(torch.from_numpy(b).cuda() for b in hl))
+    head = orc.quantize(FMT[d["head_fmt"]], inputs.weights(d["vocab"], d["hidden"], seed=seed, tensor_id=tid))
+    model = kq.DecodeModel(d["n_layers"], d["hidden"], d["q_dim"], d["kv_dim"], d["head_dim"], d["ffn"],
+                           d["vocab"], dev_layers, torch.from_numpy(head).cuda(), d["layer_fmt"],
+                           d["head_fmt"], d["eps"])
+    odims = dict(d, layer_fmt=FMT[d["layer_fmt"]], head_fmt=FMT[d["head_fmt"]])
+    return model, host_layers, head, odims
+
+
+def check_logits(orc, odims, head, logits_gpu, ref, xfinal):
+    depth = max(1, odims["n_layers"])
+    # tolerance base: sum_k |w_k x_k| over the head row, x = the oracle's final activations
+    W = orc.dequant(odims["head_fmt"], head, odims["vocab"], odims["hidden"])
+    base = np.abs(inputs.bf16_bits_to_f32(xfinal).astype(np.float64)) @ np.abs(W).T
+    err = np.abs(logits_gpu.astype(np.float64) - ref)
+    assert np.all(err <= 1e-2 * base), f"max err/base {(err / base).max():.3g}"
+    assert np.median(err / base) < 1e-5 * depth, f"median err/base {np.median(err / base):.3g}"
+
+
+TINY = dict(n_layers=2, hidden=256, q_dim=256, kv_dim=128, head_dim=64, ffn=512, vocab=1000,
+            layer_fmt="q4_k", head_fmt="q8_0", eps=1e-6)
+
+
+def test_tiny_decode_matches_oracle_and_is_batch_invariant(built, orc):
+    model, hl, head, od = make(orc, TINY, seed=11)
+    x = inputs.activations_bf16(16, TINY["hidden"], seed=12)
+    xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+    full = model.step(xd).cpu().numpy()
+    ref, xf = orc.decode_step(od, hl, head, x, return_head_input=True)
+    check_logits(orc, od, head, full, ref, xf)
+    for M in (1, 3, 8):
+        y = model.step(xd[:M].contiguous()).cpu().numpy()
+        assert np.array_equal(y.view(np.uint32), full[:M].view(np.uint32)), f"M={M}"
+    assert kq.device_errors() == 0
+
+
+def test_decode_graph_replay_matches_eager(built, orc):
+    model, hl, head, od = make(orc, dict(TINY, head_fmt="q4_k", vocab=512), seed=13)
+    g = kqd.GraphStep(model, 4)
+    x = inputs.activations_bf16(4, TINY["hidden"], seed=14)
+    g.x.copy_(torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16))
+    g.replay()
+    torch.cuda.synchronize()
+    eager = model.step(g.x.clone()).cpu().numpy()
+    assert np.array_equal(g.logits.cpu().numpy().view(np.uint32), eager.view(np.uint32))
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_full_dense_28_layer_decode_step(built, orc, M):
+    d = kqd.DENSE_28L
+    model, hl, head, od = make(orc, d, seed=0)
+    x = inputs.activations_bf16(M, d["hidden"], seed=0, tensor_id=5000)
+    xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+    logits = model.step(xd).cpu().numpy()
+    ref, xf = orc.decode_step(od, hl, head, x, return_head_input=True)
+    check_logits(orc, od, head, logits, ref, xf)
+    assert kq.device_errors() == 0
