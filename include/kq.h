@@ -173,6 +173,28 @@ size_t kq_decode_workspace_size(const kq_decode_model* model, int M);
 int kq_decode_step(const kq_decode_model* model, const void* x, float* logits, int M, void* workspace,
                    size_t ws_bytes, void* stream);
 
+/* ---- Decode step that allocates nothing (no counterpart in the engine pages) ----
+ * kq_decode_step needs a device workspace from its caller. Some callers cannot call
+ * cudaMalloc or any allocating routine: code that only borrows a GPU from a host framework
+ * that owns every device allocation, code on a latency-critical path where an allocation
+ * could synchronise the device, or code that must not allocate while a stream is being
+ * captured. kq_decode_step_static runs the same step with scratch memory that the library
+ * holds in a fixed device array of KQ_DECODE_STATIC_SCRATCH_BYTES (4 MiB): every GPU that
+ * loads the library keeps that array until the process exits, and nothing is allocated
+ * per call (no cudaMalloc, no allocating library routine).
+ *  - The caller still passes x and logits (device memory), as for kq_decode_step.
+ *  - Models whose kq_decode_workspace_size(model, M) exceeds the array are rejected with
+ *    KQ_ERR_WORKSPACE and a message giving both sizes.
+ *  - The first call on a device looks up the array's device address (with that device
+ *    current) and caches it; make that first call before capturing any stream.
+ *  - Every call on a device shares the one array and leaves the last step's intermediate
+ *    values in it; the step writes each value before reading it, so nothing needs
+ *    clearing. Two calls that run at the same time on one device (for example on two
+ *    streams) race on the array: serialise them.
+ * Other arguments, results and errors as kq_decode_step. */
+#define KQ_DECODE_STATIC_SCRATCH_BYTES (4u << 20)
+int kq_decode_step_static(const kq_decode_model* model, const void* x, float* logits, int M, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

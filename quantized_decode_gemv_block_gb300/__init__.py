@@ -75,6 +75,8 @@ def load_library(path: str = LIB_PATH):
     L.kq_decode_workspace_size.restype = SZ
     L.kq_decode_step.argtypes = [ctypes.POINTER(DecodeModelC), P, P, I, P, SZ, P]
     L.kq_decode_step.restype = I
+    L.kq_decode_step_static.argtypes = [ctypes.POINTER(DecodeModelC), P, P, I, P]
+    L.kq_decode_step_static.restype = I
     _lib = L
     return L
 
@@ -212,4 +214,10 @@ class DecodeModel:
             workspace = torch.empty(self.workspace_size(M), dtype=torch.uint8, device=x.device)
         _check(lib().kq_decode_step(ctypes.byref(self.c), x.data_ptr(), logits.data_ptr(), M,
                                     workspace.data_ptr(), workspace.numel(), _stream(stream)))
+        return logits
+
+    def step_static(self, x: torch.Tensor, logits: torch.Tensor, stream=None) -> torch.Tensor:
+        """The same step through kq_decode_step_static (library-held scratch, no allocation)."""
+        _check(lib().kq_decode_step_static(ctypes.byref(self.c), x.data_ptr(), logits.data_ptr(),
+                                           x.shape[0], _stream(stream)))
         return logits

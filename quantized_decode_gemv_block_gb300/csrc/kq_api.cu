@@ -2,6 +2,7 @@
 // The declarations, their sources and their contracts are in include/kq.h.
 #include <cstdint>
 #include <cstdio>
+#include <mutex>
 #include <string>
 
 #include "kq.h"
@@ -196,6 +197,63 @@ int kq_quantize(int fmt, const float* w, void* w_blocks, int N, int K, void* str
   if (!aligned(w, 4) || !aligned(w_blocks, 2)) return fail(KQ_ERR_ARG, "misaligned w or w_blocks");
   std::string err;
   if (kq::launch_quantize(fmt, w, w_blocks, N, K, static_cast<cudaStream_t>(stream), &err) != 0)
+    return fail(KQ_ERR_CUDA, err);
+  return ok();
+}
+
+// ---- Decode step with library-owned scratch (kq_decode_step_static) ----
+// The scratch lives in one file-scope device array, so no call allocates. Host code may
+// not use the array's name as a device address (on the host it names a stand-in object):
+// the address comes from cudaGetSymbolAddress, looked up once per device by the first
+// call on that device (with that device current) and cached.
+static __device__ __align__(256) unsigned char g_decode_scratch[KQ_DECODE_STATIC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[64] = {nullptr};
+}  // namespace
+
+int kq_decode_step_static(const kq_decode_model* model, const void* x, float* logits, int M, void* stream) {
+  std::string err;
+  if (kq::decode_check(model, M, &err) != 0) return fail(KQ_ERR_ARG, err);
+  if (!fmt_known(model->layer_fmt) || !fmt_known(model->head_fmt))
+    return fail(KQ_ERR_UNSUPPORTED, "unknown weight format in the model");
+  if (!x || !logits) return fail(KQ_ERR_ARG, "x or logits is NULL");
+  if (!aligned(x, 16) || !aligned(logits, 4)) return fail(KQ_ERR_ARG, "misaligned x or logits");
+  const size_t need = kq::decode_workspace_size(model, M);
+  if (need > (size_t)KQ_DECODE_STATIC_SCRATCH_BYTES)
+    return fail(KQ_ERR_WORKSPACE, "this model needs " + std::to_string(need) + " bytes of scratch for M=" +
+                                      std::to_string(M) + "; the static scratch holds " +
+                                      std::to_string((size_t)KQ_DECODE_STATIC_SCRATCH_BYTES) +
+                                      " bytes (use kq_decode_step with a caller workspace)");
+  for (int l = 0; l < model->n_layers; ++l) {
+    const void* ps[4] = {model->w_qkv[l], model->w_o[l], model->w_gate_up[l], model->w_down[l]};
+    for (const void* p : ps)
+      if (!p || !aligned(p, 16)) return fail(KQ_ERR_ARG, "layer " + std::to_string(l) + ": NULL or misaligned weights");
+  }
+  if (!aligned(model->w_head, 16)) return fail(KQ_ERR_ARG, "misaligned w_head");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(KQ_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return fail(KQ_ERR_UNSUPPORTED, "device index beyond 63");
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_decode_scratch);
+      if (e != cudaSuccess || !p)
+        return fail(KQ_ERR_CUDA, std::string("cudaGetSymbolAddress of the decode scratch: ") + cudaGetErrorString(e));
+      g_scratch_ptr[dev] = p;
+    }
+    scratch = g_scratch_ptr[dev];
+  }
+  const int sms = sm_count(&err);
+  if (sms < 0) return fail(KQ_ERR_CUDA, err);
+  // Every buffer of the scratch is written before it is read within a step, so nothing
+  // needs clearing between calls.
+  if (kq::decode_step(model, static_cast<const uint16_t*>(x), logits, M, scratch, sms,
+                      static_cast<cudaStream_t>(stream), &err) != 0)
     return fail(KQ_ERR_CUDA, err);
   return ok();
 }
