@@ -8,6 +8,10 @@ Prints ONE JSON line (rank 0). Workloads (synthetic data, seeded):
            one bf16 activation row each. One step = both GEMVs.
   verify   Q4_K speculative-verify GEMM, W 12288x4096, M bf16 rows (--m, default 16).
   q8_0     Q8_0 GEMV, W 1024x1024, one fp32 row.
+  head     Q8_0 lm-head GEMV, W 151936x2048, M bf16 rows (--m).
+  decode   the dense 28-layer decode step (kq_decode_step) in a CUDA graph, M rows (--m).
+  prefill  Q4_K prefill GEMM on the tensor cores, W 9728x2560, X 2048x2560 bf16; reported in
+           TFLOP/s (2*M*N*K per step) against the measured dense bf16/fp16 peak.
 Metric: weight block bytes read per step / step time (GB/s). Inputs: rotating copies of
 the weights totalling >= 4x the L2 size, so every launch streams its weights from HBM.
 K steps are captured in one CUDA graph and replayed; a second replay with an event pair
@@ -48,6 +52,9 @@ def workload_spec(name: str, m: int):
     if name == "decode":
         return dict(name=f"decode step dense 28 layers hidden 2048 ffn 6144 vocab 151936, M={m}",
                     fmt="q4_k", mats=[], M=m, dtype="bf16", decode=True)
+    if name == "prefill":
+        return dict(name="q4_k prefill gemm 9728x2560, X 2048x2560 bf16", fmt="q4_k", mats=[(9728, 2560)],
+                    M=2048, dtype="bf16", prefill=True)
     if name == "head":
         return dict(name=f"q8_0 lm head 151936x2048, M={m} bf16", fmt="q8_0", mats=[(151936, 2048)],
                     M=m, dtype="bf16")
@@ -201,15 +208,182 @@ def run_reference(args, spec):
             oracle.gemv(f, blocks, x, N, K, nthreads=cores)
     el = time.perf_counter() - t0
     v = nbytes * args.steps / el / 1e9
-    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+    unit, metric = "GB/s", METRIC
+    if spec.get("prefill"):
+        N, K = spec["mats"][0]
+        v, unit, metric = 2.0 * spec["M"] * N * K * args.steps / el / 1e12, "TFLOP/s", PREFILL_METRIC
+    line = {"impl": "reference", "metric": metric, "value": v, "unit": unit, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": spec["name"], "M": spec["M"]},
-            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                             "sample": f"full workload per step ({nbytes} weight bytes), fp64 scalar oracle, "
-                                       f"OpenMP over output rows"},
-            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "cpu_baseline": {"value": v, "unit": unit, "cores": cores, "kind": "oracle",
+                             "sample": f"M={spec['M']} rows against the full matrices per step ({nbytes} weight "
+                                       f"bytes), fp64 scalar oracle, OpenMP over output rows"},
+            "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+PREFILL_METRIC = "prefill GEMM TFLOP/s (Q4_K W 9728x2560, X 2048x2560 bf16, fp32 accumulate)"
+
+
+def run_prefill(args, spec):
+    """kq_gemm with M = 2048 (convert X + tcgen05 GEMM), K steps captured in one CUDA graph."""
+    import torch
+    import torch.distributed as dist
+
+    import quantized_decode_gemv_block_gb300 as kq
+    from quantized_decode_gemv_block_gb300 import build, inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    if rank == 0 or not os.path.exists(kq.LIB_PATH):
+        build.build()
+    if world > 1:
+        dist.barrier()
+    kq.load_library()
+    dev = torch.device("cuda", local)
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 129 * 2**20) or 129 * 2**20
+    (N, K), M = spec["mats"][0], spec["M"]
+    flops = 2.0 * M * N * K
+    w32 = inputs.weights_cuda(N, K, seed=rank, tensor_id=0, device=str(dev))
+    wq = kq.quantize("q4_k", w32)
+    del w32
+    x0 = inputs.activations_cuda(M, K, seed=rank, tensor_id=1000, dtype=torch.bfloat16, device=str(dev))
+    need = kq.gemm_workspace_size("q4_k", torch.bfloat16, M, N, K)
+    per_set = wq.numel() + x0.numel() * 2 + need + M * N * 4
+    copies = max(2, math.ceil(4 * l2 / per_set))
+    sets = [(wq.clone(), x0.clone(), torch.empty(need, dtype=torch.uint8, device=dev),
+             torch.empty((M, N), dtype=torch.float32, device=dev)) for _ in range(copies)]
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(s, events=None):
+        w, x, ws, y = sets[s % copies]
+        if events is not None:
+            events[s][0].record()
+        kq.gemm("q4_k", w, x, N, K, y=y, workspace=ws)
+        if events is not None:
+            events[s][1].record()
+
+    def capture(nsteps, events=None):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            step(0)
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for s in range(nsteps):
+                    step(s, events)
+        return g
+
+    K_ = args.steps
+    g_warm, g_main = capture(args.warmup), capture(K_)
+    ev = [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
+          for _ in range(K_)]
+    g_inst = capture(K_, ev)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        g_warm.replay()
+    stream.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record()
+        g_main.replay()
+        t1.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms_total = t0.elapsed_time(t1)
+    with torch.cuda.stream(stream):
+        g_inst.replay()
+    torch.cuda.synchronize()
+    call_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < 1.5:
+        with torch.cuda.stream(stream):
+            g_main.replay()
+        stream.synchronize()
+    clocks = sampler.stop()
+    # e2e: pinned-host X in, Y out, every step, eager calls through the public API
+    xh = x0.cpu().pin_memory()
+    yh = torch.empty((M, N), dtype=torch.float32).pin_memory()
+    n_e2e = min(K_, 20)
+    w, xd, ws, y = sets[0]
+    for _ in range(2):
+        xd.copy_(xh, non_blocking=True)
+        kq.gemm("q4_k", w, xd, N, K, y=y, workspace=ws)
+        yh.copy_(y, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n_e2e):
+        xd.copy_(xh, non_blocking=True)
+        kq.gemm("q4_k", w, xd, N, K, y=y, workspace=ws)
+        yh.copy_(y, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    t = torch.tensor([ms_total, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_step, e2e_ms = float(t[0]) / K_, float(t[1])
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, peak_kind = float(json.load(f)["bf16_tflops"]), "measured bf16_tflops (burst; fp16 runs at the bf16 rate)"
+    except Exception:
+        peak, peak_kind = 1900.0, "fallback bf16 burst"
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        blocks = wq.cpu().numpy()
+        xs = inputs.activations_bf16(16, K, seed=0, tensor_id=1000)
+        cores = os.cpu_count() or 1
+        passes, c0 = 0, time.perf_counter()
+        while time.perf_counter() - c0 < args.cpu_budget:
+            oracle.gemv(2, blocks, xs, N, K, nthreads=cores)
+            passes += 1
+        el = time.perf_counter() - c0
+        cpu = {"value": 2.0 * 16 * N * K * passes / el / 1e12, "unit": "TFLOP/s", "cores": cores,
+               "kind": "oracle", "sample": f"{passes} oracle passes of 16 of the 2048 tokens against the full "
+                                           f"9728x2560 Q4_K matrix in {el:.1f} s (fp64 scalar, OpenMP over rows)"}
+    if rank == 0:
+        value = world * flops / (ms_step * 1e-3) / 1e12
+        achieved = flops / (call_ms * 1e-3) / 1e12
+        line = {
+            "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K_,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp16 x fp16 -> fp32 (bf16 X and Q4_K W converted in-kernel)",
+            "data": "synthetic",
+            "config": {"workload": spec["name"], "M": M, "N": N, "K": K, "flop_per_step": flops,
+                       "weight_bytes_per_step": wq.numel(),
+                       "weight_gbs_equivalent": world * wq.numel() / (ms_step * 1e-3) / 1e9,
+                       "l2": f"rotating W/X/workspace/Y sets: {copies} x {per_set} B >= 4x L2 ({l2} B)",
+                       "parallelism": "replicas" if world > 1 else "single gpu"},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": None, "peak_source": peak_kind,
+                         "kernel": "convert_x_kernel + gemm_q4k_tc_kernel (one kq_gemm call, event pair around it)",
+                         "launch_us": call_ms * 1e3},
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": xh.numel() * 2, "d2h_bytes_per_step": yh.numel() * 4,
+                    "note": "pinned-host X copied in, kq_gemm, Y copied out, every step"},
+            "gpu_launches": 2 * K_,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
 
 
 def run_decode(args, spec):
@@ -354,7 +528,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="kq", choices=["kq", "reference"])
-    ap.add_argument("--workload", default="ffn", choices=["ffn", "verify", "q8_0", "head", "decode"])
+    ap.add_argument("--workload", default="ffn", choices=["ffn", "verify", "q8_0", "head", "decode", "prefill"])
     ap.add_argument("--m", type=int, default=16)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -364,10 +538,15 @@ def main():
     if args.impl == "reference":
         if spec.get("decode"):
             spec = dict(spec, fmt="q4_k", mats=[(3072, 2048), (2048, 2048), (12288, 2048), (2048, 6144)])
+        if spec.get("prefill"):
+            spec = dict(spec, M=16)  # bounded sample: 16 of the 2048 tokens per step
         run_reference(args, spec)
         return
     if spec.get("decode"):
         run_decode(args, spec)
+        return
+    if spec.get("prefill"):
+        run_prefill(args, spec)
         return
 
     import torch

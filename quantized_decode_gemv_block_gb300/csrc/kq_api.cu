@@ -127,8 +127,11 @@ int kq_device_errors(void) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return fail(KQ_ERR_CUDA, std::string("cudaDeviceSynchronize: ") + cudaGetErrorString(e));
   std::string err;
-  const unsigned int v = kq::take_device_errors(&err);
+  unsigned int v = kq::take_device_errors(&err);
   if (v == 0xFFFFFFFFu) return fail(KQ_ERR_CUDA, err);
+  const unsigned int vt = kq::take_tc_errors();
+  if (vt == 0xFFFFFFFFu) return fail(KQ_ERR_CUDA, "reading the prefill error word");
+  v |= vt;
   ok();
   return static_cast<int>(v & 0x7FFFFFFFu);
 }
@@ -144,16 +147,34 @@ int kq_gemv_ex(int fmt, const void* w_blocks, int x_dtype, const void* x, float*
 }
 
 size_t kq_gemm_workspace_size(int fmt, int x_dtype, int M, int N, int K) {
-  (void)fmt; (void)x_dtype; (void)M; (void)N; (void)K;
-  return 0;
+  if (M <= 16 || N <= 0 || fmt != KQ_Q4_K || x_dtype != KQ_BF16 || K <= 0 || K % 256 != 0) return 0;
+  return kq::gemm_tc_workspace(M, N, K);
 }
 
 int kq_gemm(int fmt, const void* w_blocks, int x_dtype, const void* x, float* y, int M, int N,
             int K, void* workspace, size_t ws_bytes, void* stream) {
-  (void)workspace; (void)ws_bytes;
   if (M <= 16)
     return gemv_impl(fmt, w_blocks, x_dtype, x, y, M, N, K, static_cast<cudaStream_t>(stream));
-  return fail(KQ_ERR_UNSUPPORTED, "kq_gemm with M > 16 is not available in this build");
+  int rc = check_common(fmt, w_blocks, x_dtype, x, y, M, N, K);
+  if (rc != KQ_OK) return rc;
+  if (fmt != KQ_Q4_K || x_dtype != KQ_BF16)
+    return fail(KQ_ERR_UNSUPPORTED, "kq_gemm with M > 16 runs Q4_K weights with bf16 activations");
+  if (N == 0) return ok();
+  if (K == 0) {
+    const cudaError_t e = cudaMemsetAsync(y, 0, sizeof(float) * (size_t)M * (size_t)N, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(KQ_ERR_CUDA, std::string("cudaMemsetAsync: ") + cudaGetErrorString(e));
+    return ok();
+  }
+  const size_t need = kq::gemm_tc_workspace(M, N, K);
+  if (!workspace || ws_bytes < need || !aligned(workspace, 256))
+    return fail(KQ_ERR_WORKSPACE, "workspace must be >= " + std::to_string(need) + " bytes, 256-byte aligned");
+  std::string err;
+  const int sms = sm_count(&err);
+  if (sms < 0) return fail(KQ_ERR_CUDA, err);
+  if (kq::launch_gemm_tc(w_blocks, x, y, M, N, K, (long long)kq_row_bytes(fmt, K), workspace, sms,
+                         static_cast<cudaStream_t>(stream), &err) != 0)
+    return fail(KQ_ERR_CUDA, err);
+  return ok();
 }
 
 size_t kq_decode_workspace_size(const kq_decode_model* model, int M) {

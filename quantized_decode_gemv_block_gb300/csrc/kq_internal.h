@@ -47,6 +47,12 @@ int launch_gemv_mma(int fmt, const void* w, const void* x, float* y, int M, int 
 int launch_gemv_f32(int fmt, const void* w, const float* x, float* y, int M, int N, int K,
                     long long row_bytes, cudaStream_t stream, std::string* err);
 
+// Tensor-core prefill (gemm_tc.cu): Q4_K weights x bf16 activations, M > 16.
+size_t gemm_tc_workspace(int M, int N, int K);
+int launch_gemm_tc(const void* w, const void* x, float* y, int M, int N, int K, long long row_bytes, void* ws,
+                   int num_sms, cudaStream_t stream, std::string* err);
+unsigned int take_tc_errors();
+
 // Decode step (decode.cu).
 int decode_check(const kq_decode_model* m, int M, std::string* err);
 size_t decode_workspace_size(const kq_decode_model* m, int M);
