@@ -84,7 +84,11 @@ KERNEL_SOURCES = ["quantized_decode_gemv_block_gb300/csrc/gemv_mma.cu",
                   "quantized_decode_gemv_block_gb300/csrc/kq_device.cuh"]
 
 
-def profile_traffic(profile_name: str):
+PREFILL_SOURCES = ["quantized_decode_gemv_block_gb300/csrc/gemm_tc.cu",
+                   "quantized_decode_gemv_block_gb300/csrc/kq_device.cuh"]
+
+
+def profile_traffic(profile_name: str, sources=None):
     """DRAM bytes per launch from a committed ncu summary, if the kernel source is unchanged."""
     path = os.path.join(ROOT, "profiles", profile_name)
     if not os.path.exists(path):
@@ -95,7 +99,7 @@ def profile_traffic(profile_name: str):
             if "=" in line and line.strip().startswith("- "):
                 k, v = line.strip()[2:].split("=", 1)
                 vals[k.strip()] = v.strip()
-    if vals.get("kernel_source_sha256") != source_sha(KERNEL_SOURCES):
+    if vals.get("kernel_source_sha256") != source_sha(sources or KERNEL_SOURCES):
         return None
     try:
         return float(vals["dram_bytes_per_launch"])
@@ -370,8 +374,9 @@ def run_prefill(args, spec):
                        "l2": f"rotating W/X/workspace/Y sets: {copies} x {per_set} B >= 4x L2 ({l2} B)",
                        "parallelism": "replicas" if world > 1 else "single gpu"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": None, "peak_source": peak_kind,
-                         "kernel": "convert_x_kernel + gemm_q4k_tc_kernel (one kq_gemm call, event pair around it)",
+                         "frac": achieved / peak,
+                         "traffic": profile_traffic("gemm_tc_prefill.md", PREFILL_SOURCES), "peak_source": peak_kind,
+                         "kernel": "prefill_prep_kernel + gemm_q4k_tc_kernel (one kq_gemm call, event pair around it)",
                          "launch_us": call_ms * 1e3},
             "cpu_baseline": cpu,
             "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
