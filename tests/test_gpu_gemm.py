@@ -53,8 +53,10 @@ def run_gemm(kq, blocks, x_bits, N, K):
 
 
 # (M, N, K): one tile; ragged M (tails of 72 and 1 tokens); ragged N (tails of 8 and 232
-# rows); several K super-blocks; more tiles than SMs.
-SHAPES = [(17, 256, 256), (200, 520, 1024), (129, 300, 512), (257, 1000, 2560), (384, 2048, 768)]
+# rows); several K super-blocks; more tiles than SMs; N % 4 != 0 (rows not 16-byte aligned:
+# the direct-store path) with an odd number of 128-row tiles (a cluster CTA with no rows).
+SHAPES = [(17, 256, 256), (200, 520, 1024), (129, 300, 512), (257, 1000, 2560), (384, 2048, 768),
+          (130, 258, 512)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
