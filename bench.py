@@ -79,6 +79,22 @@ def source_sha(files):
     return h.hexdigest()[:16]
 
 
+def max_over_ranks(values, device, world):
+    """Each rank's timings -> the maximum over ranks (every rank gets it); one process: as is."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def replica_rate(world: int, units_per_rank: float, ms_per_step_max: float) -> float:
+    """Whole-job throughput of `world` independent replicas (weak scaling): the work of every
+    rank over the slowest rank's time, in units per second."""
+    return world * units_per_rank / (ms_per_step_max * 1e-3)
+
+
 KERNEL_SOURCES = ["quantized_decode_gemv_block_gb300/csrc/gemv_mma.cu",
                   "quantized_decode_gemv_block_gb300/csrc/gemv_formats.cuh",
                   "quantized_decode_gemv_block_gb300/csrc/kq_device.cuh"]
@@ -337,10 +353,8 @@ def run_prefill(args, spec):
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / n_e2e
-    t = torch.tensor([ms_total, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_step, e2e_ms = float(t[0]) / K_, float(t[1])
+    ms_total, e2e_ms = max_over_ranks([ms_total, e2e_ms], dev, world)
+    ms_step = ms_total / K_
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             peak, peak_kind = float(json.load(f)["bf16_tflops"]), "measured bf16_tflops (burst; fp16 runs at the bf16 rate)"
@@ -361,7 +375,7 @@ def run_prefill(args, spec):
                "kind": "oracle", "sample": f"{passes} oracle passes of 16 of the 2048 tokens against the full "
                                            f"9728x2560 Q4_K matrix in {el:.1f} s (fp64 scalar, OpenMP over rows)"}
     if rank == 0:
-        value = world * flops / (ms_step * 1e-3) / 1e12
+        value = replica_rate(world, flops, ms_step) / 1e12
         achieved = flops / (call_ms * 1e-3) / 1e12
         line = {
             "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K_,
@@ -485,10 +499,7 @@ def run_decode(args, spec):
         e1.record()
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / n_e2e
-    t = torch.tensor([ms_step, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_step, e2e_ms = float(t[0]), float(t[1])
+    ms_step, e2e_ms = max_over_ranks([ms_step, e2e_ms], dev, world)
     peak, peak_kind = measured_peaks()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -499,7 +510,7 @@ def run_decode(args, spec):
                "sample": f"{passes} passes over one layer's four Q4_K matrices (fp64 scalar oracle GEMV, "
                          f"OpenMP over rows, M={M}) in {el:.1f} s"}
     if rank == 0:
-        value = world * wbytes / (ms_step * 1e-3) / 1e9
+        value = replica_rate(world, wbytes, ms_step) / 1e9
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -687,12 +698,9 @@ def main():
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
     # ---- reduce over ranks (max time)
-    t = torch.tensor([ms_total, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_total, e2e_ms = float(t[0]), float(t[1])
+    ms_total, e2e_ms = max_over_ranks([ms_total, e2e_ms], dev, world)
     ms_step = ms_total / K_
-    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    value = replica_rate(world, step_bytes, ms_step) / 1e9
 
     flat = np.array(durs).reshape(K_, -1)
     isolated_ms = float(flat.mean())
