@@ -6,6 +6,9 @@
 // written out from the definitions, in fp64, one weight at a time.
 //
 // What it computes (sources are the engine READMEs this library follows):
+//  (Q5_K, the next GGUF k-quant after Q4_K, follows GGUF's published Q5_K layout for
+//  the same reason as Q4_K: GGUF files are to work unchanged; Q4_K_M files mix in
+//  higher-precision k-quant tensors.)
 //  * Kinetic README, "What makes it fast": a dense model reads all of its
 //    weights once per token; a speculative check runs every guess through one
 //    pass over the weights. The result of that pass is the plain product
@@ -37,7 +40,7 @@
 
 namespace {
 
-enum { ORC_Q8_0 = 1, ORC_Q4_K = 2, ORC_AFFINE4 = 3 };
+enum { ORC_Q8_0 = 1, ORC_Q4_K = 2, ORC_AFFINE4 = 3, ORC_Q5_K = 4 };
 enum { ORC_F32 = 1, ORC_BF16 = 2 };
 
 // ---------------------------------------------------------------- fp16 ----
@@ -119,11 +122,11 @@ uint16_t rd16(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] << 8)); }
 void wr16(uint8_t* p, uint16_t v) { p[0] = (uint8_t)(v & 0xFF); p[1] = (uint8_t)(v >> 8); }
 
 int block_bytes(int fmt) {
-  switch (fmt) { case ORC_Q8_0: return 34; case ORC_Q4_K: return 144; case ORC_AFFINE4: return 20; }
+  switch (fmt) { case ORC_Q8_0: return 34; case ORC_Q4_K: return 144; case ORC_AFFINE4: return 20; case ORC_Q5_K: return 176; }
   return 0;
 }
 int block_weights(int fmt) {
-  switch (fmt) { case ORC_Q8_0: return 32; case ORC_Q4_K: return 256; case ORC_AFFINE4: return 32; }
+  switch (fmt) { case ORC_Q8_0: return 32; case ORC_Q4_K: return 256; case ORC_AFFINE4: return 32; case ORC_Q5_K: return 256; }
   return 0;
 }
 
@@ -269,6 +272,103 @@ void deq_q4_k(const uint8_t* blk, double* out) {
   }
 }
 
+// ---------------------------------------------------------------- Q5_K ----
+// 176 bytes: d (fp16), dmin (fp16), scales[12] (packed exactly as in Q4_K), qh[32],
+// qs[128]. The low four bits of weight i sit where Q4_K keeps its code (chunk c = i/64,
+// l = i%32: low nibble of qs[32c + l] for i%64 < 32, high nibble otherwise); the fifth
+// bit is bit (2c + (i%64 >= 32)) of qh[l]. q = low4 + 16*bit5 in 0..31.
+// w = d * sc_j * q - dmin * m_j, sub-block j = i/32 as in Q4_K.
+int code_q5_k(const uint8_t* blk, int i) {
+  const int c = i / 64, r = i % 64, l = r % 32;
+  const int low4 = code_q4_k(blk + 48, i);
+  const int bit5 = (blk[16 + l] >> (2 * c + (r >= 32 ? 1 : 0))) & 1;
+  return low4 + 16 * bit5;
+}
+// Quantizer: the Q4_K covering scheme with 31 levels per step:
+//  dmin = smallest fp16 >= max(mraw)/63, m_j = ceil(mraw_j / dmin), t_j = hi_j + dmin*m_j,
+//  d = smallest fp16 >= max(t)/(63*31), sc_j = ceil(t_j / (31 d)),
+//  q = round_half_away((w + dmin*m_j) / (d*sc_j)), which lies in [0, 31].
+void quant_q5_k(const float* w, uint8_t* blk) {
+  double lo[8], hi[8], mraw[8];
+  for (int j = 0; j < 8; ++j) {
+    lo[j] = 0.0; hi[j] = 0.0;
+    for (int i = 0; i < 32; ++i) {
+      const double v = (double)w[32 * j + i];
+      lo[j] = std::min(lo[j], v);
+      hi[j] = std::max(hi[j], v);
+    }
+    mraw[j] = -lo[j];
+  }
+  double maxm = 0.0;
+  for (int j = 0; j < 8; ++j) maxm = std::max(maxm, mraw[j]);
+  uint16_t dmin16 = 0;
+  int m[8] = {0};
+  if (maxm > 0.0) {
+    dmin16 = double_to_half_up(maxm / 63.0);
+    for (;;) {
+      const double dmin = half_to_double(dmin16);
+      bool ok = true;
+      for (int j = 0; j < 8; ++j) {
+        m[j] = (int)std::ceil(mraw[j] / dmin);
+        if (m[j] > 63) ok = false;
+      }
+      if (ok) break;
+      dmin16 = half_next_up(dmin16);
+    }
+  }
+  const double dmin = half_to_double(dmin16);
+  double t[8], maxt = 0.0;
+  for (int j = 0; j < 8; ++j) {
+    t[j] = hi[j] + dmin * (double)m[j];
+    maxt = std::max(maxt, t[j]);
+  }
+  uint16_t d16 = 0;
+  int sc[8] = {0};
+  if (maxt > 0.0) {
+    d16 = double_to_half_up(maxt / (63.0 * 31.0));
+    for (;;) {
+      const double d = half_to_double(d16);
+      bool ok = true;
+      for (int j = 0; j < 8; ++j) {
+        sc[j] = (int)std::ceil(t[j] / (31.0 * d));
+        if (sc[j] > 63) ok = false;
+      }
+      if (ok) break;
+      d16 = half_next_up(d16);
+    }
+  }
+  const double d = half_to_double(d16);
+  wr16(blk + 0, d16);
+  wr16(blk + 2, dmin16);
+  pack_scale_min(sc, m, blk + 4);
+  uint8_t* qh = blk + 16;
+  uint8_t* qs = blk + 48;
+  std::memset(qh, 0, 32);
+  std::memset(qs, 0, 128);
+  for (int i = 0; i < 256; ++i) {
+    const int j = i / 32;
+    const double step = d * (double)sc[j];
+    int q = 0;
+    if (step != 0.0) {
+      const double r = std::round(((double)w[i] + dmin * (double)m[j]) / step);
+      q = (int)std::min(31.0, std::max(0.0, r));
+    }
+    const int c = i / 64, r = i % 64, l = r % 32;
+    if (r < 32) qs[32 * c + l] |= (uint8_t)(q & 15);
+    else qs[32 * c + l] |= (uint8_t)((q & 15) << 4);
+    if (q & 16) qh[l] |= (uint8_t)(1u << (2 * c + (r >= 32 ? 1 : 0)));
+  }
+}
+void deq_q5_k(const uint8_t* blk, double* out) {
+  const double d = half_to_double(rd16(blk + 0));
+  const double dmin = half_to_double(rd16(blk + 2));
+  for (int i = 0; i < 256; ++i) {
+    int sc, m;
+    unpack_scale_min(blk + 4, i / 32, &sc, &m);
+    out[i] = d * (double)sc * (double)code_q5_k(blk, i) - dmin * (double)m;
+  }
+}
+
 // ------------------------------------------------------------- affine4 ----
 // 20 bytes: s (fp16), b (fp16), codes[16]; weight 2i = low nibble of codes[i],
 // weight 2i+1 = high nibble. w = s * q + b.
@@ -303,6 +403,7 @@ void deq_affine4(const uint8_t* blk, double* out) {
 void deq_block(int fmt, const uint8_t* blk, double* out) {
   if (fmt == ORC_Q8_0) deq_q8_0(blk, out);
   else if (fmt == ORC_Q4_K) deq_q4_k(blk, out);
+  else if (fmt == ORC_Q5_K) deq_q5_k(blk, out);
   else deq_affine4(blk, out);
 }
 void deq_row(int fmt, const uint8_t* row, int64_t K, double* out) {
@@ -339,6 +440,7 @@ int orc_quantize(int fmt, const float* w, int64_t N, int64_t K, uint8_t* blocks,
       uint8_t* dst = blocks + (n * nb + b) * bb;
       if (fmt == ORC_Q8_0) quant_q8_0(src, dst);
       else if (fmt == ORC_Q4_K) quant_q4_k(src, dst);
+      else if (fmt == ORC_Q5_K) quant_q5_k(src, dst);
       else quant_affine4(src, dst);
     }
   }

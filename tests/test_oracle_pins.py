@@ -15,7 +15,7 @@ import pytest
 from conftest import load_golden
 from quantized_decode_gemv_block_gb300 import inputs
 
-Q8_0, Q4_K, AFFINE4 = 1, 2, 3
+Q8_0, Q4_K, AFFINE4, Q5_K = 1, 2, 3, 4
 
 
 # ------------------------------------------------------------------- fp16 --
@@ -72,7 +72,9 @@ def test_block_sizes(orc):
     assert (orc.block_bytes(Q8_0), orc.block_weights(Q8_0)) == (34, 32)
     assert (orc.block_bytes(Q4_K), orc.block_weights(Q4_K)) == (144, 256)
     assert (orc.block_bytes(AFFINE4), orc.block_weights(AFFINE4)) == (20, 32)
+    assert (orc.block_bytes(Q5_K), orc.block_weights(Q5_K)) == (176, 256)
     for K in (256, 2048, 2560, 9728):
+        assert orc.row_bytes(Q5_K, K) == K * 11 // 16
         assert orc.row_bytes(Q8_0, K) == K * 17 // 16
         assert orc.row_bytes(Q4_K, K) == K * 9 // 16
         assert orc.row_bytes(AFFINE4, K) == K * 5 // 8
@@ -112,6 +114,46 @@ def test_q4_k_worked_example(orc):
     assert (y[0, 0], ay[0, 0]) == (7768984.0, 7871992.0)
 
 
+def _q5k_from_q4k(q4k_block: bytes, qh: bytes) -> bytes:
+    """A Q5_K block with Q4_K's header (d, dmin, packed scales) and 4-bit codes plus the
+    given 32 bytes of fifth bits: 16 header bytes, qh[32], then the 128 code bytes."""
+    assert len(q4k_block) == 144 and len(qh) == 32
+    return q4k_block[:16] + qh + q4k_block[16:]
+
+
+def test_q5_k_reduces_to_q4_k_without_fifth_bits(orc):
+    """With every fifth bit clear, Q5_K's w = d*sc*q - dmin*m is Q4_K's on the same bytes."""
+    blk4, _ = load_golden("q4k_e2.txt")
+    blk5 = _q5k_from_q4k(blk4, bytes(32))
+    w4 = orc.dequant(Q4_K, np.frombuffer(blk4, np.uint8).reshape(1, 144), 1, 256)[0]
+    w5 = orc.dequant(Q5_K, np.frombuffer(blk5, np.uint8).reshape(1, 176), 1, 256)[0]
+    assert np.array_equal(w4, w5)
+
+
+def test_q5_k_fifth_bit_positions(orc):
+    """Hand-placed fifth bits. GGUF's Q5_K keeps the fifth bit of weight i in bit
+    2c + h of qh[l], c = i // 64, h = 1 for the high-nibble half (i % 64 >= 32), l = i % 32:
+    qh[0] bit 0 -> weight 0, qh[1] bit 1 -> weight 33, qh[2] bit 2 -> weight 66,
+    qh[31] bit 7 -> weight 255. Exactly those weights gain 16*d*sc_j."""
+    blk4, f = load_golden("q4k_e2.txt")
+    d, sc = f["d"][0], [int(v) for v in f["sc"]]
+    qh = bytearray(32)
+    qh[0], qh[1], qh[2], qh[31] = 0x01, 0x02, 0x04, 0x80
+    w4 = orc.dequant(Q4_K, np.frombuffer(blk4, np.uint8).reshape(1, 144), 1, 256)[0]
+    w5 = orc.dequant(Q5_K, np.frombuffer(_q5k_from_q4k(blk4, bytes(qh)), np.uint8).reshape(1, 176), 1, 256)[0]
+    diff = w5 - w4
+    hit = {0, 33, 66, 255}
+    for i in range(256):
+        assert diff[i] == (16 * d * sc[i // 32] if i in hit else 0.0), i
+    # every fifth bit set: every weight gains 16*d*sc_j; x = 1 then adds 16*32*d*sum(sc)
+    w_all = orc.dequant(Q5_K, np.frombuffer(_q5k_from_q4k(blk4, bytes([0xFF] * 32)), np.uint8).reshape(1, 176),
+                        1, 256)[0]
+    assert np.array_equal(w_all - w4, np.array([16 * d * sc[i // 32] for i in range(256)]))
+    b = np.frombuffer(_q5k_from_q4k(blk4, bytes([0xFF] * 32)), np.uint8).reshape(1, 176)
+    y, _ = orc.gemv(Q5_K, b, np.ones((1, 256), np.float32), 1, 256)
+    assert y[0, 0] == 38480 + 16 * 32 * d * sum(sc)  # Q4_K example's sum (tests/golden) + the fifth bits
+
+
 def test_affine4_nibble_order(orc):
     """Hand-built group: s = 2, b = -1, codes byte i = (2i mod 16) | ((2i+1 mod 16) << 4)."""
     blk = bytes([0x00, 0x40, 0x00, 0xBC]) + bytes(((2 * i) % 16) | ((((2 * i) + 1) % 16) << 4)
@@ -131,7 +173,7 @@ def _adversarial_blocks(bw, rng):
     return np.stack(rows).astype(np.float32)
 
 
-@pytest.mark.parametrize("fmt", [Q8_0, Q4_K, AFFINE4])
+@pytest.mark.parametrize("fmt", [Q8_0, Q4_K, AFFINE4, Q5_K])
 def test_round_trip_bound(orc, fmt):
     """|w - deq(q(w))| <= step/2 for every block (the quantizer's covering bound)."""
     bw, bb = orc.block_weights(fmt), orc.block_bytes(fmt)
@@ -158,7 +200,7 @@ def test_round_trip_bound(orc, fmt):
             q = b[2:].view(np.int8)
             assert q.min() >= -127
             assert d == float(np.float16(np.abs(w[r].astype(np.float64)).max() / 127))
-        elif fmt == Q4_K:
+        elif fmt in (Q4_K, Q5_K):
             d = orc.half_to_double(int(b[0]) | (int(b[1]) << 8))
             dmin = orc.half_to_double(int(b[2]) | (int(b[3]) << 8))
             for j in range(8):
@@ -189,7 +231,7 @@ def test_q8_0_codes_match_exact_rounding(orc):
 
 
 # ------------------------------------------------------------------- gemv --
-@pytest.mark.parametrize("fmt", [Q8_0, Q4_K, AFFINE4])
+@pytest.mark.parametrize("fmt", [Q8_0, Q4_K, AFFINE4, Q5_K])
 @pytest.mark.parametrize("K", [256, 512])
 def test_gemv_brute_force(orc, fmt, K):
     """Oracle GEMV == numpy dense fp64 matmul of the dequantized matrix (other summation order)."""
