@@ -42,8 +42,13 @@ extern "C" {
  *                weight 64c+l in its low nibble and 64c+32+l in its high nibble);
  *                w = d*sc_j*q - dmin*m_j for sub-block j = weight/32
  * KQ_AFFINE4_G32 20 bytes / 32 weights: fp16 s, fp16 b, codes[16] (weight 2i in the
- *                low nibble of byte i, weight 2i+1 in the high nibble); w = s*q + b */
-enum kq_fmt { KQ_Q8_0 = 1, KQ_Q4_K = 2, KQ_AFFINE4_G32 = 3 };
+ *                low nibble of byte i, weight 2i+1 in the high nibble); w = s*q + b
+ * KQ_Q5_K       176 bytes / 256 weights: Q4_K's d, dmin and scales[12], then qh[32],
+ *                then Q4_K's qs[128] holding the low four code bits; the fifth bit of
+ *                weight 64c+32h+l (c = 0..3, h = 0/1, l = 0..31) is bit 2c+h of qh[l];
+ *                codes 0..31, w = d*sc_j*q - dmin*m_j (GGUF's Q5_K; the next k-quant
+ *                that Q4_K_M model files mix in) */
+enum kq_fmt { KQ_Q8_0 = 1, KQ_Q4_K = 2, KQ_AFFINE4_G32 = 3, KQ_Q5_K = 4 };
 
 /* Activation element types. */
 enum kq_dtype { KQ_F32 = 1, KQ_BF16 = 2 };
@@ -77,7 +82,7 @@ const char* kq_version(void);
 int kq_device_errors(void);
 
 /* Quantized GEMV / speculative-verify product (Kinetic README, "What makes it fast").
- *   fmt       KQ_Q8_0, KQ_Q4_K or KQ_AFFINE4_G32
+ *   fmt       KQ_Q8_0, KQ_Q4_K, KQ_AFFINE4_G32 or KQ_Q5_K
  *   w_blocks  N * kq_row_bytes(fmt, K) bytes, 16-byte aligned
  *   x_dtype   KQ_BF16 (tensor-core path) or KQ_F32 (CUDA-core path)
  *   x         M x K activations, 16-byte aligned
@@ -132,6 +137,8 @@ size_t kq_gemm_workspace_size(int fmt, int x_dtype, int M, int N, int K);
  *            dmin = smallest fp16 >= max(-lo)/63, m_j = ceil(-lo_j/dmin);
  *            t_j = hi_j + dmin*m_j, d = smallest fp16 >= max(t)/945,
  *            sc_j = ceil(t_j/(15 d)), q = round_half_away((w + dmin*m_j)/(d*sc_j))
+ *   Q5_K:    as Q4_K with 31 levels: d = smallest fp16 >= max(t)/1953,
+ *            sc_j = ceil(t_j/(31 d)), q = round_half_away((w + dmin*m_j)/(d*sc_j)) in 0..31
  *   AFFINE4: b = largest fp16 <= min w, s = smallest fp16 >= (max w - b)/15,
  *            q = clamp(round_half_away((w - b)/s), 0, 15)
  * These make data for tests and benchmarks (the GEMV never quantizes). K must be a

@@ -53,6 +53,32 @@ __device__ __forceinline__ void decode_slice(const uint8_t* unit, int gi, int q,
       c[k] = static_cast<float>((b.x >> (8 * k + nsh)) & 15u);
       c[4 + k] = static_cast<float>((b.y >> (8 * k + nsh)) & 15u);
     }
+  } else if (FMT == FMT_Q5_K) {  // Q4_K's scales; low nibbles at 48, fifth bits (bit gi of qh[l]) at 16
+    const uint4 h = ldg128(unit);
+    const int ch = gi >> 1;
+    const uint2 b = ldg64(unit + 48 + 32 * ch + 8 * q);
+    const uint2 hb = ldg64(unit + 16 + 8 * q);
+    const uint32_t s0 = h.y, s1 = h.z, s2 = h.w;
+    uint32_t scw, mw;
+    if (gi < 4) {
+      scw = s0 & 0x3F3F3F3Fu;
+      mw = s1 & 0x3F3F3F3Fu;
+    } else {
+      scw = (s2 & 0x0F0F0F0Fu) | ((s0 >> 2) & 0x30303030u);
+      mw = ((s2 >> 4) & 0x0F0F0F0Fu) | ((s1 >> 2) & 0x30303030u);
+    }
+    const int sh = 8 * (gi & 3);
+    const float sc = static_cast<float>((scw >> sh) & 0xFFu);
+    const float m = static_cast<float>((mw >> sh) & 0xFFu);
+    const float d = half_bits_to_float(h.x), dmin = half_bits_to_float(h.x >> 16);
+    scale = d * sc;      // exact: 11-bit x 6-bit
+    offset = -dmin * m;  // exact
+    const int nsh = (gi & 1) ? 4 : 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      c[k] = static_cast<float>(((b.x >> (8 * k + nsh)) & 15u) | (((hb.x >> (8 * k + gi)) & 1u) << 4));
+      c[4 + k] = static_cast<float>(((b.y >> (8 * k + nsh)) & 15u) | (((hb.y >> (8 * k + gi)) & 1u) << 4));
+    }
   } else if (FMT == FMT_Q8_0) {
     const uint8_t* blk = unit + 34 * gi;
     scale = half_bits_to_float(ldg16(blk));
@@ -79,7 +105,7 @@ __device__ __forceinline__ void decode_slice(const uint8_t* unit, int gi, int q,
 
 template <int FMT>
 constexpr int unit_bytes() {
-  return FMT == FMT_Q4_K ? 144 : (FMT == FMT_Q8_0 ? 272 : 160);
+  return FMT == FMT_Q4_K ? 144 : (FMT == FMT_Q5_K ? 176 : (FMT == FMT_Q8_0 ? 272 : 160));
 }
 
 template <int FMT, int MT>
@@ -122,7 +148,7 @@ __global__ void __launch_bounds__(kThreadsF) gemv_f32_kernel(const uint8_t* __re
 #pragma unroll
           for (int k = 0; k < 8; ++k) p = __fmaf_rn(c[i][k], xv[k], p);
           acc[i][j] = __fmaf_rn(sc[i], p, acc[i][j]);
-          if (FMT != FMT_Q8_0) acc[i][j] = __fmaf_rn(off[i], s, acc[i][j]);
+          if (FMT != FMT_Q8_0) acc[i][j] = __fmaf_rn(off[i], s, acc[i][j]);  // min / bias
         }
       }
     }
@@ -160,6 +186,7 @@ int launch_gemv_f32(int fmt, const void* w, const float* x, float* y, int M, int
     case FMT_Q4_K: launch_fmt<FMT_Q4_K>(wb, x, y, M, N, K, row_bytes, stream); break;
     case FMT_Q8_0: launch_fmt<FMT_Q8_0>(wb, x, y, M, N, K, row_bytes, stream); break;
     case FMT_AFFINE4: launch_fmt<FMT_AFFINE4>(wb, x, y, M, N, K, row_bytes, stream); break;
+    case FMT_Q5_K: launch_fmt<FMT_Q5_K>(wb, x, y, M, N, K, row_bytes, stream); break;
     default: *err = "unsupported format"; return -1;
   }
   const cudaError_t e = cudaGetLastError();

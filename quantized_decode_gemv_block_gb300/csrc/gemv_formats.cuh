@@ -104,6 +104,94 @@ struct FmtQ4K {
   }
 };
 
+// ------------------------------------------------------------------ Q5_K --
+// One unit = one 176-byte super-block: Q4_K's 16-byte header (d, dmin, packed 6-bit
+// scales and mins), qh[32] (the fifth code bit of weight i is bit 2c + h of qh[i % 32],
+// c = i/64, h = 1 for the high-nibble half; i.e. bit b for sub-block b), then Q4_K's 128
+// bytes of low nibbles. Codes 0..31, w = d*sc*q - dmin*m.
+struct FmtQ5K {
+  static constexpr bool kHalfX = false;
+  static constexpr int kUnitBytes = 176;
+  static constexpr bool kPerm0213 = false;
+  static constexpr bool kNeedsSum = true;
+  struct Raw {
+    uint4 h[2];
+    uint2 qs[2][4];
+    uint2 qh[2];  // fifth bits of weights 8q..8q+7 of every sub-block (bit b for sub-block b)
+  };
+  template <class Ld>
+  __device__ static void load(Raw& r, const uint8_t* pa, const uint8_t* pb, int q) {
+    r.h[0] = Ld::v128(pa);
+    r.h[1] = Ld::v128(pb);
+    r.qh[0] = Ld::v64(pa + 16 + 8 * q);
+    r.qh[1] = Ld::v64(pb + 16 + 8 * q);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      r.qs[0][c] = Ld::v64(pa + 48 + 32 * c + 8 * q);
+      r.qs[1][c] = Ld::v64(pb + 48 + 32 * c + 8 * q);
+    }
+  }
+  // 4-bit codes -> bf16 pairs: slots (2q, 2q+1) <- bytes (0,1), (2q+8, 2q+9) <- bytes (2,3).
+  template <int NT>
+  __device__ static void compute(const Raw& r, float (&acc)[NT][4], const uint16_t* xs_unit,
+                                 int xstride, const float* s_unit, int lane, int M) {
+    constexpr int T = 8 * NT;
+    const int g = lane >> 2, q = lane & 3;
+    uint32_t sc_lo[2], sc_hi[2], m_lo[2], m_hi[2];
+    float d[2], nd[2], dmin[2], pdmin[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint32_t s0 = r.h[i].y, s1 = r.h[i].z, s2 = r.h[i].w;
+      sc_lo[i] = s0 & 0x3F3F3F3Fu;
+      m_lo[i] = s1 & 0x3F3F3F3Fu;
+      sc_hi[i] = (s2 & 0x0F0F0F0Fu) | ((s0 >> 2) & 0x30303030u);
+      m_hi[i] = ((s2 >> 4) & 0x0F0F0F0Fu) | ((s1 >> 2) & 0x30303030u);
+      d[i] = half_bits_to_float(r.h[i].x);
+      dmin[i] = half_bits_to_float(r.h[i].x >> 16);
+      nd[i] = -8388608.f * d[i];
+      pdmin[i] = 8388608.f * dmin[i];
+    }
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const int c = b >> 1;
+      uint32_t a0[4], a1[4];
+      float ds[2], ndm[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint32_t w0 = r.qs[i][c].x, w1 = r.qs[i][c].y;
+        // 5-bit codes: the nibble plus 16 * (bit b of the weight's qh byte), each < 32
+        const uint32_t n0 = ((b & 1) ? ((w0 >> 4) & 0x0F0F0F0Fu) : (w0 & 0x0F0F0F0Fu)) |
+                            (((r.qh[i].x >> b) & 0x01010101u) << 4);
+        const uint32_t n1 = ((b & 1) ? ((w1 >> 4) & 0x0F0F0F0Fu) : (w1 & 0x0F0F0F0Fu)) |
+                            (((r.qh[i].y >> b) & 0x01010101u) << 4);
+        a0[i] = bf16x2_sub(prmt(n0, kBf16Magic, 0x4140u), kBf16x2_128);
+        a0[i + 2] = bf16x2_sub(prmt(n0, kBf16Magic, 0x4342u), kBf16x2_128);
+        a1[i] = bf16x2_sub(prmt(n1, kBf16Magic, 0x4140u), kBf16x2_128);
+        a1[i + 2] = bf16x2_sub(prmt(n1, kBf16Magic, 0x4342u), kBf16x2_128);
+        const uint32_t scw = (b < 4) ? sc_lo[i] : sc_hi[i];
+        const uint32_t mw = (b < 4) ? m_lo[i] : m_hi[i];
+        ds[i] = scaled_byte(scw, b & 3, d[i], nd[i]);          //  d * sc_b (exact)
+        ndm[i] = scaled_byte(mw, b & 3, -dmin[i], pdmin[i]);   // -dmin * m_b (exact)
+      }
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int tok = 8 * t + g;
+        uint4 xb = make_uint4(0u, 0u, 0u, 0u);
+        if (tok < M) xb = lds128(xs_unit + tok * xstride + 32 * b + 8 * q);
+        const float z[4] = {0.f, 0.f, 0.f, 0.f};
+        float p[4];
+        mma_bf16_16816(p, a0, xb.x, xb.y, z);
+        mma_bf16_16816(p, a1, xb.z, xb.w, p);
+        const float2 sv = lds_f2(s_unit + b * T + 8 * t + 2 * q);
+        acc[t][0] = __fmaf_rn(ndm[0], sv.x, __fmaf_rn(ds[0], p[0], acc[t][0]));
+        acc[t][1] = __fmaf_rn(ndm[0], sv.y, __fmaf_rn(ds[0], p[1], acc[t][1]));
+        acc[t][2] = __fmaf_rn(ndm[1], sv.x, __fmaf_rn(ds[1], p[2], acc[t][2]));
+        acc[t][3] = __fmaf_rn(ndm[1], sv.y, __fmaf_rn(ds[1], p[3], acc[t][3]));
+      }
+    }
+  }
+};
+
 // ------------------------------------------------------------------ Q8_0 --
 // One unit = 8 blocks of 34 bytes = 272 bytes, read as 4 pairs of 68 bytes. The
 // even block of a pair starts on a 4-byte boundary (its codes 2 bytes after it),
@@ -254,6 +342,7 @@ template <int FMT> struct FmtOf;
 template <> struct FmtOf<FMT_Q4_K> { using type = FmtQ4K; };
 template <> struct FmtOf<FMT_Q8_0> { using type = FmtQ8_0; };
 template <> struct FmtOf<FMT_AFFINE4> { using type = FmtAffine4; };
+template <> struct FmtOf<FMT_Q5_K> { using type = FmtQ5K; };
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -362,6 +451,169 @@ struct FmtQ4KH {
         alo[i + 2] = h2_fma(and_or(w8, 0x000F000Fu, kMagic), sa[i], nsa[i]);
         ahi[i] = h2_fma(and_or(w, 0x00F000F0u, kMagic), sb16[i], nsb64[i]);
         ahi[i + 2] = h2_fma(and_or(w8, 0x00F000F0u, kMagic), sb16[i], nsb64[i]);
+      }
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int tok = 8 * t + g;
+        // chunk i = k/2 holds MMAs 2i, 2i+1 of the low half; chunk 4 + k/2 of the high half
+        const uint8_t* base = xh_unit + xo[t];
+        const uint4 xlo = *reinterpret_cast<const uint4*>(base + 64 * (k >> 1));
+        const uint4 xhi = *reinterpret_cast<const uint4*>(base + 64 * (4 + (k >> 1)));
+        const uint32_t bl0 = (k & 1) ? xlo.z : xlo.x, bl1 = (k & 1) ? xlo.w : xlo.y;
+        const uint32_t bh0 = (k & 1) ? xhi.z : xhi.x, bh1 = (k & 1) ? xhi.w : xhi.y;
+        const int c = 2 * (k & 1);
+        mma_f16_16816(p[t][c], alo, bl0, bl1, p[t][c]);
+        mma_f16_16816(p[t][c + 1], ahi, bh0, bh1, p[t][c + 1]);
+      }
+    }
+    // min term: A2 slots (2q, 2q+1) = m_2q, (2q+8, 2q+9) = m_2q+1; B2 = S/64 hi/lo parts
+    const uint32_t a2[4] = {ma[0], ma[1], mb[0], mb[1]};
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const int tok = 8 * t + g;
+      const uint2 b2 = *reinterpret_cast<const uint2*>(s2_unit + so[t]);
+      const float z[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_f16_16816(mnv[t], a2, b2.x, b2.y, z);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) ps[t][e] = (p[t][0][e] + p[t][1][e]) + (p[t][2][e] + p[t][3][e]);
+    }
+  }
+
+  // acc += d*ps - 64*dmin*mn, rows g (elements 0, 1) and g+8 (elements 2, 3)
+  template <int NT>
+  __device__ static void promote(float (&acc)[NT][4], const float (&ps)[NT][4], const float (&mnv)[NT][4],
+                                 const float (&d)[2], const float (&dmin)[2]) {
+    const float nd0 = -64.f * dmin[0], nd1 = -64.f * dmin[1];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      acc[t][0] = __fmaf_rn(nd0, mnv[t][0], __fmaf_rn(d[0], ps[t][0], acc[t][0]));
+      acc[t][1] = __fmaf_rn(nd0, mnv[t][1], __fmaf_rn(d[0], ps[t][1], acc[t][1]));
+      acc[t][2] = __fmaf_rn(nd1, mnv[t][2], __fmaf_rn(d[1], ps[t][2], acc[t][2]));
+      acc[t][3] = __fmaf_rn(nd1, mnv[t][3], __fmaf_rn(d[1], ps[t][3], acc[t][3]));
+    }
+  }
+
+  template <int NT>
+  __device__ static void compute(const Raw& r, float (&acc)[NT][4], const uint8_t* xh_unit,
+                                 const int (&xo)[NT], const uint8_t* s2_unit, const int (&so)[NT],
+                                 int lane) {
+    float ps[NT][4], mnv[NT][4], d[2], dmin[2];
+    sums<NT>(r, xh_unit, xo, s2_unit, so, lane, ps, mnv, d, dmin);
+    promote<NT>(acc, ps, mnv, d, dmin);
+  }
+
+  // Two consecutive super-blocks (x and min-term operands of the second 512 and 32 bytes
+  // further on); the same arithmetic, in the same order, as two compute() calls.
+  template <int NT>
+  __device__ static void compute2(const Raw& r0, const Raw& r1, float (&acc)[NT][4],
+                                  const uint8_t* xh_unit, const int (&xo)[NT], const uint8_t* s2_unit,
+                                  const int (&so)[NT], int lane) {
+    float ps0[NT][4], mn0[NT][4], d0[2], dm0[2], ps1[NT][4], mn1[NT][4], d1[2], dm1[2];
+    sums<NT>(r0, xh_unit, xo, s2_unit, so, lane, ps0, mn0, d0, dm0);
+    sums<NT>(r1, xh_unit + 512, xo, s2_unit + 32, so, lane, ps1, mn1, d1, dm1);
+    promote<NT>(acc, ps0, mn0, d0, dm0);
+    promote<NT>(acc, ps1, mn1, d1, dm1);
+  }
+};
+
+// ------------------------------------------------------- Q5_K, fp16 path --
+// FmtQ4KH's arithmetic with 5-bit codes: the fifth bit joins the code inside the fp16
+// magic word before the fma that forms sc*q (<= 63*31 = 1953, still an exact fp16
+// integer; the fused fma rounds once, so (1024 + 31)*63 never has to fit fp16).
+struct FmtQ5KH {
+  static constexpr bool kHalfX = true;
+  static constexpr bool kPerm0213 = false;
+  static constexpr bool kNeedsSum = false;
+  static constexpr int kUnitBytes = 176;
+  struct Raw {
+    uint4 h[2];
+    uint4 c[2][2];
+    uint4 qh[2][2];  // all 32 fifth-bit bytes of each row (thread q needs bits 2q, 2q+1)
+  };
+  template <class Ld>
+  __device__ static void load(Raw& r, const uint8_t* pa, const uint8_t* pb, int q) {
+    r.h[0] = Ld::v128(pa);
+    r.h[1] = Ld::v128(pb);
+    r.qh[0][0] = Ld::v128(pa + 16);
+    r.qh[0][1] = Ld::v128(pa + 32);
+    r.qh[1][0] = Ld::v128(pb + 16);
+    r.qh[1][1] = Ld::v128(pb + 32);
+    r.c[0][0] = Ld::v128(pa + 48 + 32 * q);
+    r.c[0][1] = Ld::v128(pa + 64 + 32 * q);
+    r.c[1][0] = Ld::v128(pb + 48 + 32 * q);
+    r.c[1][1] = Ld::v128(pb + 64 + 32 * q);
+  }
+  // Byte offset, within one token's 512-byte super-block slot, of the 16-byte chunk i
+  // (0..7) of thread q: the quad's four chunks i sit side by side (64 bytes), and tokens
+  // are 64 bytes apart modulo 128, so a quarter-warp's loads hit 32 distinct banks.
+  __device__ static int chunk_off(int q, int i) { return 64 * i + 16 * q; }
+
+  // xh_unit: token 0's slot of this super-block; xts: token stride (bytes).
+  // s2_unit: token 0's min-term operands of this super-block; s2ts: their token stride.
+  // The fp32 sums of one super-block: ps = sum (sc*q)*x per (row, token) and mn = sum m*S/64.
+  // xo[t] / so[t]: byte offsets of this thread's token row in tile t within the staged x
+  // and min-term operands (absent tokens point at the zero row), 16q / 8q included.
+  template <int NT>
+  __device__ static void sums(const Raw& r, const uint8_t* xh_unit, const int (&xo)[NT],
+                              const uint8_t* s2_unit, const int (&so)[NT], int lane,
+                              float (&ps)[NT][4], float (&mnv)[NT][4], float (&d)[2], float (&dmin)[2]) {
+    const int g = lane >> 2, q = lane & 3;
+    const uint32_t kMagic = 0x64006400u;   // fp16 1024 in both halves
+    uint32_t sa[2], nsa[2], sb16[2], nsb64[2], ma[2], mb[2];
+    // Thread q needs sub-blocks j = 2q and 2q+1. For j < 4 (q < 2): sc = scales[j] & 63,
+    // m = scales[j+4] & 63. For j >= 4 (q >= 2): sc = (scales[j+4] & 15) | (scales[j-4] >> 6) << 4,
+    // m = (scales[j+4] >> 4) | (scales[j] >> 6) << 4. One permute gathers, per thread,
+    // bytes (sc_a, sc_b, m_a, m_b) of the low form and one the high-bit sources.
+    const uint32_t ja = static_cast<uint32_t>((2 * q) & 3);
+    // low form: q < 2 -> [s0.ja, s0.ja+1, s1.ja, s1.ja+1]; q >= 2 -> [s2.ja, s2.ja+1, s2.ja, s2.ja+1]
+    const uint32_t sel_lo = q < 2 ? (ja | ((ja + 1) << 4) | ((ja + 4) << 8) | ((ja + 5) << 12))
+                                  : (ja | ((ja + 1) << 4) | (ja << 8) | ((ja + 1) << 12));
+    // high bits (q >= 2): [s0.ja, s0.ja+1, s1.ja, s1.ja+1] >> 6 << 4
+    const uint32_t sel_hi = ja | ((ja + 1) << 4) | ((ja + 4) << 8) | ((ja + 5) << 12);
+    const uint32_t pa_sel = 0x4040u, pb_sel = 0x4141u, pma_sel = 0x4242u, pmb_sel = 0x4343u;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint32_t s0 = r.h[i].y, s1 = r.h[i].z, s2 = r.h[i].w;
+      // bytes: sc_2q, sc_2q+1, m_2q, m_2q+1 (both forms computed, one selected: no branch)
+      const uint32_t v6 = prmt(s0, s1, sel_lo) & 0x3F3F3F3Fu;
+      const uint32_t lo = prmt(s2, s2, sel_lo);
+      const uint32_t hb = (prmt(s0, s1, sel_hi) >> 2) & 0x30303030u;
+      const uint32_t v4 = (((lo & 0x0000FFFFu) | ((lo >> 4) & 0x0F0F0000u)) & 0x0F0F0F0Fu) | hb;
+      const uint32_t v = q < 2 ? v6 : v4;
+      sa[i] = h2_sub(prmt(v, 0x64646464u, pa_sel), kMagic);               // (sc_2q, sc_2q)
+      nsa[i] = h2_mul(sa[i], 0xE400E400u);                                 // -1024 * sc_2q
+      const uint32_t sb = h2_sub(prmt(v, 0x64646464u, pb_sel), kMagic);   // sc_2q+1
+      sb16[i] = h2_mul(sb, 0x2C002C00u);                                   // sc_2q+1 / 16
+      nsb64[i] = h2_mul(sb, 0xD400D400u);                                  // -64 * sc_2q+1
+      ma[i] = h2_sub(prmt(v, 0x64646464u, pma_sel), kMagic);              // (m_2q, m_2q)
+      mb[i] = h2_sub(prmt(v, 0x64646464u, pmb_sel), kMagic);              // (m_2q+1, m_2q+1)
+      d[i] = half_bits_to_float(r.h[i].x);
+      dmin[i] = half_bits_to_float(r.h[i].x >> 16);
+    }
+    // four independent accumulation chains (word parity x low/high nibbles), added in a
+    // fixed order at the end: the MMAs of one super-block overlap instead of queueing
+    float p[NT][4][4];
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) p[t][c][0] = p[t][c][1] = p[t][c][2] = p[t][c][3] = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {  // code word k: MMA k (low nibbles) and MMA 8+k (high nibbles)
+      uint32_t alo[4], ahi[4];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint4 cv = r.c[i][k >> 2];
+        const uint32_t w = (k & 3) == 0 ? cv.x : (k & 3) == 1 ? cv.y : (k & 3) == 2 ? cv.z : cv.w;
+        const uint32_t w8 = w >> 8;
+        // fifth bits of the same four weights l = 4k..4k+3: bit 2q (low nibbles) and bit
+        // 2q+1 (high nibbles) of qh[l]; as fp16 they add 16 to 1024 + q (bit 4 of the
+        // word) or 256 to 1024 + 16q (bit 8)
+        const uint4 hv = r.qh[i][k >> 2];
+        const uint32_t hw = ((k & 3) == 0 ? hv.x : (k & 3) == 1 ? hv.y : (k & 3) == 2 ? hv.z : hv.w) >> (2 * q);
+        alo[i] = h2_fma(and_or(w, 0x000F000Fu, and_or(hw << 4, 0x00100010u, kMagic)), sa[i], nsa[i]);
+        alo[i + 2] = h2_fma(and_or(w8, 0x000F000Fu, and_or(hw >> 4, 0x00100010u, kMagic)), sa[i], nsa[i]);
+        ahi[i] = h2_fma(and_or(w, 0x00F000F0u, and_or(hw << 7, 0x01000100u, kMagic)), sb16[i], nsb64[i]);
+        ahi[i + 2] = h2_fma(and_or(w8, 0x00F000F0u, and_or(hw >> 1, 0x01000100u, kMagic)), sb16[i], nsb64[i]);
       }
 #pragma unroll
       for (int t = 0; t < NT; ++t) {

@@ -568,7 +568,9 @@ int launch_tma(const CUtensorMap& tm, const TmaParams& prm, size_t smem, int gri
   return 0;
 }
 
-int unit_bytes_of(int fmt) { return fmt == FMT_Q4_K ? 144 : (fmt == FMT_Q8_0 ? 272 : 160); }
+int unit_bytes_of(int fmt) {
+  return fmt == FMT_Q4_K ? 144 : (fmt == FMT_Q5_K ? 176 : (fmt == FMT_Q8_0 ? 272 : 160));
+}
 // Units per stage: one tensor copy brings 16 rows of >= 544 bytes each (row-strided copies
 // below ~576 bytes per row measured well under the HBM rate).
 int stage_units_of(int fmt) { return fmt == FMT_Q8_0 ? 2 : 4; }
@@ -582,7 +584,7 @@ bool tma_layout(int fmt, const TmaPlan& pl, int M, TmaParams* prm, size_t* smem)
   auto al = [](size_t v) { return (v + 127) & ~size_t(127); };
   const int T = M > 8 ? 16 : 8;
   const int ub = unit_bytes_of(fmt);
-  const bool half_x = fmt == FMT_Q4_K;
+  const bool half_x = fmt == FMT_Q4_K || fmt == FMT_Q5_K;
   const int smax = (pl.units + pl.C - 1) / pl.C;
   int xstride = 0, xts = 0, s2ts = 0;
   size_t xbytes = 0, sbytes = 0;
@@ -641,15 +643,16 @@ bool tma_layout(int fmt, const TmaPlan& pl, int M, TmaParams* prm, size_t* smem)
 // Max co-resident clusters of C CTAs for the streaming kernel of `fmt` at `smem` bytes of
 // shared memory per CTA. Cached per device, format and C. Returns 0 if the query fails.
 int max_clusters(int fmt, int C, size_t smem) {
-  static int cache[64][4][5];
+  static int cache[64][8][5];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return 0;
   int ci = 0;
   while ((1 << ci) < C) ++ci;
-  int& slot = cache[dev][fmt & 3][ci];
+  int& slot = cache[dev][fmt & 7][ci];
   if (slot > 0) return slot;
   const void* fn = nullptr;
   if (fmt == FMT_Q4_K) fn = (const void*)gemv_tma_kernel<FmtQ4KH, 2>;
+  else if (fmt == FMT_Q5_K) fn = (const void*)gemv_tma_kernel<FmtQ5KH, 2>;
   else if (fmt == FMT_Q8_0) fn = (const void*)gemv_tma_kernel<FmtQ8_0, 2>;
   else fn = (const void*)gemv_tma_kernel<FmtAffine4, 2>;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemCap) != cudaSuccess)
@@ -797,6 +800,9 @@ int launch_gemv_mma(int fmt, const void* w, const void* x, float* y, int M, int 
       case FMT_AFFINE4:
         return two ? launch_tma<FmtAffine4, 2>(tm, prm, smem, grid, stream, overlap, err)
                    : launch_tma<FmtAffine4, 1>(tm, prm, smem, grid, stream, overlap, err);
+      case FMT_Q5_K:
+        return two ? launch_tma<FmtQ5KH, 2>(tm, prm, smem, grid, stream, overlap, err)
+                   : launch_tma<FmtQ5KH, 1>(tm, prm, smem, grid, stream, overlap, err);
     }
     *err = "unsupported format";
     return -1;
@@ -826,6 +832,9 @@ int launch_gemv_mma(int fmt, const void* w, const void* x, float* y, int M, int 
     case FMT_AFFINE4:
       return two ? launch_chunked<FMT_AFFINE4, 2>(prm, smem, stream, err)
                  : launch_chunked<FMT_AFFINE4, 1>(prm, smem, stream, err);
+    case FMT_Q5_K:
+      return two ? launch_chunked<FMT_Q5_K, 2>(prm, smem, stream, err)
+                 : launch_chunked<FMT_Q5_K, 1>(prm, smem, stream, err);
   }
   *err = "unsupported format";
   return -1;

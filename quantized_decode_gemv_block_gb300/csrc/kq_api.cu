@@ -21,7 +21,7 @@ int ok() {
   return KQ_OK;
 }
 
-bool fmt_known(int fmt) { return fmt == KQ_Q8_0 || fmt == KQ_Q4_K || fmt == KQ_AFFINE4_G32; }
+bool fmt_known(int fmt) { return fmt == KQ_Q8_0 || fmt == KQ_Q4_K || fmt == KQ_AFFINE4_G32 || fmt == KQ_Q5_K; }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -99,6 +99,7 @@ size_t kq_block_bytes(int fmt) {
   switch (fmt) {
     case KQ_Q8_0: return 34;
     case KQ_Q4_K: return 144;
+    case KQ_Q5_K: return 176;
     case KQ_AFFINE4_G32: return 20;
   }
   return 0;
@@ -108,6 +109,7 @@ size_t kq_block_weights(int fmt) {
   switch (fmt) {
     case KQ_Q8_0: return 32;
     case KQ_Q4_K: return 256;
+    case KQ_Q5_K: return 256;
     case KQ_AFFINE4_G32: return 32;
   }
   return 0;

@@ -9,6 +9,7 @@ namespace kq {
 constexpr int FMT_Q8_0 = 1;
 constexpr int FMT_Q4_K = 2;
 constexpr int FMT_AFFINE4 = 3;
+constexpr int FMT_Q5_K = 4;
 
 // Read-only global loads (weights and activations are never written by a kernel
 // that reads them).

@@ -72,8 +72,12 @@ __global__ void quant_q8_0_kernel(const float* __restrict__ w, uint8_t* __restri
   }
 }
 
-__global__ void quant_q4_k_kernel(const float* __restrict__ w, uint8_t* __restrict__ out,
-                                  long long nblk) {
+// Q4_K (LEVELS = 15, 144-byte blocks) and Q5_K (LEVELS = 31, 176-byte blocks: the fifth
+// code bit of weight i goes to bit 2c + h of qh[l], c = i/64, h = (i%64 >= 32), l = i%32).
+template <int LEVELS>
+__global__ void quant_qk_kernel(const float* __restrict__ w, uint8_t* __restrict__ out, long long nblk) {
+  constexpr int kBytes = LEVELS == 15 ? 144 : 176;
+  constexpr int kCodes = LEVELS == 15 ? 16 : 48;  // offset of the low-nibble bytes
   const long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   if (b >= nblk) return;
   const float* src = w + b * 256;
@@ -116,12 +120,12 @@ __global__ void quant_q4_k_kernel(const float* __restrict__ w, uint8_t* __restri
   int sc[8];
   for (int j = 0; j < 8; ++j) sc[j] = 0;
   if (maxt > 0.0) {
-    d16 = d2h_up(__ddiv_rn(maxt, 945.0));
+    d16 = d2h_up(__ddiv_rn(maxt, 63.0 * LEVELS));
     for (int guard = 0; guard < 64; ++guard) {
       const double dd = h2d(d16);
       bool ok = true;
       for (int j = 0; j < 8; ++j) {
-        sc[j] = static_cast<int>(ceil(__ddiv_rn(t[j], __dmul_rn(15.0, dd))));
+        sc[j] = static_cast<int>(ceil(__ddiv_rn(t[j], __dmul_rn(static_cast<double>(LEVELS), dd))));
         if (sc[j] > 63) ok = false;
       }
       if (ok) break;
@@ -129,7 +133,7 @@ __global__ void quant_q4_k_kernel(const float* __restrict__ w, uint8_t* __restri
     }
   }
   const double d = h2d(d16);
-  uint8_t* dst = out + b * 144;
+  uint8_t* dst = out + b * kBytes;
   put16(dst, d16);
   put16(dst + 2, dmin16);
   uint8_t scales[12];
@@ -144,6 +148,8 @@ __global__ void quant_q4_k_kernel(const float* __restrict__ w, uint8_t* __restri
     scales[j] = static_cast<uint8_t>(scales[j] | ((m[j] >> 4) << 6));
   }
   for (int i = 0; i < 12; ++i) dst[4 + i] = scales[i];
+  uint8_t qh[32];
+  for (int l = 0; l < 32; ++l) qh[l] = 0;
   for (int c = 0; c < 4; ++c) {
     for (int l = 0; l < 32; ++l) {
       int qq[2];
@@ -155,13 +161,16 @@ __global__ void quant_q4_k_kernel(const float* __restrict__ w, uint8_t* __restri
           const double r = round(__ddiv_rn(
               __dadd_rn(static_cast<double>(src[i]), __dmul_rn(dmin, static_cast<double>(m[j]))),
               step));
-          qv = static_cast<int>(fmin(15.0, fmax(0.0, r)));
+          qv = static_cast<int>(fmin(static_cast<double>(LEVELS), fmax(0.0, r)));
         }
         qq[hsel] = qv;
+        if (qv & 16) qh[l] = static_cast<uint8_t>(qh[l] | (1u << (2 * c + hsel)));
       }
-      dst[16 + 32 * c + l] = static_cast<uint8_t>(qq[0] | (qq[1] << 4));
+      dst[kCodes + 32 * c + l] = static_cast<uint8_t>((qq[0] & 15) | ((qq[1] & 15) << 4));
     }
   }
+  if (LEVELS == 31)
+    for (int l = 0; l < 32; ++l) dst[16 + l] = qh[l];
 }
 
 __global__ void quant_affine4_kernel(const float* __restrict__ w, uint8_t* __restrict__ out,
@@ -201,13 +210,14 @@ __global__ void quant_affine4_kernel(const float* __restrict__ w, uint8_t* __res
 int launch_quantize(int fmt, const float* w, void* blocks, int N, int K, cudaStream_t stream,
                     std::string* err) {
   uint8_t* out = static_cast<uint8_t*>(blocks);
-  const int bw = fmt == FMT_Q4_K ? 256 : 32;
+  const int bw = (fmt == FMT_Q4_K || fmt == FMT_Q5_K) ? 256 : 32;
   const long long nblk = (long long)N * (K / bw);
   if (nblk == 0) return 0;
   const int threads = 128;
   const long long grid = (nblk + threads - 1) / threads;
   if (fmt == FMT_Q8_0) quant_q8_0_kernel<<<(unsigned)grid, threads, 0, stream>>>(w, out, nblk);
-  else if (fmt == FMT_Q4_K) quant_q4_k_kernel<<<(unsigned)grid, threads, 0, stream>>>(w, out, nblk);
+  else if (fmt == FMT_Q4_K) quant_qk_kernel<15><<<(unsigned)grid, threads, 0, stream>>>(w, out, nblk);
+  else if (fmt == FMT_Q5_K) quant_qk_kernel<31><<<(unsigned)grid, threads, 0, stream>>>(w, out, nblk);
   else quant_affine4_kernel<<<(unsigned)grid, threads, 0, stream>>>(w, out, nblk);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
