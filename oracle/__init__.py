@@ -20,7 +20,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SO = os.path.join(_HERE, "liboracle.so")
 _SOURCES = [os.path.join(_HERE, "oracle.cpp"), os.path.join(_HERE, "decode.cpp")]
 
-Q8_0, Q4_K, AFFINE4, Q5_K = 1, 2, 3, 4
+Q8_0, Q4_K, AFFINE4, Q5_K, Q6_K = 1, 2, 3, 4, 5
 F32, BF16 = 1, 2
 
 _lib = None

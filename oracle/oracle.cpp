@@ -6,8 +6,8 @@
 // written out from the definitions, in fp64, one weight at a time.
 //
 // What it computes (sources are the engine READMEs this library follows):
-//  (Q5_K, the next GGUF k-quant after Q4_K, follows GGUF's published Q5_K layout for
-//  the same reason as Q4_K: GGUF files are to work unchanged; Q4_K_M files mix in
+//  (Q5_K and Q6_K, the GGUF k-quants next to Q4_K, follow GGUF's published layouts for
+//  the same reason as Q4_K: GGUF files are to work unchanged, and Q4_K_M files mix in
 //  higher-precision k-quant tensors.)
 //  * Kinetic README, "What makes it fast": a dense model reads all of its
 //    weights once per token; a speculative check runs every guess through one
@@ -40,7 +40,7 @@
 
 namespace {
 
-enum { ORC_Q8_0 = 1, ORC_Q4_K = 2, ORC_AFFINE4 = 3, ORC_Q5_K = 4 };
+enum { ORC_Q8_0 = 1, ORC_Q4_K = 2, ORC_AFFINE4 = 3, ORC_Q5_K = 4, ORC_Q6_K = 5 };
 enum { ORC_F32 = 1, ORC_BF16 = 2 };
 
 // ---------------------------------------------------------------- fp16 ----
@@ -122,11 +122,11 @@ uint16_t rd16(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] << 8)); }
 void wr16(uint8_t* p, uint16_t v) { p[0] = (uint8_t)(v & 0xFF); p[1] = (uint8_t)(v >> 8); }
 
 int block_bytes(int fmt) {
-  switch (fmt) { case ORC_Q8_0: return 34; case ORC_Q4_K: return 144; case ORC_AFFINE4: return 20; case ORC_Q5_K: return 176; }
+  switch (fmt) { case ORC_Q8_0: return 34; case ORC_Q4_K: return 144; case ORC_AFFINE4: return 20; case ORC_Q5_K: return 176; case ORC_Q6_K: return 210; }
   return 0;
 }
 int block_weights(int fmt) {
-  switch (fmt) { case ORC_Q8_0: return 32; case ORC_Q4_K: return 256; case ORC_AFFINE4: return 32; case ORC_Q5_K: return 256; }
+  switch (fmt) { case ORC_Q8_0: return 32; case ORC_Q4_K: return 256; case ORC_AFFINE4: return 32; case ORC_Q5_K: return 256; case ORC_Q6_K: return 256; }
   return 0;
 }
 
@@ -369,6 +369,66 @@ void deq_q5_k(const uint8_t* blk, double* out) {
   }
 }
 
+// ---------------------------------------------------------------- Q6_K ----
+// 210 bytes: ql[128], qh[64], scales[16] (int8), d (fp16) at byte 208 (GGUF's Q6_K).
+// Weight i = 128n + 32k + l (half n = 0..1, quarter k = 0..3, l = 0..31) has the 6-bit code
+//   q = low4 | (high2 << 4), low4 = nibble (k < 2 ? low : high) of ql[64n + 32*(k%2) + l],
+//   high2 = bits 2k..2k+1 of qh[32n + l],
+// and sub-block b = i/16 with int8 scale scales[b]: w = d * scales[b] * (q - 32).
+int code_q6_k(const uint8_t* blk, int i) {
+  const int n = i / 128, k = (i % 128) / 32, l = i % 32;
+  const uint8_t qlb = blk[64 * n + 32 * (k % 2) + l];
+  const int low4 = k < 2 ? (qlb & 15) : (qlb >> 4);
+  const int high2 = (blk[128 + 32 * n + l] >> (2 * k)) & 3;
+  return low4 | (high2 << 4);
+}
+// Quantizer (covering): a_b = max |w| over sub-block b (16 weights); d = smallest fp16 >=
+// max(a)/(127*31); sc_b = ceil(a_b / (31 d)) <= 127; q = 32 + round_half_away(w / (d sc_b)),
+// so q - 32 lies in [-31, 31] and |w - deq| <= d*sc_b/2.
+void quant_q6_k(const float* w, uint8_t* blk) {
+  double a[16], amax = 0.0;
+  for (int b = 0; b < 16; ++b) {
+    a[b] = 0.0;
+    for (int i = 0; i < 16; ++i) a[b] = std::max(a[b], std::fabs((double)w[16 * b + i]));
+    amax = std::max(amax, a[b]);
+  }
+  uint16_t d16 = 0;
+  int sc[16] = {0};
+  if (amax > 0.0) {
+    d16 = double_to_half_up(amax / (127.0 * 31.0));
+    for (;;) {
+      const double d = half_to_double(d16);
+      bool ok = true;
+      for (int b = 0; b < 16; ++b) {
+        sc[b] = (int)std::ceil(a[b] / (31.0 * d));
+        if (sc[b] > 127) ok = false;
+      }
+      if (ok) break;
+      d16 = half_next_up(d16);
+    }
+  }
+  const double d = half_to_double(d16);
+  std::memset(blk, 0, 210);
+  for (int b = 0; b < 16; ++b) blk[192 + b] = (uint8_t)(int8_t)sc[b];
+  wr16(blk + 208, d16);
+  for (int i = 0; i < 256; ++i) {
+    const double step = d * (double)sc[i / 16];
+    int q = 32;
+    if (step != 0.0) q = 32 + (int)std::min(31.0, std::max(-31.0, std::round((double)w[i] / step)));
+    const int n = i / 128, k = (i % 128) / 32, l = i % 32;
+    uint8_t& qlb = blk[64 * n + 32 * (k % 2) + l];
+    qlb |= (uint8_t)(k < 2 ? (q & 15) : ((q & 15) << 4));
+    blk[128 + 32 * n + l] |= (uint8_t)(((q >> 4) & 3) << (2 * k));
+  }
+}
+void deq_q6_k(const uint8_t* blk, double* out) {
+  const double d = half_to_double(rd16(blk + 208));
+  for (int i = 0; i < 256; ++i) {
+    const int sc = (int)(int8_t)blk[192 + i / 16];
+    out[i] = d * (double)sc * (double)(code_q6_k(blk, i) - 32);
+  }
+}
+
 // ------------------------------------------------------------- affine4 ----
 // 20 bytes: s (fp16), b (fp16), codes[16]; weight 2i = low nibble of codes[i],
 // weight 2i+1 = high nibble. w = s * q + b.
@@ -404,6 +464,7 @@ void deq_block(int fmt, const uint8_t* blk, double* out) {
   if (fmt == ORC_Q8_0) deq_q8_0(blk, out);
   else if (fmt == ORC_Q4_K) deq_q4_k(blk, out);
   else if (fmt == ORC_Q5_K) deq_q5_k(blk, out);
+  else if (fmt == ORC_Q6_K) deq_q6_k(blk, out);
   else deq_affine4(blk, out);
 }
 void deq_row(int fmt, const uint8_t* row, int64_t K, double* out) {
@@ -441,6 +502,7 @@ int orc_quantize(int fmt, const float* w, int64_t N, int64_t K, uint8_t* blocks,
       if (fmt == ORC_Q8_0) quant_q8_0(src, dst);
       else if (fmt == ORC_Q4_K) quant_q4_k(src, dst);
       else if (fmt == ORC_Q5_K) quant_q5_k(src, dst);
+      else if (fmt == ORC_Q6_K) quant_q6_k(src, dst);
       else quant_affine4(src, dst);
     }
   }

@@ -15,7 +15,7 @@ import pytest
 from conftest import load_golden
 from quantized_decode_gemv_block_gb300 import inputs
 
-Q8_0, Q4_K, AFFINE4, Q5_K = 1, 2, 3, 4
+Q8_0, Q4_K, AFFINE4, Q5_K, Q6_K = 1, 2, 3, 4, 5
 
 
 # ------------------------------------------------------------------- fp16 --
@@ -73,8 +73,10 @@ def test_block_sizes(orc):
     assert (orc.block_bytes(Q4_K), orc.block_weights(Q4_K)) == (144, 256)
     assert (orc.block_bytes(AFFINE4), orc.block_weights(AFFINE4)) == (20, 32)
     assert (orc.block_bytes(Q5_K), orc.block_weights(Q5_K)) == (176, 256)
+    assert (orc.block_bytes(Q6_K), orc.block_weights(Q6_K)) == (210, 256)
     for K in (256, 2048, 2560, 9728):
         assert orc.row_bytes(Q5_K, K) == K * 11 // 16
+        assert orc.row_bytes(Q6_K, K) == K * 105 // 128
         assert orc.row_bytes(Q8_0, K) == K * 17 // 16
         assert orc.row_bytes(Q4_K, K) == K * 9 // 16
         assert orc.row_bytes(AFFINE4, K) == K * 5 // 8
@@ -154,6 +156,40 @@ def test_q5_k_fifth_bit_positions(orc):
     assert y[0, 0] == 38480 + 16 * 32 * d * sum(sc)  # Q4_K example's sum (tests/golden) + the fifth bits
 
 
+def _q6k_block(ql=None, qh=None, scales=None, d_bits=0x3800):
+    """Q6_K bytes: ql[128], qh[64], int8 scales[16], then fp16 d (0x3800 = 0.5) at byte 208."""
+    ql = bytearray(128) if ql is None else ql
+    qh = bytearray(64) if qh is None else qh
+    sc = bytes((v & 0xFF) for v in (scales if scales is not None else range(16)))
+    return bytes(ql) + bytes(qh) + sc + bytes([d_bits & 0xFF, d_bits >> 8])
+
+
+def test_q6_k_zero_codes_and_signed_scales(orc):
+    """All codes 0 (so q - 32 = -32) and scales[b] = b - 8 (negative ones included): weight i
+    of sub-block b = i // 16 is d * (b - 8) * (-32) = -16 * (b - 8) with d = 0.5."""
+    blk = _q6k_block(scales=[b - 8 for b in range(16)])
+    w = orc.dequant(Q6_K, np.frombuffer(blk, np.uint8).reshape(1, 210), 1, 256)[0]
+    assert np.array_equal(w, np.array([-16.0 * (i // 16 - 8) for i in range(256)]))
+
+
+def test_q6_k_code_bit_positions(orc):
+    """Hand-placed code bits. GGUF's Q6_K: weight 128n + 32k + l takes its low four bits from
+    ql[64n + 32(k%2) + l] (low nibble for k < 2, high nibble otherwise) and its top two bits
+    from bits 2k, 2k+1 of qh[32n + l]. So ql[0] = 0x0F sets weight 0 to 15 and ql[0] = 0xF0
+    weight 64 to 15; ql[37] = 0x03 sets weight 37 (k = 1, l = 5) to 3; qh[39] = 0xC0 sets
+    weight 231 (n = 1, k = 3, l = 7) to 48. Every other code stays 0."""
+    ql, qh = bytearray(128), bytearray(64)
+    ql[0] = 0xFF
+    ql[37] = 0x03
+    qh[39] = 0xC0
+    scales = [1 + b for b in range(16)]
+    blk = _q6k_block(ql, qh, scales)
+    w = orc.dequant(Q6_K, np.frombuffer(blk, np.uint8).reshape(1, 210), 1, 256)[0]
+    code = {0: 15, 64: 15, 37: 3, 231: 48}
+    expect = np.array([0.5 * scales[i // 16] * (code.get(i, 0) - 32) for i in range(256)])
+    assert np.array_equal(w, expect)
+
+
 def test_affine4_nibble_order(orc):
     """Hand-built group: s = 2, b = -1, codes byte i = (2i mod 16) | ((2i+1 mod 16) << 4)."""
     blk = bytes([0x00, 0x40, 0x00, 0xBC]) + bytes(((2 * i) % 16) | ((((2 * i) + 1) % 16) << 4)
@@ -173,7 +209,7 @@ def _adversarial_blocks(bw, rng):
     return np.stack(rows).astype(np.float32)
 
 
-@pytest.mark.parametrize("fmt", [Q8_0, Q4_K, AFFINE4, Q5_K])
+@pytest.mark.parametrize("fmt", [Q8_0, Q4_K, AFFINE4, Q5_K, Q6_K])
 def test_round_trip_bound(orc, fmt):
     """|w - deq(q(w))| <= step/2 for every block (the quantizer's covering bound)."""
     bw, bb = orc.block_weights(fmt), orc.block_bytes(fmt)
@@ -210,6 +246,13 @@ def test_round_trip_bound(orc, fmt):
                 assert err[r, seg].max() <= d * sc / 2 * (1 + 1e-12) + 1e-300
                 # the min covers the most negative weight of the sub-block
                 assert dmin * m >= -min(0.0, float(w[r, seg].min()))
+        elif fmt == Q6_K:
+            d = orc.half_to_double(int(b[208]) | (int(b[209]) << 8))
+            for j in range(16):
+                sc = int(np.int8(b[192 + j]))
+                assert 0 <= sc <= 127
+                seg = slice(16 * j, 16 * j + 16)
+                assert err[r, seg].max() <= d * sc / 2 * (1 + 1e-12) + 1e-300
         else:
             s = orc.half_to_double(int(b[0]) | (int(b[1]) << 8))
             bias = orc.half_to_double(int(b[2]) | (int(b[3]) << 8))
@@ -231,7 +274,7 @@ def test_q8_0_codes_match_exact_rounding(orc):
 
 
 # ------------------------------------------------------------------- gemv --
-@pytest.mark.parametrize("fmt", [Q8_0, Q4_K, AFFINE4, Q5_K])
+@pytest.mark.parametrize("fmt", [Q8_0, Q4_K, AFFINE4, Q5_K, Q6_K])
 @pytest.mark.parametrize("K", [256, 512])
 def test_gemv_brute_force(orc, fmt, K):
     """Oracle GEMV == numpy dense fp64 matmul of the dequantized matrix (other summation order)."""
