@@ -9,6 +9,7 @@ Prints ONE JSON line (rank 0). Workloads (synthetic data, seeded):
   verify   Q4_K speculative-verify GEMM, W 12288x4096, M bf16 rows (--m, default 16).
   q8_0     Q8_0 GEMV, W 1024x1024, one fp32 row.
   ffn_q5k  the ffn pair with Q5_K blocks (176 bytes per 256 weights).
+  ffn_q6k  the ffn pair with Q6_K blocks (210 bytes per 256 weights; CUDA-core kernel).
   head     Q8_0 lm-head GEMV, W 151936x2048, M bf16 rows (--m).
   decode   the dense 28-layer decode step (kq_decode_step) in a CUDA graph, M rows (--m).
   prefill  Q4_K prefill GEMM on the tensor cores, W 9728x2560, X 2048x2560 bf16; reported in
@@ -37,7 +38,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "effective weight-read HBM GB/s (and % of 8 TB/s) for quantized GEMV at M=1..16"
-FMT_ID = {"q8_0": 1, "q4_k": 2, "affine4": 3, "q5_k": 4}
+FMT_ID = {"q8_0": 1, "q4_k": 2, "affine4": 3, "q5_k": 4, "q6_k": 5}
 
 
 def workload_spec(name: str, m: int):
@@ -46,6 +47,9 @@ def workload_spec(name: str, m: int):
                     mats=[(9728, 2560), (2560, 9728)], M=1, dtype="bf16")
     if name == "ffn_q5k":
         return dict(name="q5_k ffn gemv 9728x2560 + 2560x9728, M=1 bf16", fmt="q5_k",
+                    mats=[(9728, 2560), (2560, 9728)], M=1, dtype="bf16")
+    if name == "ffn_q6k":
+        return dict(name="q6_k ffn gemv 9728x2560 + 2560x9728, M=1 bf16", fmt="q6_k",
                     mats=[(9728, 2560), (2560, 9728)], M=1, dtype="bf16")
     if name == "verify":
         return dict(name=f"q4_k verify 12288x4096, M={m} bf16", fmt="q4_k", mats=[(12288, 4096)],
@@ -548,7 +552,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="kq", choices=["kq", "reference"])
-    ap.add_argument("--workload", default="ffn", choices=["ffn", "ffn_q5k", "verify", "q8_0", "head", "decode", "prefill"])
+    ap.add_argument("--workload", default="ffn", choices=["ffn", "ffn_q5k", "ffn_q6k", "verify", "q8_0", "head", "decode", "prefill"])
     ap.add_argument("--m", type=int, default=16)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -734,7 +738,7 @@ def main():
                        "pct_of_8tbs": value / world / 8000.0},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": f"{peak_kind} hbm_gbs", "kernel": "gemv_tma_kernel" if spec["dtype"] == "bf16" else "gemv_f32_kernel",
+                         "peak_source": f"{peak_kind} hbm_gbs", "kernel": ("gemv_tma_kernel" if spec["dtype"] == "bf16" and spec["fmt"] != "q6_k" else "gemv_f32_kernel"),
                          "launch_us": launch_ms * 1e3, "launch_us_isolated": isolated_ms * 1e3,
                          "timing": "timed region (graph of K steps) / launches; isolated = event pair per launch"},
             "cpu_baseline": cpu,

@@ -47,8 +47,13 @@ extern "C" {
  *                then Q4_K's qs[128] holding the low four code bits; the fifth bit of
  *                weight 64c+32h+l (c = 0..3, h = 0/1, l = 0..31) is bit 2c+h of qh[l];
  *                codes 0..31, w = d*sc_j*q - dmin*m_j (GGUF's Q5_K; the next k-quant
- *                that Q4_K_M model files mix in) */
-enum kq_fmt { KQ_Q8_0 = 1, KQ_Q4_K = 2, KQ_AFFINE4_G32 = 3, KQ_Q5_K = 4 };
+ *                that Q4_K_M model files mix in)
+ * KQ_Q6_K       210 bytes / 256 weights: ql[128], qh[64], int8 scales[16], fp16 d (GGUF's
+ *                Q6_K); weight 128n+32k+l takes its low 4 code bits from ql[64n+32(k%2)+l]
+ *                (low nibble for k < 2, else high) and its top 2 from bits 2k..2k+1 of
+ *                qh[32n+l]; w = d*scales[i/16]*(q - 32). Rows are only 2-byte aligned, so
+ *                Q6_K runs on CUDA cores for both activation types. */
+enum kq_fmt { KQ_Q8_0 = 1, KQ_Q4_K = 2, KQ_AFFINE4_G32 = 3, KQ_Q5_K = 4, KQ_Q6_K = 5 };
 
 /* Activation element types. */
 enum kq_dtype { KQ_F32 = 1, KQ_BF16 = 2 };
@@ -82,7 +87,7 @@ const char* kq_version(void);
 int kq_device_errors(void);
 
 /* Quantized GEMV / speculative-verify product (Kinetic README, "What makes it fast").
- *   fmt       KQ_Q8_0, KQ_Q4_K, KQ_AFFINE4_G32 or KQ_Q5_K
+ *   fmt       KQ_Q8_0, KQ_Q4_K, KQ_AFFINE4_G32, KQ_Q5_K or KQ_Q6_K
  *   w_blocks  N * kq_row_bytes(fmt, K) bytes, 16-byte aligned
  *   x_dtype   KQ_BF16 (tensor-core path) or KQ_F32 (CUDA-core path)
  *   x         M x K activations, 16-byte aligned
@@ -139,6 +144,8 @@ size_t kq_gemm_workspace_size(int fmt, int x_dtype, int M, int N, int K);
  *            sc_j = ceil(t_j/(15 d)), q = round_half_away((w + dmin*m_j)/(d*sc_j))
  *   Q5_K:    as Q4_K with 31 levels: d = smallest fp16 >= max(t)/1953,
  *            sc_j = ceil(t_j/(31 d)), q = round_half_away((w + dmin*m_j)/(d*sc_j)) in 0..31
+ *   Q6_K:    per 16-weight sub-block a = max|w|, d = smallest fp16 >= max(a)/3937,
+ *            sc = ceil(a/(31 d)), q = 32 + round_half_away(w/(d*sc)) in 1..63
  *   AFFINE4: b = largest fp16 <= min w, s = smallest fp16 >= (max w - b)/15,
  *            q = clamp(round_half_away((w - b)/s), 0, 15)
  * These make data for tests and benchmarks (the GEMV never quantizes). K must be a

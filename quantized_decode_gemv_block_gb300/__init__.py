@@ -17,9 +17,9 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkq.so")
 
-Q8_0, Q4_K, AFFINE4, Q5_K = 1, 2, 3, 4
+Q8_0, Q4_K, AFFINE4, Q5_K, Q6_K = 1, 2, 3, 4, 5
 F32, BF16 = 1, 2
-FORMATS = {"q8_0": Q8_0, "q4_k": Q4_K, "affine4": AFFINE4, "q5_k": Q5_K}
+FORMATS = {"q8_0": Q8_0, "q4_k": Q4_K, "affine4": AFFINE4, "q5_k": Q5_K, "q6_k": Q6_K}
 KQ_OK, KQ_ERR_ARG, KQ_ERR_UNSUPPORTED, KQ_ERR_WORKSPACE, KQ_ERR_CUDA, KQ_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
 
 

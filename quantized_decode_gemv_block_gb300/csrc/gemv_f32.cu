@@ -1,4 +1,6 @@
-// CUDA-core GEMV for fp32 activations, M = 1..16.
+// CUDA-core GEMV for fp32 activations (every format) and for bf16 activations of Q6_K
+// blocks, M = 1..16. (Q6_K's 210-byte blocks leave rows only 2-byte aligned, which no tensor
+// copy accepts, so Q6_K is read with 16-bit loads here for both activation types.)
 //
 // Same product as the tensor-core path, Y[j][n] = sum_k deq(W)[n][k] * X[j][k]
 // (Kinetic README, "What makes it fast"), for callers whose activations are fp32
@@ -28,7 +30,27 @@ __device__ __forceinline__ uint32_t ldg16(const void* p) {
 template <int FMT>
 __device__ __forceinline__ void decode_slice(const uint8_t* unit, int gi, int q, float (&c)[8],
                                              float& scale, float& offset) {
-  if (FMT == FMT_Q4_K) {
+  if (FMT == FMT_Q6_K) {
+    // weights 32gi + 8q + k: half n = gi/4, quarter kq = gi%4, l = 8q + k; sub-block 2gi + q/2
+    const int n = gi >> 2, kq = gi & 3;
+    const uint8_t* qlp = unit + 64 * n + 32 * (kq & 1) + 8 * q;
+    const uint8_t* qhp = unit + 128 + 32 * n + 8 * q;
+    const int b = 2 * gi + (q >> 1);
+    const uint32_t sp = ldg16(unit + 192 + (b & ~1));
+    const int sc = static_cast<int>(static_cast<int8_t>((b & 1) ? (sp >> 8) : (sp & 0xFFu)));
+    scale = half_bits_to_float(ldg16(unit + 208)) * static_cast<float>(sc);  // exact: 11-bit x 8-bit
+    offset = 0.f;
+    const int nsh = (kq >= 2) ? 4 : 0, hsh = 2 * kq;
+#pragma unroll
+    for (int k = 0; k < 8; k += 2) {
+      const uint32_t l2 = ldg16(qlp + k), h2 = ldg16(qhp + k);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const uint32_t lo4 = ((l2 >> (8 * e)) >> nsh) & 15u, hi2 = ((h2 >> (8 * e)) >> hsh) & 3u;
+        c[k + e] = static_cast<float>(static_cast<int>(lo4 | (hi2 << 4)) - 32);
+      }
+    }
+  } else if (FMT == FMT_Q4_K) {
     const uint4 h = ldg128(unit);
     const int ch = gi >> 1;
     const uint2 b = ldg64(unit + 16 + 32 * ch + 8 * q);
@@ -105,12 +127,31 @@ __device__ __forceinline__ void decode_slice(const uint8_t* unit, int gi, int q,
 
 template <int FMT>
 constexpr int unit_bytes() {
-  return FMT == FMT_Q4_K ? 144 : (FMT == FMT_Q5_K ? 176 : (FMT == FMT_Q8_0 ? 272 : 160));
+  return FMT == FMT_Q4_K ? 144 : (FMT == FMT_Q5_K ? 176 : (FMT == FMT_Q6_K ? 210 : (FMT == FMT_Q8_0 ? 272 : 160)));
 }
 
-template <int FMT, int MT>
+// 8 activations of token j at k (a multiple of 8) as fp32: XT = float, or uint16_t (bf16 bits).
+template <class XT>
+__device__ __forceinline__ void load_x8f(const XT* x, long long off, float (&xv)[8]) {
+  if constexpr (sizeof(XT) == 4) {
+    const uint4 v0 = ldg128(x + off), v1 = ldg128(x + off + 4);
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) xv[k] = __uint_as_float(w[k]);
+  } else {
+    const uint4 v = ldg128(x + off);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      xv[2 * k] = __uint_as_float(w[k] << 16);
+      xv[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+  }
+}
+
+template <int FMT, int MT, class XT>
 __global__ void __launch_bounds__(kThreadsF) gemv_f32_kernel(const uint8_t* __restrict__ w,
-                                                             const float* __restrict__ x,
+                                                             const XT* __restrict__ x,
                                                              float* __restrict__ y, int M, int N,
                                                              int K, long long row_bytes) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -134,11 +175,8 @@ __global__ void __launch_bounds__(kThreadsF) gemv_f32_kernel(const uint8_t* __re
 #pragma unroll
     for (int j = 0; j < MT; ++j) {
       if (j < M) {
-        const float* xp = x + (long long)j * K + u * 256 + 32 * gi + 8 * q;
-        const uint4 v0 = ldg128(xp), v1 = ldg128(xp + 4);
-        const float xv[8] = {__uint_as_float(v0.x), __uint_as_float(v0.y), __uint_as_float(v0.z),
-                             __uint_as_float(v0.w), __uint_as_float(v1.x), __uint_as_float(v1.y),
-                             __uint_as_float(v1.z), __uint_as_float(v1.w)};
+        float xv[8];
+        load_x8f<XT>(x, (long long)j * K + u * 256 + 32 * gi + 8 * q, xv);
         float s = 0.f;
 #pragma unroll
         for (int k = 0; k < 8; ++k) s = __fadd_rn(s, xv[k]);
@@ -148,7 +186,7 @@ __global__ void __launch_bounds__(kThreadsF) gemv_f32_kernel(const uint8_t* __re
 #pragma unroll
           for (int k = 0; k < 8; ++k) p = __fmaf_rn(c[i][k], xv[k], p);
           acc[i][j] = __fmaf_rn(sc[i], p, acc[i][j]);
-          if (FMT != FMT_Q8_0) acc[i][j] = __fmaf_rn(off[i], s, acc[i][j]);  // min / bias
+          if (FMT != FMT_Q8_0 && FMT != FMT_Q6_K) acc[i][j] = __fmaf_rn(off[i], s, acc[i][j]);  // min / bias
         }
       }
     }
@@ -165,15 +203,15 @@ __global__ void __launch_bounds__(kThreadsF) gemv_f32_kernel(const uint8_t* __re
   }
 }
 
-template <int FMT>
-int launch_fmt(const uint8_t* w, const float* x, float* y, int M, int N, int K,
+template <int FMT, class XT>
+int launch_fmt(const uint8_t* w, const XT* x, float* y, int M, int N, int K,
                long long row_bytes, cudaStream_t s) {
   const dim3 grid((N + kRowsPerCtaF - 1) / kRowsPerCtaF), block(kThreadsF);
-  if (M <= 1) gemv_f32_kernel<FMT, 1><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
-  else if (M <= 2) gemv_f32_kernel<FMT, 2><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
-  else if (M <= 4) gemv_f32_kernel<FMT, 4><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
-  else if (M <= 8) gemv_f32_kernel<FMT, 8><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
-  else gemv_f32_kernel<FMT, 16><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
+  if (M <= 1) gemv_f32_kernel<FMT, 1, XT><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
+  else if (M <= 2) gemv_f32_kernel<FMT, 2, XT><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
+  else if (M <= 4) gemv_f32_kernel<FMT, 4, XT><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
+  else if (M <= 8) gemv_f32_kernel<FMT, 8, XT><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
+  else gemv_f32_kernel<FMT, 16, XT><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
   return 0;
 }
 
@@ -187,11 +225,23 @@ int launch_gemv_f32(int fmt, const void* w, const float* x, float* y, int M, int
     case FMT_Q8_0: launch_fmt<FMT_Q8_0>(wb, x, y, M, N, K, row_bytes, stream); break;
     case FMT_AFFINE4: launch_fmt<FMT_AFFINE4>(wb, x, y, M, N, K, row_bytes, stream); break;
     case FMT_Q5_K: launch_fmt<FMT_Q5_K>(wb, x, y, M, N, K, row_bytes, stream); break;
+    case FMT_Q6_K: launch_fmt<FMT_Q6_K>(wb, x, y, M, N, K, row_bytes, stream); break;
     default: *err = "unsupported format"; return -1;
   }
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     *err = std::string("gemv (fp32 x) launch: ") + cudaGetErrorString(e);
+    return -1;
+  }
+  return 0;
+}
+
+int launch_gemv_q6k_bf16(const void* w, const uint16_t* x, float* y, int M, int N, int K, long long row_bytes,
+                         cudaStream_t stream, std::string* err) {
+  launch_fmt<FMT_Q6_K>(static_cast<const uint8_t*>(w), x, y, M, N, K, row_bytes, stream);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    *err = std::string("gemv (Q6_K, bf16 x) launch: ") + cudaGetErrorString(e);
     return -1;
   }
   return 0;

@@ -21,7 +21,9 @@ int ok() {
   return KQ_OK;
 }
 
-bool fmt_known(int fmt) { return fmt == KQ_Q8_0 || fmt == KQ_Q4_K || fmt == KQ_AFFINE4_G32 || fmt == KQ_Q5_K; }
+bool fmt_known(int fmt) {
+  return fmt == KQ_Q8_0 || fmt == KQ_Q4_K || fmt == KQ_AFFINE4_G32 || fmt == KQ_Q5_K || fmt == KQ_Q6_K;
+}
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -78,7 +80,10 @@ int gemv_impl(int fmt, const void* w, int x_dtype, const void* x, float* y, int 
   }
   std::string err;
   const long long row_bytes = (long long)kq_row_bytes(fmt, K);
-  if (x_dtype == KQ_BF16) {
+  if (fmt == KQ_Q6_K && x_dtype == KQ_BF16) {  // 2-byte aligned rows: the CUDA-core kernel
+    if (kq::launch_gemv_q6k_bf16(w, static_cast<const uint16_t*>(x), y, M, N, K, row_bytes, s, &err) != 0)
+      return fail(KQ_ERR_CUDA, err);
+  } else if (x_dtype == KQ_BF16) {
     const int sms = sm_count(&err);
     if (sms < 0) return fail(KQ_ERR_CUDA, err);
     if (kq::launch_gemv_mma(fmt, w, x, y, M, N, K, row_bytes, sms, s, (flags & KQ_OVERLAP_PREVIOUS) != 0,
@@ -100,6 +105,7 @@ size_t kq_block_bytes(int fmt) {
     case KQ_Q8_0: return 34;
     case KQ_Q4_K: return 144;
     case KQ_Q5_K: return 176;
+    case KQ_Q6_K: return 210;
     case KQ_AFFINE4_G32: return 20;
   }
   return 0;
@@ -110,6 +116,7 @@ size_t kq_block_weights(int fmt) {
     case KQ_Q8_0: return 32;
     case KQ_Q4_K: return 256;
     case KQ_Q5_K: return 256;
+    case KQ_Q6_K: return 256;
     case KQ_AFFINE4_G32: return 32;
   }
   return 0;

@@ -10,6 +10,7 @@ constexpr int FMT_Q8_0 = 1;
 constexpr int FMT_Q4_K = 2;
 constexpr int FMT_AFFINE4 = 3;
 constexpr int FMT_Q5_K = 4;
+constexpr int FMT_Q6_K = 5;
 
 // Read-only global loads (weights and activations are never written by a kernel
 // that reads them).

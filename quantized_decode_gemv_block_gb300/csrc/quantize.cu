@@ -173,6 +173,58 @@ __global__ void quant_qk_kernel(const float* __restrict__ w, uint8_t* __restrict
     for (int l = 0; l < 32; ++l) dst[16 + l] = qh[l];
 }
 
+// Q6_K (GGUF): per 16-weight sub-block a = max |w|; d = smallest fp16 >= max(a)/(127*31);
+// sc = ceil(a / (31 d)) <= 127; q = 32 + round_half_away(w / (d sc)) in [1, 63]. Same fp64
+// operations, in the same order, as the oracle's quantizer.
+__global__ void quant_q6_k_kernel(const float* __restrict__ w, uint8_t* __restrict__ out, long long nblk) {
+  const long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (b >= nblk) return;
+  const float* src = w + b * 256;
+  double a[16];
+  double amax = 0.0;
+  for (int s = 0; s < 16; ++s) {
+    double m = 0.0;
+    for (int i = 0; i < 16; ++i) m = dmax_of(m, fabs(static_cast<double>(src[16 * s + i])));
+    a[s] = m;
+    amax = dmax_of(amax, m);
+  }
+  uint16_t d16 = 0;
+  int sc[16];
+  for (int s = 0; s < 16; ++s) sc[s] = 0;
+  if (amax > 0.0) {
+    d16 = d2h_up(__ddiv_rn(amax, 127.0 * 31.0));
+    for (int guard = 0; guard < 64; ++guard) {
+      const double dd = h2d(d16);
+      bool ok = true;
+      for (int s = 0; s < 16; ++s) {
+        sc[s] = static_cast<int>(ceil(__ddiv_rn(a[s], __dmul_rn(31.0, dd))));
+        if (sc[s] > 127) ok = false;
+      }
+      if (ok) break;
+      d16 = h_next_up(d16);
+    }
+  }
+  const double d = h2d(d16);
+  uint8_t* dst = out + b * 210;
+  uint8_t ql[128], qh[64];
+  for (int i = 0; i < 128; ++i) ql[i] = 0;
+  for (int i = 0; i < 64; ++i) qh[i] = 0;
+  for (int i = 0; i < 256; ++i) {
+    const double step = __dmul_rn(d, static_cast<double>(sc[i / 16]));
+    int qv = 32;
+    if (step != 0.0) qv = 32 + static_cast<int>(fmin(31.0, fmax(-31.0, round(__ddiv_rn(static_cast<double>(src[i]), step)))));
+    const int n = i / 128, k = (i % 128) / 32, l = i % 32;
+    const int qi = 64 * n + 32 * (k % 2) + l;
+    ql[qi] = static_cast<uint8_t>(ql[qi] | (k < 2 ? (qv & 15) : ((qv & 15) << 4)));
+    qh[32 * n + l] = static_cast<uint8_t>(qh[32 * n + l] | (((qv >> 4) & 3) << (2 * k)));
+  }
+  for (int i = 0; i < 128; ++i) dst[i] = ql[i];
+  for (int i = 0; i < 64; ++i) dst[128 + i] = qh[i];
+  for (int s = 0; s < 16; ++s) dst[192 + s] = static_cast<uint8_t>(static_cast<int8_t>(sc[s]));
+  dst[208] = static_cast<uint8_t>(d16 & 0xFFu);
+  dst[209] = static_cast<uint8_t>(d16 >> 8);
+}
+
 __global__ void quant_affine4_kernel(const float* __restrict__ w, uint8_t* __restrict__ out,
                                      long long nblk) {
   const long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x;
@@ -210,7 +262,7 @@ __global__ void quant_affine4_kernel(const float* __restrict__ w, uint8_t* __res
 int launch_quantize(int fmt, const float* w, void* blocks, int N, int K, cudaStream_t stream,
                     std::string* err) {
   uint8_t* out = static_cast<uint8_t*>(blocks);
-  const int bw = (fmt == FMT_Q4_K || fmt == FMT_Q5_K) ? 256 : 32;
+  const int bw = (fmt == FMT_Q4_K || fmt == FMT_Q5_K || fmt == FMT_Q6_K) ? 256 : 32;
   const long long nblk = (long long)N * (K / bw);
   if (nblk == 0) return 0;
   const int threads = 128;
@@ -218,6 +270,7 @@ int launch_quantize(int fmt, const float* w, void* blocks, int N, int K, cudaStr
   if (fmt == FMT_Q8_0) quant_q8_0_kernel<<<(unsigned)grid, threads, 0, stream>>>(w, out, nblk);
   else if (fmt == FMT_Q4_K) quant_qk_kernel<15><<<(unsigned)grid, threads, 0, stream>>>(w, out, nblk);
   else if (fmt == FMT_Q5_K) quant_qk_kernel<31><<<(unsigned)grid, threads, 0, stream>>>(w, out, nblk);
+  else if (fmt == FMT_Q6_K) quant_q6_k_kernel<<<(unsigned)grid, threads, 0, stream>>>(w, out, nblk);
   else quant_affine4_kernel<<<(unsigned)grid, threads, 0, stream>>>(w, out, nblk);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {

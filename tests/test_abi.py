@@ -45,6 +45,10 @@ def test_size_helpers(kqlib):
     assert (kqlib.block_bytes("q8_0"), kqlib.block_weights("q8_0")) == (34, 32)
     assert (kqlib.block_bytes("q4_k"), kqlib.block_weights("q4_k")) == (144, 256)
     assert (kqlib.block_bytes("affine4"), kqlib.block_weights("affine4")) == (20, 32)
+    assert (kqlib.block_bytes("q5_k"), kqlib.block_weights("q5_k")) == (176, 256)
+    assert (kqlib.block_bytes("q6_k"), kqlib.block_weights("q6_k")) == (210, 256)
+    assert kqlib.row_bytes("q5_k", 2560) == 1760
+    assert kqlib.row_bytes("q6_k", 2560) == 2100
     assert kqlib.block_bytes(99) == 0
     assert kqlib.row_bytes("q4_k", 2560) == 1440
     assert kqlib.row_bytes("q8_0", 2048) == 2176
@@ -77,7 +81,7 @@ def test_argument_errors_before_any_cuda_call(kqlib):
     assert L.kq_gemv(kqlib.Q4_K, None, kqlib.BF16, None, None, 4, 0, 256, None) == 0
     assert L.kq_last_error().decode() == ""
     assert L.kq_quantize(kqlib.Q4_K, fake, fake, 4, 100, None) == kqlib.KQ_ERR_ARG
-    assert L.kq_quantize(5, fake, fake, 4, 256, None) == kqlib.KQ_ERR_UNSUPPORTED
+    assert L.kq_quantize(99, fake, fake, 4, 256, None) == kqlib.KQ_ERR_UNSUPPORTED
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

@@ -12,7 +12,7 @@ from quantized_decode_gemv_block_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
 
-FMTS = {"q8_0": 1, "q4_k": 2, "affine4": 3, "q5_k": 4}
+FMTS = {"q8_0": 1, "q4_k": 2, "affine4": 3, "q5_k": 4, "q6_k": 5}
 TOL = 1e-4
 
 
@@ -206,6 +206,11 @@ def test_full_q4_k_ffn_gemv(kq, orc, N, K):
 @pytest.mark.parametrize("N,K", [(9728, 2560), (2560, 9728)])
 def test_full_q5_k_ffn_gemv(kq, orc, N, K):
     sampled_check(kq, orc, 4, "q5_k", N, K, [1, 16], "bf16", seed=0)
+
+
+@pytest.mark.parametrize("N,K", [(9728, 2560), (2560, 9728)])
+def test_full_q6_k_ffn_gemv(kq, orc, N, K):
+    sampled_check(kq, orc, 5, "q6_k", N, K, [1, 16], "bf16", seed=0)
 
 
 def test_full_q4_k_verify_12288x4096(kq, orc):
