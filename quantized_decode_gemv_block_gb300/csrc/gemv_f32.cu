@@ -125,6 +125,22 @@ __device__ __forceinline__ void decode_slice(const uint8_t* unit, int gi, int q,
   }
 }
 
+// Raw bytes one lane needs from a Q6_K unit for its 8-weight slice (16-bit loads: Q6_K rows
+// are only 2-byte aligned): 8 bytes of ql, 8 of qh, the scale pair, d.
+struct Q6Raw {
+  unsigned short l[4], h[4], s, d;
+};
+__device__ __forceinline__ void q6_load_raw(Q6Raw& r, const uint8_t* unit, int ql_off, int qh_off, int s_off) {
+  const unsigned short* u16 = reinterpret_cast<const unsigned short*>(unit);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    r.l[k] = __ldg(u16 + (ql_off >> 1) + k);
+    r.h[k] = __ldg(u16 + (qh_off >> 1) + k);
+  }
+  r.s = __ldg(u16 + (s_off >> 1));
+  r.d = __ldg(u16 + 104);
+}
+
 template <int FMT>
 constexpr int unit_bytes() {
   return FMT == FMT_Q4_K ? 144 : (FMT == FMT_Q5_K ? 176 : (FMT == FMT_Q6_K ? 210 : (FMT == FMT_Q8_0 ? 272 : 160)));
@@ -164,6 +180,56 @@ __global__ void __launch_bounds__(kThreadsF) gemv_f32_kernel(const uint8_t* __re
     for (int j = 0; j < MT; ++j) acc[i][j] = 0.f;
 
   const int units = K / 256;
+  if (FMT == FMT_Q6_K) {
+    // Q6_K: the next unit's raw bytes are loaded (plain, schedulable loads) before the
+    // current unit is decoded, so each warp keeps two units of loads in flight.
+    const int n = gi >> 2, kq = gi & 3;
+    const int ql_off = 64 * n + 32 * (kq & 1) + 8 * q, qh_off = 128 + 32 * n + 8 * q;
+    const int b = 2 * gi + (q >> 1), s_off = 192 + (b & ~1);
+    const int nsh = (kq >= 2) ? 4 : 0, hsh = 2 * kq;
+    Q6Raw nxt[kRowsPerWarp];
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) q6_load_raw(nxt[i], w + min(nbase + i, N - 1) * row_bytes, ql_off, qh_off, s_off);
+    for (int u = 0; u < units; ++u) {
+      Q6Raw cur[kRowsPerWarp];
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i) cur[i] = nxt[i];
+      if (u + 1 < units) {
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i)
+          q6_load_raw(nxt[i], w + min(nbase + i, N - 1) * row_bytes + (long long)(u + 1) * 210, ql_off, qh_off, s_off);
+      }
+      float c[kRowsPerWarp][8], sc[kRowsPerWarp];
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i) {
+        const int scv = static_cast<int>(static_cast<int8_t>((b & 1) ? (cur[i].s >> 8) : (cur[i].s & 0xFFu)));
+        sc[i] = half_bits_to_float(cur[i].d) * static_cast<float>(scv);  // exact: 11-bit x 8-bit
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const uint32_t lo4 = ((static_cast<uint32_t>(cur[i].l[k]) >> (8 * e)) >> nsh) & 15u;
+            const uint32_t hi2 = ((static_cast<uint32_t>(cur[i].h[k]) >> (8 * e)) >> hsh) & 3u;
+            c[i][2 * k + e] = static_cast<float>(static_cast<int>(lo4 | (hi2 << 4)) - 32);
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < MT; ++j) {
+        if (j < M) {
+          float xv[8];
+          load_x8f<XT>(x, (long long)j * K + u * 256 + 32 * gi + 8 * q, xv);
+#pragma unroll
+          for (int i = 0; i < kRowsPerWarp; ++i) {
+            float p = 0.f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) p = __fmaf_rn(c[i][k], xv[k], p);
+            acc[i][j] = __fmaf_rn(sc[i], p, acc[i][j]);
+          }
+        }
+      }
+    }
+  } else {
   for (int u = 0; u < units; ++u) {
     float c[kRowsPerWarp][8], sc[kRowsPerWarp], off[kRowsPerWarp];
 #pragma unroll
@@ -190,6 +256,7 @@ __global__ void __launch_bounds__(kThreadsF) gemv_f32_kernel(const uint8_t* __re
         }
       }
     }
+  }
   }
 #pragma unroll
   for (int i = 0; i < kRowsPerWarp; ++i) {
