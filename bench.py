@@ -678,32 +678,58 @@ def main():
         stream.synchronize()
     clocks = sampler.stop()
 
-    # ---- e2e through the public API with host buffers (H2D of x, D2H of y, every step)
-    xh = [x.cpu().pin_memory() for x in xs]
-    yh = [torch.empty(y.shape, dtype=torch.float32).pin_memory() for y in ys]
-    xd = [torch.empty_like(x) for x in xs]
-    h2d = sum(x.numel() * x.element_size() for x in xh)
-    d2h = sum(y.numel() * 4 for y in yh)
+    # ---- e2e through the public API with host buffers: every step copies all of its
+    # activations in from pinned host memory (one copy), runs its kq.gemv calls and copies
+    # all of its outputs back (one copy). The K steps are recorded once as a CUDA graph, as
+    # a serving loop replays its step, so the host's Python overhead stays out of the GPU
+    # timeline; the copies run on every replay.
+    al = lambda n: (n + 255) // 256 * 256
+    xbytes = [x.numel() * x.element_size() for x in xs]
+    ybytes = [y.numel() * 4 for y in ys]
+    h2d, d2h = sum(xbytes), sum(ybytes)
+    xh_all = torch.zeros(sum(al(n) for n in xbytes), dtype=torch.uint8).pin_memory()
+    yh_all = torch.empty(sum(al(n) for n in ybytes), dtype=torch.uint8).pin_memory()
+    xd_all = torch.empty(xh_all.numel(), dtype=torch.uint8, device=dev)
+    yd_all = torch.empty(yh_all.numel(), dtype=torch.uint8, device=dev)
+    xd, yd, off = [], [], 0
+    for x, nb in zip(xs, xbytes):
+        xh_all[off:off + nb].copy_(x.contiguous().view(torch.uint8).reshape(-1).cpu())
+        xd.append(xd_all[off:off + nb].view(x.dtype).view(x.shape))
+        off += al(nb)
+    off = 0
+    for y, nb in zip(ys, ybytes):
+        yd.append(yd_all[off:off + nb].view(torch.float32).view(y.shape))
+        off += al(nb)
     e2e_steps = min(K_, 100)
-    for s in range(3):
+
+    def e2e_step(s):
+        xd_all.copy_(xh_all, non_blocking=True)
         for i, (N, K) in enumerate(spec["mats"]):
-            xd[i].copy_(xh[i], non_blocking=True)
-            kq.gemv(fmt, wsets[s % copies][i], xd[i], N, K, y=ys[i])
-            yh[i].copy_(ys[i], non_blocking=True)
-    torch.cuda.synchronize()
+            kq.gemv(fmt, wsets[s % copies][i], xd[i], N, K, y=yd[i],
+                    overlap=(i > 0 and spec["dtype"] == "bf16"))
+        yh_all.copy_(yd_all, non_blocking=True)
+
+    g_e2e = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        e2e_step(0)  # untimed eager step outside the capture
+        stream.synchronize()
+        with torch.cuda.graph(g_e2e, stream=stream):
+            for s in range(e2e_steps):
+                e2e_step(s)
+        g_e2e.replay()  # warm-up replay
+        stream.synchronize()
     if world > 1:
         dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for s in range(e2e_steps):
-        for i, (N, K) in enumerate(spec["mats"]):
-            xd[i].copy_(xh[i], non_blocking=True)
-            kq.gemv(fmt, wsets[s % copies][i], xd[i], N, K, y=ys[i])
-            yh[i].copy_(ys[i], non_blocking=True)
-    e1.record()
+    with torch.cuda.stream(stream):
+        e0.record()
+        g_e2e.replay()
+        e1.record()
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    # the graph's last step must have brought this step's result back to the host
+    assert torch.equal(yh_all[:ybytes[0]].view(torch.float32).view(ys[0].shape), yd[0].cpu())
 
     # ---- reduce over ranks (max time)
     ms_total, e2e_ms = max_over_ranks([ms_total, e2e_ms], dev, world)
@@ -744,7 +770,8 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "note": "eager kq.gemv calls from Python, pinned-host x in, y out, every step"},
+                    "note": "per step: one H2D copy of all x from pinned host memory, the kq.gemv calls, one "
+                            "D2H copy of all y; K steps recorded as one CUDA graph and replayed"},
             "gpu_launches": K_ * len(spec["mats"]),
             "clocks": clocks,
         }
