@@ -611,6 +611,16 @@ def main():
     torch.cuda.synchronize()
 
     stream = torch.cuda.Stream(device=dev)
+    # M > 16 (batched verify): kq_gemm, which runs the GEMV in passes of 16 token rows up to
+    # M = 32 (each row keeps its M = 1 bits) and the tensor-core product beyond
+    wsp = [torch.empty(max(256, kq.gemm_workspace_size(fmt, xdt, M, N, K)), dtype=torch.uint8, device=dev)
+           for (N, K) in spec["mats"]]
+
+    def product(i, w, x, N, K, y, overlap):
+        if M <= 16:
+            kq.gemv(fmt, w, x, N, K, y=y, overlap=overlap)
+        else:
+            kq.gemm(fmt, w, x, N, K, y=y, workspace=wsp[i])
 
     def launch_step(s, events=None):
         ws = wsets[s % copies]
@@ -619,7 +629,7 @@ def main():
                 events[s][i][0].record()
             # weights are never written inside the step: each launch may stream its
             # weights while the previous one finishes (programmatic dependent launch)
-            kq.gemv(fmt, ws[i], xs[i], N, K, y=ys[i], overlap=(spec["dtype"] == "bf16"))
+            product(i, ws[i], xs[i], N, K, ys[i], spec["dtype"] == "bf16")
             if events is not None:
                 events[s][i][1].record()
 
@@ -705,8 +715,7 @@ def main():
     def e2e_step(s):
         xd_all.copy_(xh_all, non_blocking=True)
         for i, (N, K) in enumerate(spec["mats"]):
-            kq.gemv(fmt, wsets[s % copies][i], xd[i], N, K, y=yd[i],
-                    overlap=(i > 0 and spec["dtype"] == "bf16"))
+            product(i, wsets[s % copies][i], xd[i], N, K, yd[i], i > 0 and spec["dtype"] == "bf16")
         yh_all.copy_(yd_all, non_blocking=True)
 
     g_e2e = torch.cuda.CUDAGraph()
@@ -764,7 +773,9 @@ def main():
                        "pct_of_8tbs": value / world / 8000.0},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": f"{peak_kind} hbm_gbs", "kernel": ("gemv_tma_kernel" if spec["dtype"] == "bf16" and spec["fmt"] != "q6_k" else "gemv_f32_kernel"),
+                         "peak_source": f"{peak_kind} hbm_gbs", "kernel": ("gemm_q4k_tc_kernel" if M > 32 else
+                                    ("gemv_tma_kernel" if spec["dtype"] == "bf16" and spec["fmt"] != "q6_k"
+                                     else "gemv_f32_kernel") + (" (16-row passes)" if M > 16 else "")),
                          "launch_us": launch_ms * 1e3, "launch_us_isolated": isolated_ms * 1e3,
                          "timing": "timed region (graph of K steps) / launches; isolated = event pair per launch"},
             "cpu_baseline": cpu,
@@ -772,7 +783,7 @@ def main():
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "note": "per step: one H2D copy of all x from pinned host memory, the kq.gemv calls, one "
                             "D2H copy of all y; K steps recorded as one CUDA graph and replayed"},
-            "gpu_launches": K_ * len(spec["mats"]),
+            "gpu_launches": K_ * len(spec["mats"]) * (-(-M // 16) if M <= 32 else 2),
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -117,10 +117,17 @@ int kq_gemv_ex(int fmt, const void* w_blocks, int x_dtype, const void* x, float*
                int K, unsigned flags, void* stream);
 
 /* Quantized GEMM (Kinetic README, "What makes it fast": long prompts as tiled matrix
- * products, each weight block unpacked once for many tokens).
+ * products, each weight block unpacked once for many tokens; a speculative check runs
+ * all of its guesses through one pass over the weights).
  *   M <= 16: identical to kq_gemv (same kernels, same bits); the workspace is unused.
- *   M  > 16: tensor-core (tcgen05) product for fmt = KQ_Q4_K, x_dtype = KQ_BF16 (other
- *            pairs: KQ_ERR_UNSUPPORTED). Every product the tensor cores form is exact: X
+ *   16 < M <= 32 with Q4_K x bf16, and every M > 16 for the other format / dtype pairs:
+ *            kq_gemv in passes of 16 token rows (rows c..c+15 in pass c/16, each pass
+ *            reading W once), so every row of Y has exactly the bits kq_gemv gives it and
+ *            the bit-identity across M holds for every M; the workspace is unused.
+ *            (Batched verify of up to 32 guesses: below a few hundred rows the tensor-core
+ *            product's time is set by unpacking W, and two passes are faster at M = 32.)
+ *   M  > 32 with fmt = KQ_Q4_K, x_dtype = KQ_BF16: tensor-core (tcgen05) product. Every
+ *            product the tensor cores form is exact: X
  *            goes to fp16 under an exact power-of-two scale per token; the weights enter
  *            as the integers sc*q with d applied per super-block in fp32 afterwards; the
  *            min term is a product of fp16 hi/lo splits of the sub-block sums of X and
@@ -128,7 +135,7 @@ int kq_gemv_ex(int fmt, const void* w_blocks, int x_dtype, const void* x, float*
  *            only (about 1e-6 of sum_k |w*x|). Not bit-identical to kq_gemv. Limits:
  *            64*dmin*m must be below 65504 (the fp16 range) for every sub-block.
  *   workspace/ws_bytes: device scratch of at least kq_gemm_workspace_size() bytes
- *            (M > 16: about M*(K + 3K/32)*2 + N*(3K/32)*2 bytes; otherwise 0),
+ *            (tensor-core route: about M*(K + 3K/32)*2 + N*(3K/32)*2 bytes; otherwise 0),
  *            256-byte aligned, owned by the caller; may be NULL when that size is 0.
  * Other arguments as kq_gemv. Errors: as kq_gemv, plus KQ_ERR_WORKSPACE. */
 int kq_gemm(int fmt, const void* w_blocks, int x_dtype, const void* x, float* y, int M, int N,

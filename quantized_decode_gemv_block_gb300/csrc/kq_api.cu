@@ -3,6 +3,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
+#include <algorithm>
 #include <string>
 
 #include "kq.h"
@@ -155,8 +156,19 @@ int kq_gemv_ex(int fmt, const void* w_blocks, int x_dtype, const void* x, float*
   return gemv_impl(fmt, w_blocks, x_dtype, x, y, M, N, K, static_cast<cudaStream_t>(stream), flags);
 }
 
+// kq_gemm's routes for M > 16. The tensor-core product exists for Q4_K x bf16; up to
+// kGemvPassMaxM rows the GEMV kernels in passes of 16 token rows are faster than it (its
+// weight unpacking, not M, sets its time below a few hundred rows) and keep every row's
+// bits those of kq_gemv. Pairs without a tensor-core product take the passes at any M.
+constexpr int kGemvPassRows = 16;
+constexpr int kGemvPassMaxM = 32;
+bool gemm_by_passes(int fmt, int x_dtype, int M) {
+  return M > kGemvPassRows && (!(fmt == KQ_Q4_K && x_dtype == KQ_BF16) || M <= kGemvPassMaxM);
+}
+
 size_t kq_gemm_workspace_size(int fmt, int x_dtype, int M, int N, int K) {
   if (M <= 16 || N <= 0 || fmt != KQ_Q4_K || x_dtype != KQ_BF16 || K <= 0 || K % 256 != 0) return 0;
+  if (gemm_by_passes(fmt, x_dtype, M)) return 0;
   return kq::gemm_tc_workspace(M, N, K);
 }
 
@@ -166,12 +178,22 @@ int kq_gemm(int fmt, const void* w_blocks, int x_dtype, const void* x, float* y,
     return gemv_impl(fmt, w_blocks, x_dtype, x, y, M, N, K, static_cast<cudaStream_t>(stream));
   int rc = check_common(fmt, w_blocks, x_dtype, x, y, M, N, K);
   if (rc != KQ_OK) return rc;
-  if (fmt != KQ_Q4_K || x_dtype != KQ_BF16)
-    return fail(KQ_ERR_UNSUPPORTED, "kq_gemm with M > 16 runs Q4_K weights with bf16 activations");
   if (N == 0) return ok();
   if (K == 0) {
     const cudaError_t e = cudaMemsetAsync(y, 0, sizeof(float) * (size_t)M * (size_t)N, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(KQ_ERR_CUDA, std::string("cudaMemsetAsync: ") + cudaGetErrorString(e));
+    return ok();
+  }
+  if (gemm_by_passes(fmt, x_dtype, M)) {
+    // token rows c..c+15 per pass; a pass may stream its weights while the previous one
+    // drains (it writes other rows of y and never w)
+    const size_t xe = x_dtype == KQ_BF16 ? 2 : 4;
+    for (int c = 0; c < M; c += kGemvPassRows) {
+      rc = gemv_impl(fmt, w_blocks, x_dtype, static_cast<const char*>(x) + (size_t)c * K * xe, y + (size_t)c * N,
+                     std::min(kGemvPassRows, M - c), N, K, static_cast<cudaStream_t>(stream),
+                     c > 0 ? static_cast<unsigned>(KQ_OVERLAP_PREVIOUS) : 0u);
+      if (rc != KQ_OK) return rc;
+    }
     return ok();
   }
   const size_t need = kq::gemm_tc_workspace(M, N, K);

@@ -1,4 +1,5 @@
-"""GPU parity of the tensor-core prefill product (kq_gemm with M > 16) against the fp64 oracle.
+"""GPU parity of kq_gemm against the fp64 oracle: the tensor-core prefill product (Q4_K x
+bf16, M > 32) and the 16-row GEMV passes (16 < M <= 32, and every M > 16 of the other pairs).
 
 Tolerance (the contract of the method): |y_gpu - y_ref| <= 1e-4 * sum_k |w_k x_k| per
 output element. The prefill path forms only exact products (X as fp16 under an exact
@@ -52,10 +53,10 @@ def run_gemm(kq, blocks, x_bits, N, K):
     return y.cpu().numpy().astype(np.float64)
 
 
-# (M, N, K): one tile; ragged M (tails of 72 and 1 tokens); ragged N (tails of 8 and 232
+# (M, N, K) of the tensor-core route (M > 32): one tile; ragged M (tails of 33, 72 and 1 tokens); ragged N (tails of 8 and 232
 # rows); several K super-blocks; more tiles than SMs; N % 4 != 0 (rows not 16-byte aligned:
 # the direct-store path) with an odd number of 128-row tiles (a cluster CTA with no rows).
-SHAPES = [(17, 256, 256), (200, 520, 1024), (129, 300, 512), (257, 1000, 2560), (384, 2048, 768),
+SHAPES = [(33, 256, 256), (200, 520, 1024), (129, 300, 512), (257, 1000, 2560), (384, 2048, 768),
           (130, 258, 512)]
 
 
@@ -120,12 +121,10 @@ def test_gemm_errors(kq):
     with pytest.raises(kq.KQError) as e:
         kq.gemm("q4_k", w, x, N, K, y=y, workspace=big[16:])  # not 256-byte aligned
     assert e.value.code == kq.KQ_ERR_WORKSPACE
-    w8 = torch.zeros((N, 34 * K // 32), dtype=torch.uint8, device="cuda")
-    with pytest.raises(kq.KQError) as e:
-        kq.gemm("q8_0", w8, x, N, K, y=y, workspace=big)
-    assert e.value.code == kq.KQ_ERR_UNSUPPORTED
-    assert kq.gemm_workspace_size("q8_0", torch.bfloat16, M, N, K) == 0
+    assert kq.gemm_workspace_size("q8_0", torch.bfloat16, M, N, K) == 0  # GEMV passes
     assert kq.gemm_workspace_size("q4_k", torch.bfloat16, 16, N, K) == 0
+    assert kq.gemm_workspace_size("q4_k", torch.bfloat16, 32, N, K) == 0  # GEMV passes
+    assert kq.gemm_workspace_size("q4_k", torch.bfloat16, 33, N, K) > 0   # tensor cores
 
 
 def test_full_prefill_9728x2560_m2048(kq, orc):
@@ -148,4 +147,52 @@ def test_full_prefill_9728x2560_m2048(kq, orc):
     yref, ay = orc.gemv_sampled(Q4_K, blocks, x, N, K, js, ns)
     got = y[js, ns].astype(np.float64)
     assert_close(got, yref, ay, "prefill 2048x9728x2560")
+    assert kq.device_errors() == 0
+
+
+def _gemv_rows_equal(kq, fmt, wd, x, y, N, K):
+    """Every row of y has the bits kq_gemv gives that row alone (M = 1)."""
+    for j in range(x.shape[0]):
+        r = kq.gemv(fmt, wd, x[j:j + 1].contiguous(), N, K)
+        torch.cuda.synchronize()
+        assert torch.equal(r.view(torch.int32)[0], y.view(torch.int32)[j]), f"{fmt} row {j}"
+
+
+@pytest.mark.parametrize("M", [17, 24, 32])
+def test_batched_verify_up_to_32_rows_is_gemv_bitwise(kq, orc, M):
+    """16 < M <= 32 (Q4_K, bf16): 16-row GEMV passes; each row keeps its M = 1 bits."""
+    N, K = 600, 1024  # ragged row tiles, four super-blocks
+    blocks = orc.quantize(Q4_K, inputs.weights(N, K, seed=M, tensor_id=Q4_K))
+    x_bits = inputs.activations_bf16(M, K, seed=M, tensor_id=3004)
+    wd, x = dev(blocks), bf16(x_bits)
+    assert kq.gemm_workspace_size("q4_k", torch.bfloat16, M, N, K) == 0
+    y = kq.gemm("q4_k", wd, x, N, K)
+    torch.cuda.synchronize()
+    yref, ay = orc.gemv(Q4_K, blocks, x_bits, N, K)
+    err = np.abs(y.cpu().numpy().astype(np.float64) - yref)
+    assert np.all(err <= TOL * ay), f"worst ratio {(err / ay).max():.3g}"
+    _gemv_rows_equal(kq, "q4_k", wd, x, y, N, K)
+    assert kq.device_errors() == 0
+
+
+@pytest.mark.parametrize("fmt,code,dtype,M", [("q8_0", 1, "f32", 20), ("q5_k", 4, "bf16", 40),
+                                              ("affine4", 3, "bf16", 18), ("q6_k", 5, "bf16", 33)])
+def test_gemm_passes_for_pairs_without_tensor_core_product(kq, orc, fmt, code, dtype, M):
+    """M > 16 for every other format / dtype pair: 16-row GEMV passes, within the contract
+    against the oracle and bit-identical, row by row, to kq_gemv."""
+    N, K = 300, 512
+    blocks = orc.quantize(code, inputs.weights(N, K, seed=M + code, tensor_id=code))
+    if dtype == "f32":
+        xh = inputs.activations_f32(M, K, seed=M, tensor_id=3005)
+        x = dev(xh)
+    else:
+        xh = inputs.activations_bf16(M, K, seed=M, tensor_id=3005)
+        x = bf16(xh)
+    wd = dev(blocks)
+    y = kq.gemm(fmt, wd, x, N, K)
+    torch.cuda.synchronize()
+    yref, ay = orc.gemv(code, blocks, xh, N, K)
+    err = np.abs(y.cpu().numpy().astype(np.float64) - yref)
+    assert np.all(err <= TOL * ay), f"{fmt}: worst ratio {(err / ay).max():.3g}"
+    _gemv_rows_equal(kq, fmt, wd, x, y, N, K)
     assert kq.device_errors() == 0
