@@ -172,6 +172,14 @@ __device__ __forceinline__ void unpack_t(uint32_t s0, uint32_t s2, const uint4& 
   }
 }
 
+// Bring super-block `sb` of a weight row into L2 (no registers, no completion to wait for).
+__device__ __forceinline__ void prefetch_block_l2(const uint8_t* rowp, int sb) {
+  const uint8_t* b = rowp + (long long)sb * 144;  // 144 bytes: at most two 128-byte lines
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(b) : "memory");
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(b + 143) : "memory");
+}
+constexpr int kPrefetchBlocks = 3;  // super-blocks (12 k-tiles) ahead of the unpacking
+
 struct RowChunk {  // what one row needs for one k-tile: header words, 32 quant bytes
   uint4 h, a, b;
 };
@@ -309,6 +317,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       RowChunk na, nb;
       load_chunk(na, rowa, 0, true);
       load_chunk(nb, rowb, 0, true);
+      // the unpacking reads each row from HBM one k-tile ahead, too late to hide its latency:
+      // keep the next few super-blocks of both rows on their way into L2
+      for (int j = 1; j <= kPrefetchBlocks && j < nsb; ++j) {
+        prefetch_block_l2(rowa, j);
+        prefetch_block_l2(rowb, j);
+      }
       for (int kt = 0; kt < kt_tile; ++kt) {
         const int s = it % STAGES;
         const RowChunk ca = na, cb = nb;
@@ -316,6 +330,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (km >= 0 && km + 1 < kt_main) {  // next chunk's bytes in flight while this one unpacks
           load_chunk(na, rowa, km + 1, ((km + 1) & 3) == 0);
           load_chunk(nb, rowb, km + 1, ((km + 1) & 3) == 0);
+        }
+        if (km >= 0 && (km & 3) == 0 && (km >> 2) + kPrefetchBlocks + 1 < nsb) {
+          prefetch_block_l2(rowa, (km >> 2) + kPrefetchBlocks + 1);
+          prefetch_block_l2(rowb, (km >> 2) + kPrefetchBlocks + 1);
         }
         if (!stage_free(it)) { fail(); stop = true; break; }
         if (aborted()) { stop = true; break; }
