@@ -51,7 +51,8 @@ constexpr int kDqThreads = kDqWarps * 32;  // each unpacks rows u and u + 64
 constexpr int kTmaWarp = kEpiWarps + kDqWarps, kMmaWarp = kTmaWarp + 1;
 constexpr int kTcThreads = (kMmaWarp + 1) * 32;
 constexpr int kTmemCols = 2 * TN;  // two accumulator groups in flight
-constexpr int kTcSmem = STAGES * kStageBytes + 1024 /*barriers*/ + 1024 /*alignment slack*/;
+constexpr int kInvBytes = kEpiWarps * (TN / 2) * 4;  // per epilogue warp: its tokens' 2^-e_j
+constexpr int kTcSmem = STAGES * kStageBytes + 1024 /*barriers*/ + kInvBytes + 1024 /*alignment slack*/;
 constexpr uint64_t kTcWaitNs = 2000000000ull;
 static_assert(kDqThreads * 2 == TM, "two weight rows per unpacking thread");
 
@@ -358,6 +359,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float acc[TN / 2];
 #pragma unroll
       for (int c = 0; c < TN / 2; ++c) acc[c] = 0.f;
+      // this warp's tokens' 2^-e_j, fetched now (their latency hides behind the first group)
+      // and read back from shared memory by the stores at the end of the tile
+      float* winv = reinterpret_cast<float*>(smem + STAGES * kStageBytes + 1024) + warp * (TN / 2);
+      for (int c = lane; c < TN / 2; c += 32) winv[c] = p.inv_scale[m0 + half * (TN / 2) + c];
       for (int g = 0; g <= nsb; ++g, ++grp) {
         const int buf = grp & 1;
         const float scale = g == 0 ? 1.0f : half_bits_to_float(ldg32(rowp + (long long)(g - 1) * 144));
@@ -381,14 +386,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // Y[j][n] = acc * 2^-e_j: for each token, the warp's 32 lanes write 32 consecutive floats
       const int j0 = m0 + half * (TN / 2);
       const bool nok = n < p.N;
+      __syncwarp();
 #pragma unroll
       for (int c0 = 0; c0 < TN / 2; c0 += 4) {
-        const float4 inv = *reinterpret_cast<const float4*>(p.inv_scale + j0 + c0);
+        const float4 inv = *reinterpret_cast<const float4*>(winv + c0);
         const float iv[4] = {inv.x, inv.y, inv.z, inv.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int j = j0 + c0 + i;
-          if (nok && j < p.M) p.y[(long long)j * p.N + n] = acc[c0 + i] * iv[i];
+          // Y is written once and not read here: stream it (evict-first in L2)
+          if (nok && j < p.M) __stcs(p.y + (long long)j * p.N + n, acc[c0 + i] * iv[i]);
         }
       }
     }
