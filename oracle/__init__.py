@@ -6,7 +6,7 @@ code with it. The arithmetic lives in ``oracle.cpp`` (plain C++, fp64, built
 without contraction); this module only marshals numpy arrays through ctypes.
 
 Each function states what it computes; the definitions and their sources are in
-the header of ``oracle.cpp`` and ``decode.cpp``.
+the headers of ``oracle.cpp``, ``decode.cpp`` and ``attention.cpp``.
 """
 from __future__ import annotations
 
@@ -18,7 +18,8 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SO = os.path.join(_HERE, "liboracle.so")
-_SOURCES = [os.path.join(_HERE, "oracle.cpp"), os.path.join(_HERE, "decode.cpp")]
+_SOURCES = [os.path.join(_HERE, "oracle.cpp"), os.path.join(_HERE, "decode.cpp"),
+            os.path.join(_HERE, "attention.cpp")]
 
 Q8_0, Q4_K, AFFINE4, Q5_K, Q6_K = 1, 2, 3, 4, 5
 F32, BF16 = 1, 2
@@ -61,6 +62,8 @@ def lib():
         L.orc_rmsnorm.argtypes = [P, P, I64, I64, ctypes.c_double]
         L.orc_decode_step.argtypes = [I, I, I, I, I, I, I, I, I, ctypes.c_double, P, P, P, P, P, P, I64,
                                       P, I, P]
+        L.orc_attention.argtypes = [I, I, I, I, I, P, P, P, P, ctypes.c_float, P, P]
+        L.orc_attention.restype = I
         _lib = L
     return _lib
 
@@ -199,3 +202,23 @@ def decode_step(dims: dict, layers: list, head: np.ndarray, x_bf16: np.ndarray, 
     if rc != 0:
         raise ValueError("orc_decode_step failed")
     return (out, xf) if return_head_input else out
+
+
+def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, L: int, n_q: int, n_kv: int, hd: int,
+              scale: float, mask: np.ndarray | None = None):
+    """(out, base), both M x (n_q*hd) fp64: decode attention of the M window tokens (definition
+    in attention.cpp). q: M x (n_q*hd) fp32; k, v: (L+M) x (n_kv*hd) bf16 bits (uint16);
+    mask: M uint32 words (bit j of word i: token i sees window token j) or None (causal)."""
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    k = np.ascontiguousarray(k, dtype=np.uint16)
+    v = np.ascontiguousarray(v, dtype=np.uint16)
+    M = q.shape[0]
+    out = np.empty((M, n_q * hd), dtype=np.float64)
+    base = np.empty((M, n_q * hd), dtype=np.float64)
+    mp = None
+    if mask is not None:
+        mask = np.ascontiguousarray(mask, dtype=np.uint32)
+        mp = _ptr(mask)
+    if lib().orc_attention(M, L, n_q, n_kv, hd, _ptr(q), _ptr(k), _ptr(v), mp, scale, _ptr(out), _ptr(base)) != 0:
+        raise ValueError("orc_attention: bad arguments")
+    return out, base
