@@ -63,6 +63,11 @@ def workload_spec(name: str, m: int):
     if name == "prefill":
         return dict(name="q4_k prefill gemm 9728x2560, X 2048x2560 bf16", fmt="q4_k", mats=[(9728, 2560)],
                     M=2048, dtype="bf16", prefill=True)
+    if name == "attention":
+        mm = min(m, 32)
+        return dict(name=f"decode attention, window of M={mm} over L=4096 cached positions, 16 q / 4 kv heads, "
+                         f"head_dim 128, bf16 KV", fmt=None, mats=[], M=mm, dtype="bf16", attention=True,
+                    L=4096, n_q=16, n_kv=4, hd=128)
     if name == "head":
         return dict(name=f"q8_0 lm head 151936x2048, M={m} bf16", fmt="q8_0", mats=[(151936, 2048)],
                     M=m, dtype="bf16")
@@ -211,9 +216,59 @@ def cpu_oracle_gbps(spec, budget_s: float, seed: int = 0):
     return nbytes * passes / el / 1e9, cores, passes, el
 
 
+ATTN_METRIC = "decode attention effective KV-cache read GB/s (window of M tokens over L cached positions)"
+
+
+def attention_inputs(spec, seed=0):
+    """Host inputs of the attention workload: q fp32, K and V bf16 bits, all N(0, 1)."""
+    from quantized_decode_gemv_block_gb300 import inputs
+    M, L, nq, nkv, hd = spec["M"], spec["L"], spec["n_q"], spec["n_kv"], spec["hd"]
+    q = inputs.activations_f32(M, nq * hd, seed=seed, tensor_id=7000)
+    k = inputs.activations_bf16(L + M, nkv * hd, seed=seed, tensor_id=7001)
+    v = inputs.activations_bf16(L + M, nkv * hd, seed=seed, tensor_id=7002)
+    return q, k, v
+
+
+def cpu_oracle_attention(spec, budget_s: float):
+    """The fp64 attention oracle (one host thread) on the same shape: KV bytes per second."""
+    import oracle
+    q, k, v = attention_inputs(spec)
+    nbytes = k.nbytes + v.nbytes
+    calls, t0 = 0, time.perf_counter()
+    while True:
+        oracle.attention(q, k, v, spec["L"], spec["n_q"], spec["n_kv"], spec["hd"], 1.0 / math.sqrt(spec["hd"]))
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return nbytes * calls / el / 1e9, 1, calls, el
+
+
 def run_reference(args, spec):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
+        return
+    if spec.get("attention"):
+        import oracle
+        q, k, v = attention_inputs(spec)
+        call = lambda: oracle.attention(q, k, v, spec["L"], spec["n_q"], spec["n_kv"], spec["hd"],
+                                        1.0 / math.sqrt(spec["hd"]))
+        for _ in range(args.warmup):
+            call()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            call()
+        el = time.perf_counter() - t0
+        v_ = (k.nbytes + v.nbytes) * args.steps / el / 1e9
+        print(json.dumps({"impl": "reference", "metric": ATTN_METRIC, "value": v_, "unit": "GB/s", "n_gpus": args.gpus,
+                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic", "config": {"workload": spec["name"], "M": spec["M"]},
+                          "cpu_baseline": {"value": v_, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                           "sample": "one attention call per step over the full shape, fp64 "
+                                                     "scalar oracle, one thread"},
+                          "e2e": {"value": v_, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+              flush=True)
         return
     import oracle
     from quantized_decode_gemv_block_gb300 import inputs
@@ -413,6 +468,135 @@ def run_prefill(args, spec):
         dist.destroy_process_group()
 
 
+def run_attention(args, spec):
+    """kq_attention (chunk kernel + combine kernel) per step, rotating KV caches, K steps per graph."""
+    import torch
+    import torch.distributed as dist
+
+    import quantized_decode_gemv_block_gb300 as kq
+    from quantized_decode_gemv_block_gb300 import build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    if rank == 0 or not os.path.exists(kq.LIB_PATH):
+        build.build()
+    if world > 1:
+        dist.barrier()
+    kq.load_library()
+    dev = torch.device("cuda", local)
+    M, L, nq, nkv, hd = spec["M"], spec["L"], spec["n_q"], spec["n_kv"], spec["hd"]
+    kvw = nkv * hd
+    step_bytes = 2 * (L + M) * kvw * 2  # every K and V row read once
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 129 * 2**20) or 129 * 2**20
+    copies = max(2, math.ceil(4 * l2 / step_bytes))
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 + rank)
+    kc = [torch.randn((L + M, kvw), generator=gen, device=dev).to(torch.bfloat16) for _ in range(copies)]
+    vc = [torch.randn((L + M, kvw), generator=gen, device=dev).to(torch.bfloat16) for _ in range(copies)]
+    q = torch.randn((M, nq * hd), generator=gen, device=dev)
+    o = torch.empty((M, nq * hd), device=dev)
+    ws = torch.empty(max(256, kq.lib().kq_attention_workspace_size(M, L, nq, nkv, hd)), dtype=torch.uint8, device=dev)
+    scale = 1.0 / math.sqrt(hd)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(s, qq=q, oo=o):
+        kq.attention(qq, kc[s % copies], vc[s % copies], L, nq, nkv, hd, scale, out=oo, workspace=ws)
+
+    def capture(n, body):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            body(0)
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for s in range(n):
+                    body(s)
+        return g
+
+    K_ = args.steps
+    g_warm, g_main = capture(args.warmup, step), capture(K_, step)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        g_warm.replay()
+    stream.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record()
+        g_main.replay()
+        t1.record()
+    torch.cuda.synchronize()
+    ms_step = t0.elapsed_time(t1) / K_
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < 1.0:
+        with torch.cuda.stream(stream):
+            g_main.replay()
+        stream.synchronize()
+    clocks = sampler.stop()
+    # e2e: q in from pinned host memory and o back, every step, graph-replayed
+    qh = q.cpu().pin_memory()
+    oh = torch.empty(o.shape, dtype=torch.float32).pin_memory()
+    qd = torch.empty_like(q)
+
+    def e2e_step(s):
+        qd.copy_(qh, non_blocking=True)
+        step(s, qd, o)
+        oh.copy_(o, non_blocking=True)
+
+    n_e2e = min(K_, 100)
+    g_e2e = capture(n_e2e, e2e_step)
+    with torch.cuda.stream(stream):
+        g_e2e.replay()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g_e2e.replay()
+        e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    ms_step, e2e_ms = max_over_ranks([ms_step, e2e_ms], dev, world)
+    peak, peak_kind = measured_peaks()
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, calls, el = cpu_oracle_attention(spec, args.cpu_budget)
+        cpu = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"{calls} full attention calls (same shape) in {el:.1f} s, fp64 scalar oracle, one thread"}
+    if rank == 0:
+        value = replica_rate(world, step_bytes, ms_step) / 1e9
+        achieved = step_bytes / (ms_step * 1e-3) / 1e9
+        line = {
+            "metric": ATTN_METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K_,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 x bf16 -> fp32", "data": "synthetic",
+            "config": {"workload": spec["name"], "M": M, "L": L, "kv_bytes_per_step": step_bytes,
+                       "l2": f"rotating KV caches: {copies} x {step_bytes} B >= 4x L2 ({l2} B)",
+                       "parallelism": "replicas" if world > 1 else "single gpu"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None, "peak_source": f"{peak_kind} hbm_gbs",
+                         "kernel": "attn_chunk_kernel + attn_combine_kernel (one kq_attention call)",
+                         "launch_us": ms_step * 1e3},
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": qh.numel() * 4, "d2h_bytes_per_step": oh.numel() * 4,
+                    "note": "per step: q in from pinned host memory, kq_attention, o out; graph-replayed"},
+            "gpu_launches": 2 * K_,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 def run_decode(args, spec):
     """The dense 28-layer decode step (kq_decode_step) as one CUDA graph, replayed K times."""
     import torch
@@ -552,7 +736,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="kq", choices=["kq", "reference"])
-    ap.add_argument("--workload", default="ffn", choices=["ffn", "ffn_q5k", "ffn_q6k", "verify", "q8_0", "head", "decode", "prefill"])
+    ap.add_argument("--workload", default="ffn", choices=["ffn", "ffn_q5k", "ffn_q6k", "verify", "q8_0", "head", "decode",
+                                                        "prefill", "attention"])
     ap.add_argument("--m", type=int, default=16)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -568,6 +753,9 @@ def main():
         return
     if spec.get("decode"):
         run_decode(args, spec)
+        return
+    if spec.get("attention"):
+        run_attention(args, spec)
         return
     if spec.get("prefill"):
         run_prefill(args, spec)

@@ -160,6 +160,32 @@ size_t kq_gemm_workspace_size(int fmt, int x_dtype, int M, int N, int K);
  * Errors: KQ_ERR_ARG, KQ_ERR_CUDA. */
 int kq_quantize(int fmt, const float* w, void* w_blocks, int N, int K, void* stream);
 
+/* ---- Decode attention of a verify window over a KV cache ----
+ * A speculative step checks its guesses in one pass (Kinetic README, "What makes it fast";
+ * Kapitsa README verifies a tree of guesses at once): window token i (0..M-1, at position
+ * L+i) attends to the cached positions 0..L-1 and to window positions L+j with j <= i, or,
+ * with a tree mask, those with bit j of mask[i] set. Query head hq reads kv head
+ * hq / (n_q / n_kv).
+ *   q        M x (n_q*head_dim) fp32 (device, 16-byte aligned); rounded to bf16 (nearest
+ *            even) before the products, as every activation between ops is bf16
+ *   k_cache, v_cache  (L+M) x (n_kv*head_dim) bf16 rows (device, 16-byte aligned); rows
+ *            L..L+M-1 hold the window's own keys and values (the caller appends them)
+ *   o        M x (n_q*head_dim) fp32 (device, overwritten)
+ *   M        1..32; L in 0..65000; head_dim 64 or 128; (n_q / n_kv) * M <= 128
+ *   mask     NULL (causal within the window) or M words in device memory
+ *   scale    multiplies q.k (usually 1/sqrt(head_dim))
+ *   o = sum_p softmax_p(scale q.k_p) v_p over the visible positions (zeros if none).
+ * Scores and sums are fp32 (products of bf16 on the tensor cores, the softmax weights
+ * carried as bf16 hi + lo pairs), so o is within about 1e-5 of sum_p w_p |v_p| of the exact
+ * value. The cached positions are cut into chunks by L alone and added in a fixed order: a
+ * token's output is bit-identical for every M and every position in the batch (given its
+ * own mask row). workspace: kq_attention_workspace_size() bytes, 256-byte aligned.
+ * Errors: KQ_ERR_ARG, KQ_ERR_WORKSPACE, KQ_ERR_CUDA. */
+size_t kq_attention_workspace_size(int M, int L, int n_q, int n_kv, int head_dim);
+int kq_attention(const float* q, const void* k_cache, const void* v_cache, float* o, int M, int L, int n_q,
+                 int n_kv, int head_dim, const unsigned int* mask, float scale, void* workspace, size_t ws_bytes,
+                 void* stream);
+
 /* ---- Decode step (composition of the GEMVs; Kinetic README, "What makes it fast": a
  * decode step is hundreds of small kernels replayed with one launch per token, and a
  * dense model reads all of its weights once per token). ----

@@ -73,6 +73,10 @@ def load_library(path: str = LIB_PATH):
     L.kq_device_errors.restype = I
     L.kq_decode_workspace_size.argtypes = [ctypes.POINTER(DecodeModelC), I]
     L.kq_decode_workspace_size.restype = SZ
+    L.kq_attention_workspace_size.argtypes = [I, I, I, I, I]
+    L.kq_attention_workspace_size.restype = SZ
+    L.kq_attention.argtypes = [P, P, P, P, I, I, I, I, I, P, ctypes.c_float, P, SZ, P]
+    L.kq_attention.restype = I
     L.kq_decode_step.argtypes = [ctypes.POINTER(DecodeModelC), P, P, I, P, SZ, P]
     L.kq_decode_step.restype = I
     L.kq_decode_step_static.argtypes = [ctypes.POINTER(DecodeModelC), P, P, I, P]
@@ -165,6 +169,23 @@ def gemm(fmt, w: torch.Tensor, x: torch.Tensor, N: int, K: int, y: torch.Tensor 
     _check(lib().kq_gemm(_fmt(fmt), w.data_ptr(), _x_dtype(x), x.data_ptr(), y.data_ptr(), M, N, K,
                          wp, wn, _stream(stream)))
     return y
+
+
+def attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, L: int, n_q: int, n_kv: int,
+              head_dim: int, scale: float, mask: torch.Tensor | None = None, out: torch.Tensor | None = None,
+              workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Decode attention of the M window tokens (kq_attention): q M x (n_q*head_dim) fp32,
+    k_cache / v_cache (L+M) x (n_kv*head_dim) bf16, mask None (causal) or M int32 words."""
+    M = q.shape[0]
+    if out is None:
+        out = torch.empty((M, n_q * head_dim), dtype=torch.float32, device=q.device)
+    need = lib().kq_attention_workspace_size(M, L, n_q, n_kv, head_dim)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(lib().kq_attention(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(), M, L, n_q,
+                              n_kv, head_dim, mask.data_ptr() if mask is not None else None, scale,
+                              workspace.data_ptr(), workspace.numel(), _stream(stream)))
+    return out
 
 
 def device_errors() -> int:

@@ -1,0 +1,336 @@
+// Decode attention of a verify window over a KV cache (grouped-query heads).
+//
+// A speculative step checks its M guesses in one pass (Kinetic README, "What makes it
+// fast"; the tree of guesses of Kapitsa README): window token i attends to every cached
+// position 0..L-1 and to the window positions L+j it may see (j <= i, or bit j of its tree
+// mask). Query head hq reads kv head hq / group. q (fp32) is rounded to bf16, K and V are
+// bf16, scores and sums are fp32.
+//
+// Work split (a function of L, never of M): the cached positions are cut into chunks of 64;
+// the window is one more chunk of its own. One CTA per (chunk, kv head) holds the chunk's
+// K and V rows and the Q rows of its head group in shared memory; row r = i*group + g is
+// query head kvh*group + g of token i, so a token's row sits in the same MMA slot whatever
+// M is. Each warp owns 16 rows: S = Q K^T on mma.sync (bf16 in, fp32 out), the chunk's
+// row maximum m and p = exp(s - m), l = sum p, and o = P V on mma.sync with P split into
+// bf16 hi + lo parts (P = hi + lo to 2^-16 relative), so o carries fp32 rounding only.
+// A second kernel adds the chunks in index order, each weighted by exp(m_c - max m).
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "kq.h"
+#include "kq_device.cuh"
+#include "kq_internal.h"
+
+namespace kq {
+namespace {
+
+constexpr int kChunk = 64;
+constexpr int kAttnThreads = 256;  // 8 warps x 16 query rows
+constexpr int kAttnMaxRows = 128;
+
+struct AttnParams {
+  const float* q;      // M x (n_q*hd)
+  const uint16_t* k;   // (L+M) x (n_kv*hd) bf16
+  const uint16_t* v;
+  const uint32_t* mask;  // M words or null (causal)
+  float* part;         // [n_kv][nchunks][R][hd + 2]: unnormalised o, m, l
+  float* o;            // M x (n_q*hd)
+  int M, L, n_q, n_kv, group, R, nchunks;
+  float scale;
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_addr(p)));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t& r0, uint32_t& r1, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(smem_addr(p)));
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t& r0, uint32_t& r1, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(smem_addr(p)));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+         ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+}
+__device__ __forceinline__ float bf16_rn_f(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
+template <int HD>
+__global__ void __launch_bounds__(kAttnThreads, 2) attn_chunk_kernel(const AttnParams p) {
+  constexpr int LD = HD + 8;  // shared row stride (elements): 16-byte pad, conflict-free ldmatrix
+  extern __shared__ __align__(16) uint16_t asmem[];
+  uint16_t* Qs = asmem;                  // [128][LD]
+  uint16_t* Ks = Qs + kAttnMaxRows * LD;  // [64][LD]
+  uint16_t* Vs = Ks + kChunk * LD;        // [64][LD]
+  const int c = blockIdx.x, kvh = blockIdx.y;
+  const int nc = p.nchunks - 1;           // cached chunks; chunk nc is the window
+  const bool win = c == nc;
+  const int pos0 = win ? p.L : c * kChunk;
+  const int npos = win ? p.M : min(kChunk, p.L - pos0);
+  const int kvw = p.n_kv * HD, qw = p.n_q * HD;
+  const int rows16 = (p.R + 15) & ~15;
+
+  // every load of the chunk's K and V rows and of the Q rows leaves before the first store
+  constexpr int KV_PER_T = kChunk * (HD / 8) / kAttnThreads;      // 16-byte pieces per thread
+  constexpr int Q_PER_T = kAttnMaxRows * (HD / 4) / kAttnThreads;  // float4 pieces per thread
+  uint4 kv[KV_PER_T], vv[KV_PER_T];
+  float4 qf[Q_PER_T];
+#pragma unroll
+  for (int t = 0; t < KV_PER_T; ++t) {
+    const int e = threadIdx.x + t * kAttnThreads, r = e / (HD / 8), c8 = e - r * (HD / 8);
+    kv[t] = vv[t] = make_uint4(0u, 0u, 0u, 0u);
+    if (r < npos) {
+      const long long off = (long long)(pos0 + r) * kvw + kvh * HD + c8 * 8;
+      kv[t] = ldg128(p.k + off);
+      vv[t] = ldg128(p.v + off);
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < Q_PER_T; ++t) {
+    const int e = threadIdx.x + t * kAttnThreads, r = e / (HD / 4), c4 = e - r * (HD / 4);
+    qf[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r < p.R) {
+      const int i = r / p.group, hq = kvh * p.group + (r - i * p.group);
+      qf[t] = __ldg(reinterpret_cast<const float4*>(p.q + (long long)i * qw + hq * HD + c4 * 4));
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < KV_PER_T; ++t) {
+    const int e = threadIdx.x + t * kAttnThreads, r = e / (HD / 8), c8 = e - r * (HD / 8);
+    *reinterpret_cast<uint4*>(Ks + r * LD + c8 * 8) = kv[t];
+    *reinterpret_cast<uint4*>(Vs + r * LD + c8 * 8) = vv[t];
+  }
+#pragma unroll
+  for (int t = 0; t < Q_PER_T; ++t) {
+    const int e = threadIdx.x + t * kAttnThreads, r = e / (HD / 4), c4 = e - r * (HD / 4);
+    if (r < rows16)
+      *reinterpret_cast<uint2*>(Qs + r * LD + c4 * 4) =
+          make_uint2(pack_bf16(qf[t].x, qf[t].y), pack_bf16(qf[t].z, qf[t].w));
+  }
+  __syncthreads();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q4 = lane & 3;
+  if (16 * warp >= p.R) return;  // no rows for this warp (uniform)
+  const int r0 = 16 * warp;
+
+  // S = Q K^T for this warp's 16 rows and the chunk's 64 positions
+  float s[8][4];
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < HD / 16; ++kk) {
+    uint32_t a[4];
+    ldsm_x4(a, Qs + (r0 + (lane & 15)) * LD + kk * 16 + (lane >> 4) * 8);
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      uint32_t b0, b1;
+      ldsm_x2(b0, b1, Ks + (nt * 8 + (lane & 7)) * LD + kk * 16 + ((lane >> 3) & 1) * 8);
+      mma_bf16_16816(s[nt], a, b0, b1, s[nt]);
+    }
+  }
+
+  // scale, visibility, row maxima (rows g and g+8 of the block; a quad shares a row)
+  const int ra = r0 + g, rb = r0 + g + 8;
+  const int ia = ra / p.group, ib = rb / p.group;
+  const uint32_t ma = win ? (p.mask ? __ldg(p.mask + min(ia, p.M - 1)) : (ia >= 31 ? 0xFFFFFFFFu : ((2u << ia) - 1u))) : 0u;
+  const uint32_t mb = win ? (p.mask ? __ldg(p.mask + min(ib, p.M - 1)) : (ib >= 31 ? 0xFFFFFFFFu : ((2u << ib) - 1u))) : 0u;
+  float mxa = -INFINITY, mxb = -INFINITY;
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int col = nt * 8 + 2 * q4 + e;
+      const bool va = ra < p.R && col < npos && (!win || ((ma >> col) & 1u));
+      const bool vb = rb < p.R && col < npos && (!win || ((mb >> col) & 1u));
+      s[nt][e] = va ? s[nt][e] * p.scale : -INFINITY;
+      s[nt][2 + e] = vb ? s[nt][2 + e] * p.scale : -INFINITY;
+      mxa = fmaxf(mxa, s[nt][e]);
+      mxb = fmaxf(mxb, s[nt][2 + e]);
+    }
+#pragma unroll
+  for (int o = 1; o <= 2; o <<= 1) {
+    mxa = fmaxf(mxa, __shfl_xor_sync(0xFFFFFFFFu, mxa, o));
+    mxb = fmaxf(mxb, __shfl_xor_sync(0xFFFFFFFFu, mxb, o));
+  }
+  const float ca = mxa == -INFINITY ? 0.f : mxa, cb = mxb == -INFINITY ? 0.f : mxb;
+  float la = 0.f, lb = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      s[nt][e] = expf(s[nt][e] - ca);  // exp(-inf) = 0 for positions not seen
+      s[nt][2 + e] = expf(s[nt][2 + e] - cb);
+      la += s[nt][e];
+      lb += s[nt][2 + e];
+    }
+#pragma unroll
+  for (int o = 1; o <= 2; o <<= 1) {
+    la += __shfl_xor_sync(0xFFFFFFFFu, la, o);
+    lb += __shfl_xor_sync(0xFFFFFFFFu, lb, o);
+  }
+
+  // o = P V, P = hi + lo in bf16; the accumulator fragment of S is the A fragment of P
+  float acc[HD / 8][4];
+#pragma unroll
+  for (int dt = 0; dt < HD / 8; ++dt) acc[dt][0] = acc[dt][1] = acc[dt][2] = acc[dt][3] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < kChunk / 16; ++kk) {
+    const float* p0 = s[2 * kk];
+    const float* p1 = s[2 * kk + 1];
+    const float hi0 = bf16_rn_f(p0[0]), hi1 = bf16_rn_f(p0[1]), hi2 = bf16_rn_f(p0[2]), hi3 = bf16_rn_f(p0[3]);
+    const float hi4 = bf16_rn_f(p1[0]), hi5 = bf16_rn_f(p1[1]), hi6 = bf16_rn_f(p1[2]), hi7 = bf16_rn_f(p1[3]);
+    const uint32_t ah[4] = {pack_bf16(hi0, hi1), pack_bf16(hi2, hi3), pack_bf16(hi4, hi5), pack_bf16(hi6, hi7)};
+    const uint32_t al[4] = {pack_bf16(p0[0] - hi0, p0[1] - hi1), pack_bf16(p0[2] - hi2, p0[3] - hi3),
+                            pack_bf16(p1[0] - hi4, p1[1] - hi5), pack_bf16(p1[2] - hi6, p1[3] - hi7)};
+#pragma unroll
+    for (int dt = 0; dt < HD / 8; ++dt) {
+      uint32_t b0, b1;
+      ldsm_x2_t(b0, b1, Vs + (kk * 16 + (lane & 15)) * LD + dt * 8);
+      mma_bf16_16816(acc[dt], ah, b0, b1, acc[dt]);
+      mma_bf16_16816(acc[dt], al, b0, b1, acc[dt]);
+    }
+  }
+
+  // the chunk's partial: unnormalised o, its row maximum and sum
+  constexpr int PW = HD + 2;
+  float* base = p.part + ((long long)kvh * p.nchunks + c) * p.R * PW;
+#pragma unroll
+  for (int dt = 0; dt < HD / 8; ++dt) {
+    const int d = dt * 8 + 2 * q4;
+    if (ra < p.R) *reinterpret_cast<float2*>(base + (long long)ra * PW + d) = make_float2(acc[dt][0], acc[dt][1]);
+    if (rb < p.R) *reinterpret_cast<float2*>(base + (long long)rb * PW + d) = make_float2(acc[dt][2], acc[dt][3]);
+  }
+  if (q4 == 0) {
+    if (ra < p.R) *reinterpret_cast<float2*>(base + (long long)ra * PW + HD) = make_float2(mxa, la);
+    if (rb < p.R) *reinterpret_cast<float2*>(base + (long long)rb * PW + HD) = make_float2(mxb, lb);
+  }
+}
+
+// out[i][hq][d] = sum_c e_c o_c[d] / sum_c e_c l_c, e_c = exp(m_c - max_c m_c); zeros when
+// the token sees no position. One CTA per (row, kv head) of kCombGroups x HD threads: group
+// g adds the chunks c = g (mod kCombGroups) in index order (eight chunks' loads in flight at
+// once), then the groups' sums are added in group order. The chunks' (m, l) pass through
+// shared memory. The order depends on L alone.
+constexpr int kMaxChunks = 1024;
+constexpr int kCombGroups = 4;
+template <int HD>
+__global__ void __launch_bounds__(HD * kCombGroups) attn_combine_kernel(const AttnParams p) {
+  constexpr int PW = HD + 2, NT = HD * kCombGroups;
+  __shared__ float sm_m[kMaxChunks], sm_l[kMaxChunks], sm_red[NT / 32];
+  __shared__ float sm_num[kCombGroups][HD], sm_den[kCombGroups];
+  const int r = blockIdx.x, kvh = blockIdx.y, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int grp = t / HD, d = t - grp * HD;
+  const float* base = p.part + (long long)kvh * p.nchunks * p.R * PW + (long long)r * PW;
+  const long long cs = (long long)p.R * PW;
+  float mloc = -INFINITY;
+  for (int c = t; c < p.nchunks; c += NT) {
+    const float2 ml = *reinterpret_cast<const float2*>(base + c * cs + HD);
+    sm_m[c] = ml.x;
+    sm_l[c] = ml.y;
+    mloc = fmaxf(mloc, ml.x);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xFFFFFFFFu, mloc, o));
+  if (lane == 0) sm_red[warp] = mloc;
+  __syncthreads();
+  float mt = sm_red[0];
+#pragma unroll
+  for (int w = 1; w < NT / 32; ++w) mt = fmaxf(mt, sm_red[w]);  // a maximum: exact in any order
+  for (int c = t; c < p.nchunks; c += NT) sm_m[c] = (mt == -INFINITY || sm_m[c] == -INFINITY) ? 0.f : expf(sm_m[c] - mt);
+  __syncthreads();
+  float num = 0.f, den = 0.f;
+  int c = grp;
+  for (; c + 7 * kCombGroups < p.nchunks; c += 8 * kCombGroups) {
+    float ov[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ov[j] = base[(c + j * kCombGroups) * cs + d];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      num = __fmaf_rn(sm_m[c + j * kCombGroups], ov[j], num);
+      den = __fmaf_rn(sm_m[c + j * kCombGroups], sm_l[c + j * kCombGroups], den);
+    }
+  }
+  for (; c < p.nchunks; c += kCombGroups) {
+    num = __fmaf_rn(sm_m[c], base[c * cs + d], num);
+    den = __fmaf_rn(sm_m[c], sm_l[c], den);
+  }
+  sm_num[grp][d] = num;
+  if (d == 0) sm_den[grp] = den;
+  __syncthreads();
+  if (grp == 0) {
+    float n = sm_num[0][d], dd = sm_den[0];
+#pragma unroll
+    for (int g = 1; g < kCombGroups; ++g) {
+      n += sm_num[g][d];
+      dd += sm_den[g];
+    }
+    const int i = r / p.group, hq = kvh * p.group + (r - i * p.group);
+    p.o[(long long)i * p.n_q * HD + hq * HD + d] = dd > 0.f ? n / dd : 0.f;
+  }
+}
+
+int attn_chunks(int L) { return (L + kChunk - 1) / kChunk + 1; }
+
+template <int HD>
+int launch_attn(const AttnParams& prm, cudaStream_t s, std::string* err) {
+  constexpr int LD = HD + 8;
+  const size_t smem = (size_t)(kAttnMaxRows + 2 * kChunk) * LD * 2;
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(attn_chunk_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) {
+      *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
+      return -1;
+    }
+    attr_done[dev] = true;
+  }
+  attn_chunk_kernel<HD><<<dim3(prm.nchunks, prm.n_kv), kAttnThreads, smem, s>>>(prm);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) {
+    attn_combine_kernel<HD><<<dim3(prm.R, prm.n_kv), HD * kCombGroups, 0, s>>>(prm);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) {
+    *err = std::string("attention launch: ") + cudaGetErrorString(e);
+    return -1;
+  }
+  return 0;
+}
+
+}  // namespace
+
+size_t attention_workspace(int M, int L, int n_q, int n_kv, int hd) {
+  const int R = (n_q / n_kv) * M;
+  return (size_t)n_kv * attn_chunks(L) * R * (hd + 2) * sizeof(float);
+}
+
+int launch_attention(const float* q, const uint16_t* k, const uint16_t* v, float* o, int M, int L, int n_q, int n_kv,
+                     int hd, const uint32_t* mask, float scale, void* ws, cudaStream_t s, std::string* err) {
+  AttnParams prm;
+  prm.q = q;
+  prm.k = k;
+  prm.v = v;
+  prm.mask = mask;
+  prm.part = static_cast<float*>(ws);
+  prm.o = o;
+  prm.M = M;
+  prm.L = L;
+  prm.n_q = n_q;
+  prm.n_kv = n_kv;
+  prm.group = n_q / n_kv;
+  prm.R = prm.group * M;
+  prm.nchunks = attn_chunks(L);
+  prm.scale = scale;
+  if (hd == 128) return launch_attn<128>(prm, s, err);
+  if (hd == 64) return launch_attn<64>(prm, s, err);
+  *err = "head_dim must be 64 or 128";
+  return -1;
+}
+
+}  // namespace kq

@@ -239,6 +239,39 @@ int kq_decode_step(const kq_decode_model* model, const void* x, float* logits, i
   return ok();
 }
 
+static int attention_check(int M, int L, int n_q, int n_kv, int head_dim, std::string* err) {
+  if (M < 1 || M > 32) { *err = "M must be in 1..32 (the window's tokens)"; return -1; }
+  if (L < 0 || L > 65000) { *err = "L must be in 0..65000"; return -1; }
+  if (n_q < 1 || n_kv < 1 || n_q % n_kv) { *err = "n_q must be a positive multiple of n_kv"; return -1; }
+  if (head_dim != 64 && head_dim != 128) { *err = "head_dim must be 64 or 128"; return -1; }
+  if ((n_q / n_kv) * M > 128) { *err = "(n_q / n_kv) * M must be <= 128"; return -1; }
+  return 0;
+}
+
+size_t kq_attention_workspace_size(int M, int L, int n_q, int n_kv, int head_dim) {
+  std::string err;
+  if (attention_check(M, L, n_q, n_kv, head_dim, &err) != 0) return 0;
+  return kq::attention_workspace(M, L, n_q, n_kv, head_dim);
+}
+
+int kq_attention(const float* q, const void* k_cache, const void* v_cache, float* o, int M, int L, int n_q,
+                 int n_kv, int head_dim, const unsigned int* mask, float scale, void* workspace, size_t ws_bytes,
+                 void* stream) {
+  std::string err;
+  if (attention_check(M, L, n_q, n_kv, head_dim, &err) != 0) return fail(KQ_ERR_ARG, err);
+  if (!q || !k_cache || !v_cache || !o) return fail(KQ_ERR_ARG, "q, k_cache, v_cache or o is NULL");
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 4) || (mask && !aligned(mask, 4)))
+    return fail(KQ_ERR_ARG, "misaligned q, k_cache, v_cache, o or mask");
+  const size_t need = kq::attention_workspace(M, L, n_q, n_kv, head_dim);
+  if (!workspace || ws_bytes < need || !aligned(workspace, 256))
+    return fail(KQ_ERR_WORKSPACE, "workspace must be >= " + std::to_string(need) + " bytes, 256-byte aligned");
+  if (kq::launch_attention(q, static_cast<const uint16_t*>(k_cache), static_cast<const uint16_t*>(v_cache), o, M, L,
+                           n_q, n_kv, head_dim, reinterpret_cast<const uint32_t*>(mask), scale, workspace,
+                           static_cast<cudaStream_t>(stream), &err) != 0)
+    return fail(KQ_ERR_CUDA, err);
+  return ok();
+}
+
 int kq_quantize(int fmt, const float* w, void* w_blocks, int N, int K, void* stream) {
   if (!fmt_known(fmt)) return fail(KQ_ERR_UNSUPPORTED, "unknown block format " + std::to_string(fmt));
   if (N < 0 || K < 0) return fail(KQ_ERR_ARG, "N and K must be >= 0");

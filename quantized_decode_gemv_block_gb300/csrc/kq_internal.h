@@ -63,6 +63,11 @@ size_t decode_workspace_size(const kq_decode_model* m, int M);
 int decode_step(const kq_decode_model* m, const uint16_t* x, float* logits, int M, void* ws, int num_sms,
                 cudaStream_t s, std::string* err);
 
+// Decode attention of a verify window over a KV cache (attention.cu).
+size_t attention_workspace(int M, int L, int n_q, int n_kv, int hd);
+int launch_attention(const float* q, const uint16_t* k, const uint16_t* v, float* o, int M, int L, int n_q, int n_kv,
+                     int hd, const uint32_t* mask, float scale, void* ws, cudaStream_t s, std::string* err);
+
 // GPU quantizers (fp64 arithmetic).
 int launch_quantize(int fmt, const float* w, void* blocks, int N, int K, cudaStream_t stream,
                     std::string* err);

@@ -82,6 +82,18 @@ def test_argument_errors_before_any_cuda_call(kqlib):
     assert L.kq_last_error().decode() == ""
     assert L.kq_quantize(kqlib.Q4_K, fake, fake, 4, 100, None) == kqlib.KQ_ERR_ARG
     assert L.kq_quantize(99, fake, fake, 4, 256, None) == kqlib.KQ_ERR_UNSUPPORTED
+    # decode attention: shape and pointer checks before any CUDA call
+    bad = [(0, 10, 16, 4, 128), (33, 10, 16, 4, 128), (4, -1, 16, 4, 128), (4, 10, 6, 4, 128),
+           (4, 10, 16, 4, 96), (32, 10, 32, 4, 128)]
+    for (M, Lc, nq, nkv, hd) in bad:
+        assert L.kq_attention_workspace_size(M, Lc, nq, nkv, hd) == 0
+        assert L.kq_attention(fake, fake, fake, fake, M, Lc, nq, nkv, hd, None, 1.0, fake, 1 << 30, None) \
+            == kqlib.KQ_ERR_ARG, (M, Lc, nq, nkv, hd)
+    need = L.kq_attention_workspace_size(8, 100, 16, 4, 128)
+    assert need == 4 * 3 * 32 * 130 * 4  # kv heads x (2 cached chunks + the window) x rows x (d + m, l)
+    assert L.kq_attention(fake, fake, fake, fake, 8, 100, 16, 4, 128, None, 1.0, fake, need - 1, None) \
+        == kqlib.KQ_ERR_WORKSPACE
+    assert L.kq_attention(None, fake, fake, fake, 8, 100, 16, 4, 128, None, 1.0, fake, need, None) == kqlib.KQ_ERR_ARG
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

@@ -1,0 +1,90 @@
+"""GPU decode attention (kq_attention) against the fp64 oracle, and its batch invariance.
+
+Tolerance: |o - o_ref| <= 1e-4 * sum_p w_p |v_p| per element (the contract's scale: the
+softmax-weighted magnitude of what is summed). The kernel's products of bf16 values are exact
+in fp32, the softmax weights enter the second product as bf16 hi + lo pairs (2^-16
+relative), so its error is fp32 rounding of the scores (a few 1e-7 relative, amplified by
+|score| through exp) and of the sums.
+"""
+import numpy as np
+import pytest
+import torch
+
+import quantized_decode_gemv_block_gb300 as kq
+from quantized_decode_gemv_block_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def built():
+    from quantized_decode_gemv_block_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+def make(M, L, n_q, n_kv, hd, seed):
+    q = inputs.activations_f32(M, n_q * hd, seed=seed, tensor_id=7000)
+    k = inputs.activations_bf16(L + M, n_kv * hd, seed=seed, tensor_id=7001)
+    v = inputs.activations_bf16(L + M, n_kv * hd, seed=seed, tensor_id=7002)
+    return q, k, v
+
+
+def dev_bf16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def run(q, k, v, L, n_q, n_kv, hd, scale, mask=None):
+    md = torch.from_numpy(mask.view(np.int32)).cuda() if mask is not None else None
+    o = kq.attention(torch.from_numpy(q).cuda(), dev_bf16(k), dev_bf16(v), L, n_q, n_kv, hd, scale, mask=md)
+    torch.cuda.synchronize()
+    return o.cpu().numpy()
+
+
+def check(o, ref, base, what):
+    err = np.abs(o.astype(np.float64) - ref)
+    bad = err > TOL * base
+    assert not bad.any(), f"{what}: {bad.sum()} outside; worst {(err / np.maximum(base, 1e-300)).max():.3g}"
+
+
+# (M, L, n_q, n_kv, head_dim): one token and no context; a partial chunk; exactly one chunk;
+# one past a chunk; head_dim 64; 128 query rows (4 heads x 32 tokens); many chunks; no GQA
+SHAPES = [(1, 0, 16, 4, 128), (1, 1, 16, 4, 128), (4, 63, 16, 4, 128), (8, 64, 16, 4, 128),
+          (16, 65, 8, 2, 64), (32, 200, 8, 2, 128), (5, 1000, 16, 4, 128), (32, 4096, 4, 4, 128)]
+
+
+@pytest.mark.parametrize("M,L,n_q,n_kv,hd", SHAPES)
+def test_attention_matches_oracle(built, orc, M, L, n_q, n_kv, hd):
+    q, k, v = make(M, L, n_q, n_kv, hd, seed=M + L)
+    scale = float(np.float32(1.0 / np.sqrt(hd)))
+    o = run(q, k, v, L, n_q, n_kv, hd, scale)
+    ref, base = orc.attention(q, k, v, L, n_q, n_kv, hd, scale)
+    check(o, ref, base, f"attention M={M} L={L} {n_q}/{n_kv} hd={hd}")
+    assert kq.device_errors() == 0
+
+
+def test_tree_mask_and_tokens_that_see_nothing(built, orc):
+    M, L, n_q, n_kv, hd = 12, 100, 16, 4, 128
+    q, k, v = make(M, L, n_q, n_kv, hd, seed=3)
+    rng = np.random.default_rng(5)
+    mask = np.array([(int(rng.integers(0, 1 << 12)) | (1 << i)) & ((2 << i) - 1) for i in range(M)], np.uint32)
+    o = run(q, k, v, L, n_q, n_kv, hd, 0.09, mask)
+    ref, base = orc.attention(q, k, v, L, n_q, n_kv, hd, 0.09, mask=mask)
+    check(o, ref, base, "tree mask")
+    # no context and an empty mask row: zeros
+    mask0 = np.array([0] + [1 << i for i in range(1, 4)], np.uint32)
+    q4, k4, v4 = make(4, 0, 4, 2, 64, seed=9)
+    o = run(q4, k4, v4, 0, 4, 2, 64, 0.125, mask0)
+    assert np.all(o[0] == 0.0)
+    ref, base = orc.attention(q4, k4, v4, 0, 4, 2, 64, 0.125, mask=mask0)
+    check(o, ref, base, "empty row")
+
+
+def test_a_tokens_output_is_the_same_for_every_window_size(built):
+    L, n_q, n_kv, hd = 777, 16, 4, 128
+    q, k, v = make(32, L, n_q, n_kv, hd, seed=11)
+    full = run(q[:8], k[:L + 8], v[:L + 8], L, n_q, n_kv, hd, 0.0883)
+    for M in (1, 3, 5, 8):
+        o = run(q[:M], k[:L + M], v[:L + M], L, n_q, n_kv, hd, 0.0883)
+        assert np.array_equal(o.view(np.uint32), full[:M].view(np.uint32)), f"M={M}"
