@@ -64,6 +64,9 @@ def lib():
                                       P, I, P]
         L.orc_attention.argtypes = [I, I, I, I, I, P, P, P, P, ctypes.c_float, P, P]
         L.orc_attention.restype = I
+        L.orc_decode_step_attn.argtypes = [I, I, I, I, I, I, I, I, I, ctypes.c_double, P, P, P, P, P, P, P, I,
+                                           P, ctypes.c_float, P, I64, P, I, P]
+        L.orc_decode_step_attn.restype = I
         _lib = L
     return _lib
 
@@ -222,3 +225,36 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, L: int, n_q: int, n_k
     if lib().orc_attention(M, L, n_q, n_kv, hd, _ptr(q), _ptr(k), _ptr(v), mp, scale, _ptr(out), _ptr(base)) != 0:
         raise ValueError("orc_attention: bad arguments")
     return out, base
+
+
+def decode_step_attn(dims: dict, layers: list, head: np.ndarray, k_cache: list, v_cache: list, L: int,
+                     x_bf16: np.ndarray, scale: float, mask: np.ndarray | None = None, nthreads: int = 0,
+                     return_head_input: bool = False):
+    """Logits (M x vocab, fp64) of one decode step with attention over a KV cache (definition in
+    decode.cpp, orc_decode_step_attn). k_cache[l], v_cache[l]: L x kv_dim bf16 bits (uint16)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    M = x.shape[0]
+    keep = [np.ascontiguousarray(a, dtype=np.uint8) for lay in layers for a in lay]
+    n = max(1, len(layers))
+    ptrs = [[keep[4 * l + i].ctypes.data for l in range(len(layers))] for i in range(4)]
+    arrs = [(ctypes.c_void_p * n)(*p) for p in ptrs]
+    kk = [np.ascontiguousarray(a, dtype=np.uint16) for a in k_cache]
+    vv = [np.ascontiguousarray(a, dtype=np.uint16) for a in v_cache]
+    karr = (ctypes.c_void_p * n)(*[a.ctypes.data for a in kk])
+    varr = (ctypes.c_void_p * n)(*[a.ctypes.data for a in vv])
+    headb = np.ascontiguousarray(head, dtype=np.uint8)
+    out = np.empty((M, dims["vocab"]), dtype=np.float64)
+    xf = np.empty((M, dims["hidden"]), dtype=np.uint16)
+    mp = None
+    if mask is not None:
+        mask = np.ascontiguousarray(mask, dtype=np.uint32)
+        mp = _ptr(mask)
+    nt = nthreads or os.cpu_count() or 1
+    rc = lib().orc_decode_step_attn(dims["n_layers"], dims["hidden"], dims["q_dim"], dims["kv_dim"],
+                                    dims["head_dim"], dims["ffn"], dims["vocab"], dims["layer_fmt"],
+                                    dims["head_fmt"], dims["eps"], *[ctypes.cast(a, ctypes.c_void_p) for a in arrs],
+                                    _ptr(headb), ctypes.cast(karr, ctypes.c_void_p), ctypes.cast(varr, ctypes.c_void_p),
+                                    L, mp, scale, _ptr(x), M, _ptr(out), nt, _ptr(xf))
+    if rc != 0:
+        raise ValueError("orc_decode_step_attn failed")
+    return (out, xf) if return_head_input else out

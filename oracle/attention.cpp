@@ -44,10 +44,22 @@ uint16_t f32_to_bf16_rn(float x) {
 
 extern "C" {
 
+int orc_attention_bf16q(int M, int L, int n_q, int n_kv, int hd, const uint16_t* qb, const uint16_t* k,
+                        const uint16_t* v, const uint32_t* mask, float scale, double* out, double* base);
+
 // q: M x (n_q*hd) fp32; k, v: (L+M) x (n_kv*hd) bf16 bits; mask: M words or NULL.
 // out, base: M x (n_q*hd) fp64. Returns 0, or -1 on bad arguments.
 int orc_attention(int M, int L, int n_q, int n_kv, int hd, const float* q, const uint16_t* k, const uint16_t* v,
                   const uint32_t* mask, float scale, double* out, double* base) {
+  if (M < 1 || M > 32 || n_q < 1 || hd < 1) return -1;
+  std::vector<uint16_t> qb((size_t)M * n_q * hd);
+  for (size_t e = 0; e < qb.size(); ++e) qb[e] = f32_to_bf16_rn(q[e]);
+  return orc_attention_bf16q(M, L, n_q, n_kv, hd, qb.data(), k, v, mask, scale, out, base);
+}
+
+// The same with q given as bf16 bits (already rounded); base may be NULL.
+int orc_attention_bf16q(int M, int L, int n_q, int n_kv, int hd, const uint16_t* qb, const uint16_t* k,
+                        const uint16_t* v, const uint32_t* mask, float scale, double* out, double* base) {
   if (M < 1 || M > 32 || L < 0 || n_q < 1 || n_kv < 1 || hd < 1 || n_q % n_kv) return -1;
   const int group = n_q / n_kv, qw = n_q * hd, kw = n_kv * hd;
   std::vector<double> qv(hd), s;
@@ -62,10 +74,13 @@ int orc_attention(int M, int L, int n_q, int n_kv, int hd, const float* q, const
     for (int hq = 0; hq < n_q; ++hq) {
       const int kvh = hq / group;
       double* o = out + (size_t)i * qw + (size_t)hq * hd;
-      double* b = base + (size_t)i * qw + (size_t)hq * hd;
-      for (int d = 0; d < hd; ++d) o[d] = b[d] = 0.0;
+      double* b = base ? base + (size_t)i * qw + (size_t)hq * hd : nullptr;
+      for (int d = 0; d < hd; ++d) {
+        o[d] = 0.0;
+        if (b) b[d] = 0.0;
+      }
       if (pos.empty()) continue;
-      for (int d = 0; d < hd; ++d) qv[d] = bf16_bits_to_double(f32_to_bf16_rn(q[(size_t)i * qw + (size_t)hq * hd + d]));
+      for (int d = 0; d < hd; ++d) qv[d] = bf16_bits_to_double(qb[(size_t)i * qw + (size_t)hq * hd + d]);
       s.assign(pos.size(), 0.0);
       double mx = -INFINITY;
       for (size_t t = 0; t < pos.size(); ++t) {
@@ -86,7 +101,7 @@ int orc_attention(int M, int L, int n_q, int n_kv, int hd, const float* q, const
         for (int d = 0; d < hd; ++d) {
           const double vv = bf16_bits_to_double(vp[d]);
           o[d] += w * vv;
-          b[d] += w * std::fabs(vv);
+          if (b) b[d] += w * std::fabs(vv);
         }
       }
     }

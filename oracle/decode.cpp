@@ -17,6 +17,8 @@
 
 extern "C" int orc_gemv(int fmt, const uint8_t* blocks, int x_dtype, const void* x, int64_t M, int64_t N,
                         int64_t K, double* y, double* absy, int nthreads);
+extern "C" int orc_attention_bf16q(int M, int L, int n_q, int n_kv, int hd, const uint16_t* qb, const uint16_t* k,
+                                   const uint16_t* v, const uint32_t* mask, float scale, double* out, double* base);
 
 namespace {
 
@@ -73,6 +75,63 @@ int orc_rmsnorm(const double* h, uint16_t* out, int64_t M, int64_t D, double eps
   std::vector<uint16_t> o;
   rmsnorm_bf16(hv, M, D, eps, o);
   std::memcpy(out, o.data(), sizeof(uint16_t) * (size_t)(M * D));
+  return 0;
+}
+
+// The step with attention over a KV cache (the step above with its attention stand-in
+// replaced; attention.cpp defines the attention): per layer the window's k and v (rounded to
+// bf16) are appended at positions L..L+M-1 of a copy of the layer's cache, q is rounded to
+// bf16, and the attention output is rounded to bf16 as it feeds Wo. k_cache[l], v_cache[l]:
+// L rows of kv_dim bf16 (read only). mask: NULL (causal) or M words. scale: the score
+// multiplier (a float, as the kernels take it).
+int orc_decode_step_attn(int n_layers, int hidden, int q_dim, int kv_dim, int head_dim, int ffn, int vocab,
+                         int layer_fmt, int head_fmt, double eps, const uint8_t* const* w_qkv,
+                         const uint8_t* const* w_o, const uint8_t* const* w_gu, const uint8_t* const* w_down,
+                         const uint8_t* w_head, const uint16_t* const* k_cache, const uint16_t* const* v_cache,
+                         int L, const uint32_t* mask, float scale, const uint16_t* x_bf16, int64_t M,
+                         double* logits, int nthreads, uint16_t* x_final) {
+  const int64_t D = hidden, QKV = q_dim + 2 * kv_dim, F = ffn;
+  const int n_q = q_dim / head_dim, n_kv = kv_dim / head_dim;
+  const int BF16 = 2;
+  std::vector<double> h((size_t)(M * D));
+  for (int64_t i = 0; i < M * D; ++i) h[(size_t)i] = bf16_to_double(x_bf16[i]);
+  std::vector<uint16_t> xb;
+  std::vector<double> qkv((size_t)(M * QKV)), y((size_t)(M * D)), gu((size_t)(M * 2 * F)), att((size_t)(M * q_dim));
+  std::vector<uint16_t> oin((size_t)(M * q_dim)), act((size_t)(M * F)), qb((size_t)(M * q_dim));
+  std::vector<uint16_t> kc((size_t)((L + M) * kv_dim)), vc((size_t)((L + M) * kv_dim));
+  for (int l = 0; l < n_layers; ++l) {
+    rmsnorm_bf16(h, M, D, eps, xb);
+    if (orc_gemv(layer_fmt, w_qkv[l], BF16, xb.data(), M, QKV, D, qkv.data(), nullptr, nthreads)) return -1;
+    if (L > 0) {
+      std::memcpy(kc.data(), k_cache[l], sizeof(uint16_t) * (size_t)L * kv_dim);
+      std::memcpy(vc.data(), v_cache[l], sizeof(uint16_t) * (size_t)L * kv_dim);
+    }
+    for (int64_t j = 0; j < M; ++j) {
+      for (int c = 0; c < q_dim; ++c) qb[(size_t)(j * q_dim + c)] = double_to_bf16_rn(qkv[(size_t)(j * QKV + c)]);
+      for (int c = 0; c < kv_dim; ++c) {
+        kc[(size_t)((L + j) * kv_dim + c)] = double_to_bf16_rn(qkv[(size_t)(j * QKV + q_dim + c)]);
+        vc[(size_t)((L + j) * kv_dim + c)] = double_to_bf16_rn(qkv[(size_t)(j * QKV + q_dim + kv_dim + c)]);
+      }
+    }
+    if (orc_attention_bf16q((int)M, L, n_q, n_kv, head_dim, qb.data(), kc.data(), vc.data(), mask, scale,
+                            att.data(), nullptr))
+      return -1;
+    for (int64_t e = 0; e < M * q_dim; ++e) oin[(size_t)e] = double_to_bf16_rn(att[(size_t)e]);
+    if (orc_gemv(layer_fmt, w_o[l], BF16, oin.data(), M, D, q_dim, y.data(), nullptr, nthreads)) return -1;
+    for (int64_t i = 0; i < M * D; ++i) h[(size_t)i] += y[(size_t)i];
+    rmsnorm_bf16(h, M, D, eps, xb);
+    if (orc_gemv(layer_fmt, w_gu[l], BF16, xb.data(), M, 2 * F, D, gu.data(), nullptr, nthreads)) return -1;
+    for (int64_t j = 0; j < M; ++j)
+      for (int64_t i = 0; i < F; ++i) {
+        const double g = gu[(size_t)(j * 2 * F + i)], u = gu[(size_t)(j * 2 * F + F + i)];
+        act[(size_t)(j * F + i)] = double_to_bf16_rn(g / (1.0 + std::exp(-g)) * u);
+      }
+    if (orc_gemv(layer_fmt, w_down[l], BF16, act.data(), M, D, F, y.data(), nullptr, nthreads)) return -1;
+    for (int64_t i = 0; i < M * D; ++i) h[(size_t)i] += y[(size_t)i];
+  }
+  rmsnorm_bf16(h, M, D, eps, xb);
+  if (x_final) std::memcpy(x_final, xb.data(), sizeof(uint16_t) * (size_t)(M * D));
+  if (orc_gemv(head_fmt, w_head, BF16, xb.data(), M, vocab, D, logits, nullptr, nthreads)) return -1;
   return 0;
 }
 

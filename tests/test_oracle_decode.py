@@ -103,3 +103,41 @@ def test_decode_composition_against_numpy_restatement(orc):
     # numpy sums in another order: allow a few ulps, and the rare bf16 tie flip upstream
     err = np.abs(got - ref) / (np.abs(ref).max() + 1e-30)
     assert np.quantile(err, 0.99) < 1e-9 and err.max() < 1e-2
+
+
+def test_attention_step_with_self_only_visibility_is_the_stand_in(orc):
+    """With no cached context and each token seeing only itself, attention over the cache is
+    the stand-in (softmax weight 1 on the token's own value): identical fp64 logits."""
+    layers, head = tiny_model(orc, TINY, seed=4)
+    M = 3
+    x = inputs.activations_bf16(M, TINY["hidden"], seed=5)
+    ref = orc.decode_step(TINY, layers, head, x)
+    empty = [np.zeros((0, TINY["kv_dim"]), np.uint16)] * TINY["n_layers"]
+    got = orc.decode_step_attn(TINY, layers, head, empty, empty, 0, x, 0.125,
+                               mask=np.array([1 << i for i in range(M)], np.uint32))
+    assert np.array_equal(got, ref)
+    # one token, causal: the same
+    got1 = orc.decode_step_attn(TINY, layers, head, empty, empty, 0, x[:1], 0.125)
+    assert np.array_equal(got1, ref[:1])
+
+
+def test_attention_step_depends_on_the_cache_and_the_window(orc):
+    layers, head = tiny_model(orc, TINY, seed=6)
+    M, L = 4, 9
+    x = inputs.activations_bf16(M, TINY["hidden"], seed=7)
+    rng = np.random.default_rng(8)
+    kc = [(rng.standard_normal((L, TINY["kv_dim"])).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+          for _ in range(TINY["n_layers"])]
+    vc = [(rng.standard_normal((L, TINY["kv_dim"])).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+          for _ in range(TINY["n_layers"])]
+    a = orc.decode_step_attn(TINY, layers, head, kc, vc, L, x, 0.125)
+    # causal: token 0 alone and token 0 inside the window agree; later tokens see the earlier ones
+    a0 = orc.decode_step_attn(TINY, layers, head, kc, vc, L, x[:1], 0.125)
+    assert np.array_equal(a0[0], a[0])
+    b = orc.decode_step_attn(TINY, layers, head, kc, vc, L, x[[0, 2, 1, 3]], 0.125)
+    assert np.array_equal(b[0], a[0]) and not np.allclose(b[3], a[3])
+    # the cached values matter
+    vc2 = [v.copy() for v in vc]
+    vc2[0][3] ^= 0x0100
+    c = orc.decode_step_attn(TINY, layers, head, kc, vc2, L, x, 0.125)
+    assert not np.array_equal(c, a)
