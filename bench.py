@@ -623,7 +623,16 @@ def run_decode(args, spec):
     model = kqd.random_model(d, seed=rank, device=str(dev))
     wbytes = kqd.weight_bytes(model)
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 129 * 2**20) or 129 * 2**20
-    g = kqd.GraphStep(model, M)
+    cache, kv_bytes, L = None, 0, args.attn_ctx
+    if L > 0:  # attention over a cache of L random bf16 rows per layer instead of the stand-in
+        cache = kq.KVCache(d["n_layers"], L + M, d["kv_dim"], device=str(dev))
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(77 + rank)
+        for t in cache.k + cache.v:
+            t.copy_(torch.randn(t.shape, generator=gen, device=dev).to(torch.bfloat16))
+        cache.length = L
+        kv_bytes = 2 * d["n_layers"] * (L + M) * d["kv_dim"] * 2
+    g = kqd.GraphStep(model, M, cache=cache)
     g.x.copy_(torch.randn((M, d["hidden"]), device=dev).to(torch.bfloat16))
     sampler = ClockSampler(local)
     sampler.start()
@@ -703,6 +712,9 @@ def run_decode(args, spec):
                          f"OpenMP over rows, M={M}) in {el:.1f} s"}
     if rank == 0:
         value = replica_rate(world, wbytes, ms_step) / 1e9
+        if cache is not None:
+            spec = dict(spec, name=spec["name"] + f", attention over L={L} cached positions (bf16 KV, "
+                                                  f"{kv_bytes} B per step)")
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -710,7 +722,8 @@ def run_decode(args, spec):
             "config": {"workload": spec["name"], "M": M, "weight_bytes_per_step": wbytes,
                        "tokens_per_s_equivalent": world * M / (ms_step * 1e-3),
                        "l2": f"weights per step {wbytes} B > 4x L2 ({l2} B): every step streams from HBM",
-                       "launches_per_step": 8 * d["n_layers"] + 2,
+                       "launches_per_step": (10 if cache is not None else 8) * d["n_layers"] + 2,
+                       "kv_cache_bytes_per_step": kv_bytes,
                        "parallelism": "replicas" if world > 1 else "single gpu",
                        "pct_of_8tbs": value / world / 8000.0},
             "roofline": {"bound": "hbm", "achieved": wbytes / (gemv_ms * 1e-3) / 1e9, "peak": peak,
@@ -721,7 +734,7 @@ def run_decode(args, spec):
             "e2e": {"value": world * wbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": xh.numel() * 2, "d2h_bytes_per_step": lh.numel() * 4,
                     "note": "pinned-host x copied in, graph of kq_decode_step, logits copied out, every step"},
-            "gpu_launches": args.steps * (8 * d["n_layers"] + 2),
+            "gpu_launches": args.steps * ((10 if cache is not None else 8) * d["n_layers"] + 2),
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
@@ -741,6 +754,8 @@ def main():
     ap.add_argument("--m", type=int, default=16)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--attn-ctx", type=int, default=0,
+                    help="decode workload: attention over this many cached positions instead of the stand-in")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     spec = workload_spec(args.workload, args.m)

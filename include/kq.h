@@ -227,6 +227,28 @@ size_t kq_decode_workspace_size(const kq_decode_model* model, int M);
 int kq_decode_step(const kq_decode_model* model, const void* x, float* logits, int M, void* workspace,
                    size_t ws_bytes, void* stream);
 
+/* ---- Decode step with attention over a KV cache (a true speculative step) ----
+ * kq_decode_step with its attention stand-in replaced by kq_attention's attention: per layer
+ * the window's k and v (rounded to bf16) are written to rows L..L+M-1 of the layer's cache,
+ * q = the first q_dim columns of [q k v], scale = 1/sqrt(head_dim) (as a float), token i sees
+ * the L cached rows and window rows j <= i (or bit j of mask[i]); the attention output is
+ * rounded to bf16 as it feeds Wo. A speculative decoder verifies M guesses in one step and
+ * then advances `length` by the guesses it accepts (the rows after them are rewritten by the
+ * next step). Model limits as kq_decode_step, plus head_dim 64 or 128 and
+ * (q_dim / kv_dim) * M <= 128. */
+typedef struct kq_kv_cache {
+  void* const* k;  /* per layer: capacity rows of kv_dim bf16 (device, 16-byte aligned) */
+  void* const* v;
+  int length;      /* L: rows 0..L-1 hold the context (0..65000) */
+  int capacity;    /* rows per layer array: L + M <= capacity */
+} kq_kv_cache;
+/* Device workspace bytes kq_decode_step_attn needs (0 on invalid arguments). */
+size_t kq_decode_attn_workspace_size(const kq_decode_model* model, int M, int L);
+/* x, logits, workspace as kq_decode_step; cache: HOST struct and pointer arrays of device
+ * pointers; mask: NULL (causal) or M words of device memory. */
+int kq_decode_step_attn(const kq_decode_model* model, const kq_kv_cache* cache, const void* x, float* logits,
+                        int M, const unsigned int* mask, void* workspace, size_t ws_bytes, void* stream);
+
 /* ---- Decode step that allocates nothing (no counterpart in the engine pages) ----
  * kq_decode_step needs a device workspace from its caller. Some callers cannot call
  * cudaMalloc or any allocating routine: code that only borrows a GPU from a host framework

@@ -77,6 +77,10 @@ def load_library(path: str = LIB_PATH):
     L.kq_attention_workspace_size.restype = SZ
     L.kq_attention.argtypes = [P, P, P, P, I, I, I, I, I, P, ctypes.c_float, P, SZ, P]
     L.kq_attention.restype = I
+    L.kq_decode_attn_workspace_size.argtypes = [ctypes.POINTER(DecodeModelC), I, I]
+    L.kq_decode_attn_workspace_size.restype = SZ
+    L.kq_decode_step_attn.argtypes = [ctypes.POINTER(DecodeModelC), ctypes.POINTER(KVCacheC), P, P, I, P, P, SZ, P]
+    L.kq_decode_step_attn.restype = I
     L.kq_decode_step.argtypes = [ctypes.POINTER(DecodeModelC), P, P, I, P, SZ, P]
     L.kq_decode_step.restype = I
     L.kq_decode_step_static.argtypes = [ctypes.POINTER(DecodeModelC), P, P, I, P]
@@ -205,6 +209,30 @@ def quantize(fmt, w: torch.Tensor, out: torch.Tensor | None = None, stream=None)
     return out
 
 
+class KVCacheC(ctypes.Structure):
+    """Mirror of kq_kv_cache (include/kq.h)."""
+    _fields_ = [("k", ctypes.POINTER(ctypes.c_void_p)), ("v", ctypes.POINTER(ctypes.c_void_p)),
+                ("length", ctypes.c_int), ("capacity", ctypes.c_int)]
+
+
+class KVCache:
+    """Per-layer bf16 K and V arrays (capacity x kv_dim device tensors) and the cached length."""
+
+    def __init__(self, n_layers: int, capacity: int, kv_dim: int, device="cuda", k=None, v=None):
+        self.k = k if k is not None else [torch.zeros((capacity, kv_dim), dtype=torch.bfloat16, device=device)
+                                          for _ in range(n_layers)]
+        self.v = v if v is not None else [torch.zeros((capacity, kv_dim), dtype=torch.bfloat16, device=device)
+                                          for _ in range(n_layers)]
+        self.capacity, self.length = capacity, 0
+        n = max(1, n_layers)
+        self._ka = (ctypes.c_void_p * n)(*[t.data_ptr() for t in self.k])
+        self._va = (ctypes.c_void_p * n)(*[t.data_ptr() for t in self.v])
+
+    def c(self) -> KVCacheC:
+        return KVCacheC(ctypes.cast(self._ka, ctypes.POINTER(ctypes.c_void_p)),
+                        ctypes.cast(self._va, ctypes.POINTER(ctypes.c_void_p)), self.length, self.capacity)
+
+
 class DecodeModel:
     """A dense decoder whose weights are block-quantized device tensors (kq_decode_step).
 
@@ -235,6 +263,26 @@ class DecodeModel:
             workspace = torch.empty(self.workspace_size(M), dtype=torch.uint8, device=x.device)
         _check(lib().kq_decode_step(ctypes.byref(self.c), x.data_ptr(), logits.data_ptr(), M,
                                     workspace.data_ptr(), workspace.numel(), _stream(stream)))
+        return logits
+
+    def attn_workspace_size(self, M: int, L: int) -> int:
+        return lib().kq_decode_attn_workspace_size(ctypes.byref(self.c), M, L)
+
+    def step_attn(self, x: torch.Tensor, cache: "KVCache", mask: torch.Tensor | None = None,
+                  logits: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+        """kq_decode_step_attn: logits for M bf16 token rows attending to cache.length cached
+        positions (the window's k, v are written at rows length..length+M-1; length is not
+        advanced here). mask: None (causal) or M int32 words."""
+        M = x.shape[0]
+        if logits is None:
+            logits = torch.empty((M, self.vocab), dtype=torch.float32, device=x.device)
+        if workspace is None:
+            workspace = torch.empty(self.attn_workspace_size(M, cache.length), dtype=torch.uint8, device=x.device)
+        cc = cache.c()
+        _check(lib().kq_decode_step_attn(ctypes.byref(self.c), ctypes.byref(cc), x.data_ptr(), logits.data_ptr(), M,
+                                         mask.data_ptr() if mask is not None else None, workspace.data_ptr(),
+                                         workspace.numel(), _stream(stream)))
         return logits
 
     def step_static(self, x: torch.Tensor, logits: torch.Tensor, stream=None) -> torch.Tensor:

@@ -30,12 +30,14 @@ constexpr int kAttnThreads = 256;  // 8 warps x 16 query rows
 constexpr int kAttnMaxRows = 128;
 
 struct AttnParams {
-  const float* q;      // M x (n_q*hd)
+  const float* q;      // M rows of n_q*hd, q_stride apart
   const uint16_t* k;   // (L+M) x (n_kv*hd) bf16
   const uint16_t* v;
   const uint32_t* mask;  // M words or null (causal)
   float* part;         // [n_kv][nchunks][R][hd + 2]: unnormalised o, m, l
-  float* o;            // M x (n_q*hd)
+  float* o;            // M x (n_q*hd) fp32, or null
+  uint16_t* o16;       // M x (n_q*hd) bf16 (nearest even), or null
+  int q_stride;        // elements between q rows
   int M, L, n_q, n_kv, group, R, nchunks;
   float scale;
 };
@@ -71,7 +73,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_chunk_kernel(const AttnP
   const bool win = c == nc;
   const int pos0 = win ? p.L : c * kChunk;
   const int npos = win ? p.M : min(kChunk, p.L - pos0);
-  const int kvw = p.n_kv * HD, qw = p.n_q * HD;
+  const int kvw = p.n_kv * HD, qw = p.q_stride;
   const int rows16 = (p.R + 15) & ~15;
 
   // every load of the chunk's K and V rows and of the Q rows leaves before the first store
@@ -269,7 +271,10 @@ __global__ void __launch_bounds__(HD * kCombGroups) attn_combine_kernel(const At
       dd += sm_den[g];
     }
     const int i = r / p.group, hq = kvh * p.group + (r - i * p.group);
-    p.o[(long long)i * p.n_q * HD + hq * HD + d] = dd > 0.f ? n / dd : 0.f;
+    const float res = dd > 0.f ? n / dd : 0.f;
+    const long long oi = (long long)i * p.n_q * HD + hq * HD + d;
+    if (p.o) p.o[oi] = res;
+    if (p.o16) p.o16[oi] = __bfloat16_as_ushort(__float2bfloat16_rn(res));
   }
 }
 
@@ -310,10 +315,13 @@ size_t attention_workspace(int M, int L, int n_q, int n_kv, int hd) {
   return (size_t)n_kv * attn_chunks(L) * R * (hd + 2) * sizeof(float);
 }
 
-int launch_attention(const float* q, const uint16_t* k, const uint16_t* v, float* o, int M, int L, int n_q, int n_kv,
-                     int hd, const uint32_t* mask, float scale, void* ws, cudaStream_t s, std::string* err) {
+int launch_attention(const float* q, int q_stride, const uint16_t* k, const uint16_t* v, float* o, uint16_t* o16,
+                     int M, int L, int n_q, int n_kv, int hd, const uint32_t* mask, float scale, void* ws,
+                     cudaStream_t s, std::string* err) {
   AttnParams prm;
   prm.q = q;
+  prm.q_stride = q_stride;
+  prm.o16 = o16;
   prm.k = k;
   prm.v = v;
   prm.mask = mask;

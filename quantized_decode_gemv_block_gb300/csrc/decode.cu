@@ -16,6 +16,7 @@
 // so each one streams its weights while the glue before it still runs.
 #include <cuda_bf16.h>
 
+#include <cmath>
 #include <vector>
 
 #include "kq.h"
@@ -110,6 +111,23 @@ __global__ void __launch_bounds__(kGlueThreads) swiglu_kernel(const float* __res
   }
 }
 
+// Rows L..L+M-1 of a layer's cache: k = bf16(qkv[:, q_dim : q_dim+kv_dim]), v = the next kv_dim.
+__global__ void __launch_bounds__(kGlueThreads) kv_append_kernel(const float* __restrict__ qkv,
+                                                                 uint16_t* __restrict__ kc, uint16_t* __restrict__ vc,
+                                                                 int M, int q_dim, int kv_dim, int L) {
+  pdl_trigger();
+  pdl_wait();
+  const int qkv_dim = q_dim + 2 * kv_dim;
+  const long long total = (long long)M * kv_dim;
+  for (long long e = blockIdx.x * (long long)kGlueThreads + threadIdx.x; e < total;
+       e += (long long)gridDim.x * kGlueThreads) {
+    const int j = (int)(e / kv_dim), c = (int)(e - (long long)j * kv_dim);
+    const float* row = qkv + (long long)j * qkv_dim + q_dim;
+    kc[(long long)(L + j) * kv_dim + c] = f2bf(row[c]);
+    vc[(long long)(L + j) * kv_dim + c] = f2bf(row[kv_dim + c]);
+  }
+}
+
 template <class... Args>
 cudaError_t launch_pdl(void (*kern)(Args...), int grid, cudaStream_t s, bool pdl, Args... args) {
   cudaLaunchConfig_t cfg = {};
@@ -193,6 +211,60 @@ int decode_step(const kq_decode_model* m, const uint16_t* x, float* logits, int 
     if (ck(launch_pdl(gqa_expand_kernel, ew_grid((long long)M * m->q_dim), s, true, (const float*)w.qkv, w.x, M,
                       m->q_dim, m->kv_dim, m->head_dim, group),
            "gqa_expand"))
+      return -1;
+    if (gemv(m->layer_fmt, m->w_o[l], w.x, w.y, m->hidden, m->q_dim)) return -1;
+    if (ck(launch_pdl(add_rmsnorm_kernel, M, s, true, w.h, (const uint16_t*)nullptr, (const float*)w.y, w.x,
+                      m->hidden, m->rms_eps),
+           "add_rmsnorm"))
+      return -1;
+    if (gemv(m->layer_fmt, m->w_gate_up[l], w.x, w.gu, 2 * m->ffn, m->hidden)) return -1;
+    if (ck(launch_pdl(swiglu_kernel, ew_grid((long long)M * m->ffn), s, true, (const float*)w.gu, w.x, M, m->ffn),
+           "swiglu"))
+      return -1;
+    if (gemv(m->layer_fmt, m->w_down[l], w.x, w.y, m->hidden, m->ffn)) return -1;
+    if (ck(launch_pdl(add_rmsnorm_kernel, M, s, true, w.h, (const uint16_t*)nullptr, (const float*)w.y, w.x,
+                      m->hidden, m->rms_eps),
+           "add_rmsnorm"))
+      return -1;
+  }
+  return gemv(m->head_fmt, m->w_head, w.x, logits, m->vocab, m->hidden);
+}
+
+size_t decode_attn_workspace_size(const kq_decode_model* m, int M, int L) {
+  return al256(carve(m, M, nullptr).bytes) +
+         attention_workspace(M, L, m->q_dim / m->head_dim, m->kv_dim / m->head_dim, m->head_dim);
+}
+
+int decode_step_attn(const kq_decode_model* m, const kq_kv_cache* c, const uint16_t* x, float* logits, int M,
+                     const uint32_t* mask, void* ws, int num_sms, cudaStream_t s, std::string* err) {
+  const Ws w = carve(m, M, ws);
+  void* aws = static_cast<uint8_t*>(ws) + al256(w.bytes);
+  const int qkv_dim = m->q_dim + 2 * m->kv_dim;
+  const int n_q = m->q_dim / m->head_dim, n_kv = m->kv_dim / m->head_dim;
+  const float scale = 1.0f / sqrtf((float)m->head_dim);
+  auto rowb = [](int fmt, int K) { return (long long)kq_row_bytes(fmt, K); };
+  auto ew_grid = [&](long long n) { return (int)std::min<long long>(4 * (long long)num_sms, (n + kGlueThreads - 1) / kGlueThreads); };
+  auto ck = [&](cudaError_t e, const char* what) {
+    if (e != cudaSuccess) { *err = std::string(what) + ": " + cudaGetErrorString(e); return -1; }
+    return 0;
+  };
+  auto gemv = [&](int fmt, const void* wt, const uint16_t* xin, float* y, int N, int K) {
+    return launch_gemv_mma(fmt, wt, xin, y, M, N, K, rowb(fmt, K), num_sms, s, true, err);
+  };
+  if (ck(launch_pdl(add_rmsnorm_kernel, M, s, false, w.h, x, (const float*)nullptr, w.x, m->hidden, m->rms_eps),
+         "add_rmsnorm"))
+    return -1;
+  for (int l = 0; l < m->n_layers; ++l) {
+    uint16_t* kc = static_cast<uint16_t*>(c->k[l]);
+    uint16_t* vc = static_cast<uint16_t*>(c->v[l]);
+    if (gemv(m->layer_fmt, m->w_qkv[l], w.x, w.qkv, qkv_dim, m->hidden)) return -1;
+    if (ck(launch_pdl(kv_append_kernel, ew_grid((long long)M * m->kv_dim), s, true, (const float*)w.qkv, kc, vc, M,
+                      m->q_dim, m->kv_dim, c->length),
+           "kv_append"))
+      return -1;
+    // attention over the cache; its output goes to the Wo GEMV's input as bf16
+    if (launch_attention(w.qkv, qkv_dim, kc, vc, nullptr, w.x, M, c->length, n_q, n_kv, m->head_dim, mask, scale,
+                         aws, s, err))
       return -1;
     if (gemv(m->layer_fmt, m->w_o[l], w.x, w.y, m->hidden, m->q_dim)) return -1;
     if (ck(launch_pdl(add_rmsnorm_kernel, M, s, true, w.h, (const uint16_t*)nullptr, (const float*)w.y, w.x,

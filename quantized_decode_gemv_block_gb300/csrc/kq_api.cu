@@ -265,9 +265,60 @@ int kq_attention(const float* q, const void* k_cache, const void* v_cache, float
   const size_t need = kq::attention_workspace(M, L, n_q, n_kv, head_dim);
   if (!workspace || ws_bytes < need || !aligned(workspace, 256))
     return fail(KQ_ERR_WORKSPACE, "workspace must be >= " + std::to_string(need) + " bytes, 256-byte aligned");
-  if (kq::launch_attention(q, static_cast<const uint16_t*>(k_cache), static_cast<const uint16_t*>(v_cache), o, M, L,
-                           n_q, n_kv, head_dim, reinterpret_cast<const uint32_t*>(mask), scale, workspace,
+  if (kq::launch_attention(q, n_q * head_dim, static_cast<const uint16_t*>(k_cache),
+                           static_cast<const uint16_t*>(v_cache), o, nullptr, M, L, n_q, n_kv, head_dim,
+                           reinterpret_cast<const uint32_t*>(mask), scale, workspace,
                            static_cast<cudaStream_t>(stream), &err) != 0)
+    return fail(KQ_ERR_CUDA, err);
+  return ok();
+}
+
+static int decode_attn_check(const kq_decode_model* model, const kq_kv_cache* cache, int M, std::string* err) {
+  if (kq::decode_check(model, M, err) != 0) return -1;
+  if (!cache) { *err = "cache is NULL"; return -1; }
+  const int n_q = model->q_dim / model->head_dim, n_kv = model->kv_dim / model->head_dim;
+  if (attention_check(M, cache->length, n_q, n_kv, model->head_dim, err) != 0) return -1;
+  if ((long long)cache->length + M > cache->capacity) { *err = "cache capacity < length + M"; return -1; }
+  if (model->n_layers > 0 && (!cache->k || !cache->v)) { *err = "cache pointer arrays are NULL"; return -1; }
+  for (int l = 0; l < model->n_layers; ++l)
+    if (!cache->k[l] || !cache->v[l] || !aligned(cache->k[l], 16) || !aligned(cache->v[l], 16)) {
+      *err = "layer " + std::to_string(l) + ": NULL or misaligned cache";
+      return -1;
+    }
+  return 0;
+}
+
+size_t kq_decode_attn_workspace_size(const kq_decode_model* model, int M, int L) {
+  std::string err;
+  if (kq::decode_check(model, M, &err) != 0 || L < 0) return 0;
+  const int n_q = model->q_dim / model->head_dim, n_kv = model->kv_dim / model->head_dim;
+  if (attention_check(M, L, n_q, n_kv, model->head_dim, &err) != 0) return 0;
+  return kq::decode_attn_workspace_size(model, M, L);
+}
+
+int kq_decode_step_attn(const kq_decode_model* model, const kq_kv_cache* cache, const void* x, float* logits,
+                        int M, const unsigned int* mask, void* workspace, size_t ws_bytes, void* stream) {
+  std::string err;
+  if (decode_attn_check(model, cache, M, &err) != 0) return fail(KQ_ERR_ARG, err);
+  if (!fmt_known(model->layer_fmt) || !fmt_known(model->head_fmt))
+    return fail(KQ_ERR_UNSUPPORTED, "unknown weight format in the model");
+  if (!x || !logits) return fail(KQ_ERR_ARG, "x or logits is NULL");
+  if (!aligned(x, 16) || !aligned(logits, 4) || (mask && !aligned(mask, 4)))
+    return fail(KQ_ERR_ARG, "misaligned x, logits or mask");
+  const size_t need = kq::decode_attn_workspace_size(model, M, cache->length);
+  if (!workspace || ws_bytes < need || !aligned(workspace, 256))
+    return fail(KQ_ERR_WORKSPACE, "workspace must be >= " + std::to_string(need) + " bytes, 256-byte aligned");
+  for (int l = 0; l < model->n_layers; ++l) {
+    const void* ps[4] = {model->w_qkv[l], model->w_o[l], model->w_gate_up[l], model->w_down[l]};
+    for (const void* p : ps)
+      if (!p || !aligned(p, 16)) return fail(KQ_ERR_ARG, "layer " + std::to_string(l) + ": NULL or misaligned weights");
+  }
+  if (!aligned(model->w_head, 16)) return fail(KQ_ERR_ARG, "misaligned w_head");
+  const int sms = sm_count(&err);
+  if (sms < 0) return fail(KQ_ERR_CUDA, err);
+  if (kq::decode_step_attn(model, cache, static_cast<const uint16_t*>(x), logits, M,
+                           reinterpret_cast<const uint32_t*>(mask), workspace, sms, static_cast<cudaStream_t>(stream),
+                           &err) != 0)
     return fail(KQ_ERR_CUDA, err);
   return ok();
 }

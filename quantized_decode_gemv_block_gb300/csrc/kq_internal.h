@@ -60,13 +60,20 @@ unsigned int take_tc_errors();
 // Decode step (decode.cu).
 int decode_check(const kq_decode_model* m, int M, std::string* err);
 size_t decode_workspace_size(const kq_decode_model* m, int M);
+// The step with attention over a KV cache (decode.cu): the window's k, v are appended to
+// the cache at positions L..L+M-1 of every layer.
+size_t decode_attn_workspace_size(const kq_decode_model* m, int M, int L);
+int decode_step_attn(const kq_decode_model* m, const kq_kv_cache* c, const uint16_t* x, float* logits, int M,
+                     const uint32_t* mask, void* ws, int num_sms, cudaStream_t s, std::string* err);
 int decode_step(const kq_decode_model* m, const uint16_t* x, float* logits, int M, void* ws, int num_sms,
                 cudaStream_t s, std::string* err);
 
 // Decode attention of a verify window over a KV cache (attention.cu).
 size_t attention_workspace(int M, int L, int n_q, int n_kv, int hd);
-int launch_attention(const float* q, const uint16_t* k, const uint16_t* v, float* o, int M, int L, int n_q, int n_kv,
-                     int hd, const uint32_t* mask, float scale, void* ws, cudaStream_t s, std::string* err);
+// q rows q_stride elements apart; the output goes to o (fp32) and/or o16 (bf16), either may be null.
+int launch_attention(const float* q, int q_stride, const uint16_t* k, const uint16_t* v, float* o, uint16_t* o16,
+                     int M, int L, int n_q, int n_kv, int hd, const uint32_t* mask, float scale, void* ws,
+                     cudaStream_t s, std::string* err);
 
 // GPU quantizers (fp64 arithmetic).
 int launch_quantize(int fmt, const float* w, void* blocks, int N, int K, cudaStream_t stream,

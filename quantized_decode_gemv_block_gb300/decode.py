@@ -50,19 +50,27 @@ def weight_bytes(model: DecodeModel) -> int:
 class GraphStep:
     """One decode step for M tokens captured in a CUDA graph over fixed buffers."""
 
-    def __init__(self, model: DecodeModel, M: int, stream: torch.cuda.Stream | None = None):
-        self.model, self.M = model, M
+    def __init__(self, model: DecodeModel, M: int, stream: torch.cuda.Stream | None = None, cache=None):
+        """cache: a KVCache to run kq_decode_step_attn over (its length fixed at capture time)."""
+        self.model, self.M, self.cache = model, M, cache
         dev = model.head.device
         self.x = torch.zeros((M, model.hidden), dtype=torch.bfloat16, device=dev)
         self.logits = torch.empty((M, model.vocab), dtype=torch.float32, device=dev)
-        self.ws = torch.empty(model.workspace_size(M), dtype=torch.uint8, device=dev)
+        nbytes = model.attn_workspace_size(M, cache.length) if cache is not None else model.workspace_size(M)
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         self.stream = stream or torch.cuda.Stream(device=dev)
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.stream(self.stream):
-            model.step(self.x, self.logits, self.ws)  # first call outside capture (lazy set-up)
+            self._step()  # first call outside capture (lazy set-up)
             self.stream.synchronize()
             with torch.cuda.graph(self.graph, stream=self.stream):
-                model.step(self.x, self.logits, self.ws)
+                self._step()
+
+    def _step(self):
+        if self.cache is None:
+            self.model.step(self.x, self.logits, self.ws)
+        else:
+            self.model.step_attn(self.x, self.cache, logits=self.logits, workspace=self.ws)
 
     def replay(self):
         with torch.cuda.stream(self.stream):

@@ -94,3 +94,75 @@ def test_full_dense_28_layer_decode_step(built, orc, M):
     ref, xf = orc.decode_step(od, hl, head, x, return_head_input=True)
     check_logits(orc, od, head, logits, ref, xf)
     assert kq.device_errors() == 0
+
+
+# ---- the step with attention over a KV cache (kq_decode_step_attn) ----
+
+def make_cache(d, L, M, seed):
+    """Random bf16 context rows (host bits) and a device cache holding them (capacity L + M)."""
+    kh, vh = [], []
+    for l in range(d["n_layers"]):
+        kh.append(inputs.activations_bf16(L, d["kv_dim"], seed=seed, tensor_id=8000 + 2 * l) if L else
+                  np.zeros((0, d["kv_dim"]), np.uint16))
+        vh.append(inputs.activations_bf16(L, d["kv_dim"], seed=seed, tensor_id=8001 + 2 * l) if L else
+                  np.zeros((0, d["kv_dim"]), np.uint16))
+    cache = kq.KVCache(d["n_layers"], L + M, d["kv_dim"])
+    for l in range(d["n_layers"]):
+        if L:
+            cache.k[l][:L].copy_(torch.from_numpy(kh[l].view(np.int16)).cuda().view(torch.bfloat16))
+            cache.v[l][:L].copy_(torch.from_numpy(vh[l].view(np.int16)).cuda().view(torch.bfloat16))
+    cache.length = L
+    return cache, kh, vh
+
+
+def attn_scale(hd):
+    return float(np.float32(1.0) / np.sqrt(np.float32(hd)))  # as the kernels form it
+
+
+def test_tiny_decode_with_attention_matches_oracle_and_is_batch_invariant(built, orc):
+    model, hl, head, od = make(orc, TINY, seed=31)
+    M, L = 5, 37
+    cache, kh, vh = make_cache(TINY, L, M, seed=32)
+    x = inputs.activations_bf16(M, TINY["hidden"], seed=33)
+    xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+    sc = attn_scale(TINY["head_dim"])
+    full = model.step_attn(xd, cache).cpu().numpy()
+    ref, xf = orc.decode_step_attn(od, hl, head, kh, vh, L, x, sc, return_head_input=True)
+    check_logits(orc, od, head, full, ref, xf)
+    for m in (1, 2):  # the first tokens alone: the same bits
+        y = model.step_attn(xd[:m].contiguous(), cache).cpu().numpy()
+        assert np.array_equal(y.view(np.uint32), full[:m].view(np.uint32)), f"M={m}"
+    # a tree of guesses: token i sees window tokens 0 and i
+    mask = np.array([1 | (1 << i) for i in range(M)], np.uint32)
+    yt = model.step_attn(xd, cache, mask=torch.from_numpy(mask.view(np.int32)).cuda()).cpu().numpy()
+    ref_t, xf_t = orc.decode_step_attn(od, hl, head, kh, vh, L, x, sc, mask=mask, return_head_input=True)
+    check_logits(orc, od, head, yt, ref_t, xf_t)
+    assert kq.device_errors() == 0
+
+
+def test_decode_with_attention_and_no_context_is_the_stand_in_step(built, orc):
+    """L = 0 and each token seeing only itself: the same logits as kq_decode_step (both
+    paths round the same values the same way)."""
+    model, hl, head, od = make(orc, TINY, seed=34)
+    M = 3
+    cache, _, _ = make_cache(TINY, 0, M, seed=35)
+    x = inputs.activations_bf16(M, TINY["hidden"], seed=36)
+    xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+    mask = torch.from_numpy(np.array([1 << i for i in range(M)], np.uint32).view(np.int32)).cuda()
+    a = model.step_attn(xd, cache, mask=mask).cpu().numpy()
+    b = model.step(xd).cpu().numpy()
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_full_dense_28_layer_decode_with_attention(built, orc, M):
+    d = kqd.DENSE_28L
+    model, hl, head, od = make(orc, d, seed=0)
+    L = 200
+    cache, kh, vh = make_cache(d, L, M, seed=37)
+    x = inputs.activations_bf16(M, d["hidden"], seed=0, tensor_id=5001)
+    xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+    logits = model.step_attn(xd, cache).cpu().numpy()
+    ref, xf = orc.decode_step_attn(od, hl, head, kh, vh, L, x, attn_scale(d["head_dim"]), return_head_input=True)
+    check_logits(orc, od, head, logits, ref, xf)
+    assert kq.device_errors() == 0
