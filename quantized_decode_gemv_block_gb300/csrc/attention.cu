@@ -6,7 +6,7 @@
 // mask). Query head hq reads kv head hq / group. q (fp32) is rounded to bf16, K and V are
 // bf16, scores and sums are fp32.
 //
-// Work split (a function of L, never of M): the cached positions are cut into chunks of 64;
+// Work split (a function of L, never of M): the cached positions are cut into chunks of 128;
 // the window is one more chunk of its own. One CTA per (chunk, kv head) holds the chunk's
 // K and V rows and the Q rows of its head group in shared memory; row r = i*group + g is
 // query head kvh*group + g of token i, so a token's row sits in the same MMA slot whatever
@@ -25,7 +25,7 @@
 namespace kq {
 namespace {
 
-constexpr int kChunk = 64;
+constexpr int kChunk = 128;
 constexpr int kAttnThreads = 256;  // 8 warps x 16 query rows
 constexpr int kAttnMaxRows = 128;
 
@@ -62,7 +62,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 __device__ __forceinline__ float bf16_rn_f(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 
 template <int HD>
-__global__ void __launch_bounds__(kAttnThreads, 2) attn_chunk_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_chunk_kernel(const AttnParams p) {
   constexpr int LD = HD + 8;  // shared row stride (elements): 16-byte pad, conflict-free ldmatrix
   extern __shared__ __align__(16) uint16_t asmem[];
   uint16_t* Qs = asmem;                  // [128][LD]
@@ -120,15 +120,15 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_chunk_kernel(const AttnP
   const int r0 = 16 * warp;
 
   // S = Q K^T for this warp's 16 rows and the chunk's 64 positions
-  float s[8][4];
+  float s[kChunk / 8][4];
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+  for (int nt = 0; nt < kChunk / 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
   for (int kk = 0; kk < HD / 16; ++kk) {
     uint32_t a[4];
     ldsm_x4(a, Qs + (r0 + (lane & 15)) * LD + kk * 16 + (lane >> 4) * 8);
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+    for (int nt = 0; nt < kChunk / 8; ++nt) {
       uint32_t b0, b1;
       ldsm_x2(b0, b1, Ks + (nt * 8 + (lane & 7)) * LD + kk * 16 + ((lane >> 3) & 1) * 8);
       mma_bf16_16816(s[nt], a, b0, b1, s[nt]);
@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_chunk_kernel(const AttnP
   const uint32_t mb = win ? (p.mask ? __ldg(p.mask + min(ib, p.M - 1)) : (ib >= 31 ? 0xFFFFFFFFu : ((2u << ib) - 1u))) : 0u;
   float mxa = -INFINITY, mxb = -INFINITY;
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
+  for (int nt = 0; nt < kChunk / 8; ++nt)
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int col = nt * 8 + 2 * q4 + e;
@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_chunk_kernel(const AttnP
   const float ca = mxa == -INFINITY ? 0.f : mxa, cb = mxb == -INFINITY ? 0.f : mxb;
   float la = 0.f, lb = 0.f;
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
+  for (int nt = 0; nt < kChunk / 8; ++nt)
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       s[nt][e] = expf(s[nt][e] - ca);  // exp(-inf) = 0 for positions not seen
