@@ -165,21 +165,27 @@ __device__ __forceinline__ void load_x8f(const XT* x, long long off, float (&xv)
   }
 }
 
-template <int FMT, int MT, class XT>
+// KS warps share each row pair, each taking a contiguous 1/KS of the K units; their sums
+// meet in shared memory and are added in slice order (KS depends on N, K and the SM count).
+template <int FMT, int MT, class XT, int KS>
 __global__ void __launch_bounds__(kThreadsF) gemv_f32_kernel(const uint8_t* __restrict__ w,
                                                              const XT* __restrict__ x,
                                                              float* __restrict__ y, int M, int N,
                                                              int K, long long row_bytes) {
+  constexpr int kGroups = 8 / KS;  // row pairs per CTA
+  __shared__ float red[KS > 1 ? 8 * kRowsPerWarp * MT : 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gi = lane >> 2, q = lane & 3;
-  const int nbase = (blockIdx.x * 8 + warp) * kRowsPerWarp;
+  const int rg = warp / KS, ks = warp - rg * KS;
+  const int nbase = (blockIdx.x * kGroups + rg) * kRowsPerWarp;
   float acc[kRowsPerWarp][MT];
 #pragma unroll
   for (int i = 0; i < kRowsPerWarp; ++i)
 #pragma unroll
     for (int j = 0; j < MT; ++j) acc[i][j] = 0.f;
 
-  const int units = K / 256;
+  const int units_all = K / 256;
+  const int u0 = ks * units_all / KS, u1 = (ks + 1) * units_all / KS;
   if (FMT == FMT_Q6_K) {
     // Q6_K: the next unit's raw bytes are loaded (plain, schedulable loads) before the
     // current unit is decoded, so each warp keeps two units of loads in flight.
@@ -188,13 +194,16 @@ __global__ void __launch_bounds__(kThreadsF) gemv_f32_kernel(const uint8_t* __re
     const int b = 2 * gi + (q >> 1), s_off = 192 + (b & ~1);
     const int nsh = (kq >= 2) ? 4 : 0, hsh = 2 * kq;
     Q6Raw nxt[kRowsPerWarp];
+    if (u0 < u1) {
 #pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) q6_load_raw(nxt[i], w + min(nbase + i, N - 1) * row_bytes, ql_off, qh_off, s_off);
-    for (int u = 0; u < units; ++u) {
+      for (int i = 0; i < kRowsPerWarp; ++i)
+        q6_load_raw(nxt[i], w + min(nbase + i, N - 1) * row_bytes + (long long)u0 * 210, ql_off, qh_off, s_off);
+    }
+    for (int u = u0; u < u1; ++u) {
       Q6Raw cur[kRowsPerWarp];
 #pragma unroll
       for (int i = 0; i < kRowsPerWarp; ++i) cur[i] = nxt[i];
-      if (u + 1 < units) {
+      if (u + 1 < u1) {
 #pragma unroll
         for (int i = 0; i < kRowsPerWarp; ++i)
           q6_load_raw(nxt[i], w + min(nbase + i, N - 1) * row_bytes + (long long)(u + 1) * 210, ql_off, qh_off, s_off);
@@ -230,7 +239,7 @@ __global__ void __launch_bounds__(kThreadsF) gemv_f32_kernel(const uint8_t* __re
       }
     }
   } else {
-  for (int u = 0; u < units; ++u) {
+  for (int u = u0; u < u1; ++u) {
     float c[kRowsPerWarp][8], sc[kRowsPerWarp], off[kRowsPerWarp];
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
@@ -265,20 +274,66 @@ __global__ void __launch_bounds__(kThreadsF) gemv_f32_kernel(const uint8_t* __re
       float v = acc[i][j];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-      if (lane == 0 && j < M && nbase + i < N) y[(long long)j * N + nbase + i] = v;
+      if (KS == 1) {
+        if (lane == 0 && j < M && nbase + i < N) y[(long long)j * N + nbase + i] = v;
+      } else if (lane == 0) {
+        red[(warp * kRowsPerWarp + i) * MT + j] = v;
+      }
     }
   }
+  if (KS > 1) {
+    __syncthreads();
+    if (ks == 0 && lane < kRowsPerWarp * MT) {
+      const int i = lane / MT, j = lane - i * MT;
+      float v = red[(warp * kRowsPerWarp + i) * MT + j];
+#pragma unroll
+      for (int k2 = 1; k2 < KS; ++k2) v = __fadd_rn(v, red[((warp + k2) * kRowsPerWarp + i) * MT + j]);
+      if (j < M && nbase + i < N) y[(long long)j * N + nbase + i] = v;
+    }
+  }
+}
+
+template <int FMT, class XT, int KS>
+void launch_ks(const uint8_t* w, const XT* x, float* y, int M, int N, int K, long long row_bytes,
+               cudaStream_t s) {
+  const int rows = (8 / KS) * kRowsPerWarp;
+  const dim3 grid((N + rows - 1) / rows), block(kThreadsF);
+  if (M <= 1) gemv_f32_kernel<FMT, 1, XT, KS><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
+  else if (M <= 2) gemv_f32_kernel<FMT, 2, XT, KS><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
+  else if (M <= 4) gemv_f32_kernel<FMT, 4, XT, KS><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
+  else if (M <= 8) gemv_f32_kernel<FMT, 8, XT, KS><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
+  else gemv_f32_kernel<FMT, 16, XT, KS><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
+}
+
+// The K split: the smallest KS (1, 2, 4, 8) that gives at least eight CTAs per SM while every
+// slice keeps at least two units. A function of (N, K, SM count) only.
+int pick_ks(int N, int K) {
+  static int sms[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int n_sm = dev < 64 ? sms[dev] : 0;
+  if (n_sm == 0) {
+    cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (n_sm <= 0) n_sm = 1;
+    if (dev < 64) sms[dev] = n_sm;
+  }
+  const int units = K / 256;
+  int ks = 1;
+  while (ks < 8 && (long long)((N + (8 / ks) * kRowsPerWarp - 1) / ((8 / ks) * kRowsPerWarp)) < 8LL * n_sm &&
+         units / (2 * ks) >= 2)
+    ks *= 2;
+  return ks;
 }
 
 template <int FMT, class XT>
 int launch_fmt(const uint8_t* w, const XT* x, float* y, int M, int N, int K,
                long long row_bytes, cudaStream_t s) {
-  const dim3 grid((N + kRowsPerCtaF - 1) / kRowsPerCtaF), block(kThreadsF);
-  if (M <= 1) gemv_f32_kernel<FMT, 1, XT><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
-  else if (M <= 2) gemv_f32_kernel<FMT, 2, XT><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
-  else if (M <= 4) gemv_f32_kernel<FMT, 4, XT><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
-  else if (M <= 8) gemv_f32_kernel<FMT, 8, XT><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
-  else gemv_f32_kernel<FMT, 16, XT><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
+  switch (pick_ks(N, K)) {
+    case 1: launch_ks<FMT, XT, 1>(w, x, y, M, N, K, row_bytes, s); break;
+    case 2: launch_ks<FMT, XT, 2>(w, x, y, M, N, K, row_bytes, s); break;
+    case 4: launch_ks<FMT, XT, 4>(w, x, y, M, N, K, row_bytes, s); break;
+    default: launch_ks<FMT, XT, 8>(w, x, y, M, N, K, row_bytes, s); break;
+  }
   return 0;
 }
 
