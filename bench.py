@@ -113,6 +113,10 @@ KERNEL_SOURCES = ["quantized_decode_gemv_block_gb300/csrc/gemv_mma.cu",
                   "quantized_decode_gemv_block_gb300/csrc/kq_device.cuh"]
 
 
+F32_SOURCES = ["quantized_decode_gemv_block_gb300/csrc/gemv_f32.cu",
+               "quantized_decode_gemv_block_gb300/csrc/kq_device.cuh"]
+ATTN_SOURCES = ["quantized_decode_gemv_block_gb300/csrc/attention.cu",
+                "quantized_decode_gemv_block_gb300/csrc/kq_device.cuh"]
 PREFILL_SOURCES = ["quantized_decode_gemv_block_gb300/csrc/gemm_tc.cu",
                    "quantized_decode_gemv_block_gb300/csrc/kq_device.cuh"]
 
@@ -581,7 +585,9 @@ def run_attention(args, spec):
                        "l2": f"rotating KV caches: {copies} x {step_bytes} B >= 4x L2 ({l2} B)",
                        "parallelism": "replicas" if world > 1 else "single gpu"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None, "peak_source": f"{peak_kind} hbm_gbs",
+                         "frac": achieved / peak,
+                         "traffic": profile_traffic("attention_decode.md", ATTN_SOURCES) if M == 8 else None,
+                         "peak_source": f"{peak_kind} hbm_gbs",
                          "kernel": "attn_chunk_kernel + attn_combine_kernel (one kq_attention call)",
                          "launch_us": ms_step * 1e3},
             "cpu_baseline": cpu,
@@ -956,7 +962,10 @@ def main():
     launch_ms = ms_step / len(spec["mats"])
     achieved = step_bytes / len(spec["mats"]) / (launch_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
-    traffic = profile_traffic(f"gemv_tma_{args.workload}.md")
+    if spec["fmt"] == "q6_k" or spec["dtype"] == "f32":
+        traffic = profile_traffic(f"gemv_f32_{args.workload}.md", F32_SOURCES)
+    else:
+        traffic = profile_traffic(f"gemv_tma_{args.workload}.md")
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
