@@ -66,8 +66,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_chunk_kernel(const AttnP
   constexpr int LD = HD + 8;  // shared row stride (elements): 16-byte pad, conflict-free ldmatrix
   extern __shared__ __align__(16) uint16_t asmem[];
   uint16_t* Qs = asmem;                  // [128][LD]
-  uint16_t* Ks = Qs + kAttnMaxRows * LD;  // [64][LD]
-  uint16_t* Vs = Ks + kChunk * LD;        // [64][LD]
+  uint16_t* Ks = Qs + kAttnMaxRows * LD;  // [kChunk][LD]
+  uint16_t* Vs = Ks + kChunk * LD;        // [kChunk][LD]
   const int c = blockIdx.x, kvh = blockIdx.y;
   const int nc = p.nchunks - 1;           // cached chunks; chunk nc is the window
   const bool win = c == nc;
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_chunk_kernel(const AttnP
   if (16 * warp >= p.R) return;  // no rows for this warp (uniform)
   const int r0 = 16 * warp;
 
-  // S = Q K^T for this warp's 16 rows and the chunk's 64 positions
+  // S = Q K^T for this warp's 16 rows and the chunk's kChunk positions
   float s[kChunk / 8][4];
 #pragma unroll
   for (int nt = 0; nt < kChunk / 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
