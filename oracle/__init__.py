@@ -6,7 +6,7 @@ code with it. The arithmetic lives in ``oracle.cpp`` (plain C++, fp64, built
 without contraction); this module only marshals numpy arrays through ctypes.
 
 Each function states what it computes; the definitions and their sources are in
-the headers of ``oracle.cpp``, ``decode.cpp`` and ``attention.cpp``.
+the headers of ``oracle.cpp``, ``decode.cpp``, ``attention.cpp`` and ``shortlist.cpp``.
 """
 from __future__ import annotations
 
@@ -19,7 +19,7 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SO = os.path.join(_HERE, "liboracle.so")
 _SOURCES = [os.path.join(_HERE, "oracle.cpp"), os.path.join(_HERE, "decode.cpp"),
-            os.path.join(_HERE, "attention.cpp")]
+            os.path.join(_HERE, "attention.cpp"), os.path.join(_HERE, "shortlist.cpp")]
 
 Q8_0, Q4_K, AFFINE4, Q5_K, Q6_K = 1, 2, 3, 4, 5
 F32, BF16 = 1, 2
@@ -67,6 +67,8 @@ def lib():
         L.orc_decode_step_attn.argtypes = [I, I, I, I, I, I, I, I, I, ctypes.c_double, P, P, P, P, P, P, P, I,
                                            P, ctypes.c_float, P, I64, P, I, P]
         L.orc_decode_step_attn.restype = I
+        L.orc_shortlist_build.argtypes = [P, I64, I64, P, P, I]
+        L.orc_shortlist_build.restype = I
         _lib = L
     return _lib
 
@@ -258,3 +260,16 @@ def decode_step_attn(dims: dict, layers: list, head: np.ndarray, k_cache: list, 
     if rc != 0:
         raise ValueError("orc_decode_step_attn failed")
     return (out, xf) if return_head_input else out
+
+
+def shortlist_build(w_q8: np.ndarray, N: int, K: int, nthreads: int = 0):
+    """Small copy (affine4 bytes, N x K/32 x 20) and per-row score bounds B_n (fp32) of a Q8_0
+    head (definition in shortlist.cpp). A row can win only if approx_n + B_n ||x|| >=
+    max_m (approx_m - B_m ||x||), approx being the small copy's product."""
+    w = np.ascontiguousarray(w_q8, dtype=np.uint8)
+    small = np.empty(N * (K // 32) * 20, dtype=np.uint8)
+    bound = np.empty(N, dtype=np.float32)
+    nt = nthreads or os.cpu_count() or 1
+    if lib().orc_shortlist_build(_ptr(w), N, K, _ptr(small), _ptr(bound), nt) != 0:
+        raise ValueError("orc_shortlist_build: bad arguments")
+    return small, bound

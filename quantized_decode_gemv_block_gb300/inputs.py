@@ -77,3 +77,25 @@ def activations_cuda(M: int, K: int, seed: int = 0, tensor_id: int = 1000, dtype
     g = torch.Generator(device=device)
     g.manual_seed((int(seed) << 20) ^ int(tensor_id))
     return torch.randn((M, K), generator=g, device=device, dtype=torch.float32).to(dtype)
+
+
+def planted_activations_f32(targets: np.ndarray, gain: float, seed: int = 0, tensor_id: int = 1000) -> np.ndarray:
+    """M x K fp32 hidden states that favour one output row each, the way a trained model's
+    last hidden state favours its next token: x_j = z_j + gain * ||z_j|| * t_j / ||t_j||, with
+    z_j ~ N(0, 1) and t_j row j of `targets` (the fp32 weights of the row to favour)."""
+    t = np.ascontiguousarray(targets, dtype=np.float32)
+    z = activations_f32(t.shape[0], t.shape[1], seed, tensor_id).astype(np.float64)
+    td = t.astype(np.float64)
+    zn = np.linalg.norm(z, axis=1, keepdims=True)
+    tn = np.linalg.norm(td, axis=1, keepdims=True)
+    return (z + gain * zn * td / np.where(tn > 0, tn, 1.0)).astype(np.float32)
+
+
+def planted_activations_cuda(targets: torch.Tensor, gain: float, seed: int = 0, tensor_id: int = 1000,
+                             dtype=torch.bfloat16) -> torch.Tensor:
+    """The same recipe on the GPU (torch's generator for z), for full-size workloads."""
+    t = targets.to(torch.float32)
+    z = activations_cuda(t.shape[0], t.shape[1], seed, tensor_id, dtype=torch.float32, device=t.device)
+    zn = z.norm(dim=1, keepdim=True)
+    tn = t.norm(dim=1, keepdim=True).clamp_min(1e-30)
+    return (z + gain * zn * t / tn).to(dtype)
