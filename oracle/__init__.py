@@ -263,11 +263,11 @@ def decode_step_attn(dims: dict, layers: list, head: np.ndarray, k_cache: list, 
 
 
 def shortlist_build(w_q8: np.ndarray, N: int, K: int, nthreads: int = 0):
-    """Small copy (affine4 bytes, N x K/32 x 20) and per-row score bounds B_n (fp32) of a Q8_0
+    """Small copy (Q4_K bytes, N x K/256 x 144) and per-row score bounds B_n (fp32) of a Q8_0
     head (definition in shortlist.cpp). A row can win only if approx_n + B_n ||x|| >=
     max_m (approx_m - B_m ||x||), approx being the small copy's product."""
     w = np.ascontiguousarray(w_q8, dtype=np.uint8)
-    small = np.empty(N * (K // 32) * 20, dtype=np.uint8)
+    small = np.empty(N * (K // 256) * 144, dtype=np.uint8)
     bound = np.empty(N, dtype=np.float32)
     nt = nthreads or os.cpu_count() or 1
     if lib().orc_shortlist_build(_ptr(w), N, K, _ptr(small), _ptr(bound), nt) != 0:
