@@ -11,6 +11,10 @@ Prints ONE JSON line (rank 0). Workloads (synthetic data, seeded):
   ffn_q5k  the ffn pair with Q5_K blocks (176 bytes per 256 weights).
   ffn_q6k  the ffn pair with Q6_K blocks (210 bytes per 256 weights; CUDA-core kernel).
   head     Q8_0 lm-head GEMV, W 151936x2048, M bf16 rows (--m).
+  shortlist  greedy next token over the same head (kq_head_argmax): scores from the small
+           Q4_K copy, exact Q8_0 scores only for rows that can still win; hidden states
+           that favour one row each, as a trained model's do. Reported as the head's Q8_0
+           bytes per call / call time (effective: the shortlist reads the small copy).
   decode   the dense 28-layer decode step (kq_decode_step) in a CUDA graph, M rows (--m).
   prefill  Q4_K prefill GEMM on the tensor cores, W 9728x2560, X 2048x2560 bf16; reported in
            TFLOP/s (2*M*N*K per step) against the measured dense bf16/fp16 peak.
@@ -71,6 +75,11 @@ def workload_spec(name: str, m: int):
     if name == "head":
         return dict(name=f"q8_0 lm head 151936x2048, M={m} bf16", fmt="q8_0", mats=[(151936, 2048)],
                     M=m, dtype="bf16")
+    if name == "shortlist":
+        mm = min(m, 16)
+        return dict(name=f"greedy token over a q8_0 lm head 151936x2048 with the shortlist, M={mm} bf16 hidden "
+                         f"states favouring one row each (gain 0.5)", fmt="q8_0", mats=[(151936, 2048)], M=mm,
+                    dtype="bf16", shortlist=True, gain=0.5)
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -603,6 +612,179 @@ def run_attention(args, spec):
         dist.destroy_process_group()
 
 
+SHORTLIST_METRIC = ("greedy next token over a Q8_0 output head: effective head GB/s (Q8_0 head bytes per call / "
+                    "call time)")
+
+
+def run_shortlist(args, spec):
+    """kq_head_argmax with the shortlist per step; two copies of the head (each 526 MB with its
+    small copy, > 4x L2 together) alternate, so every call streams its small copy from HBM."""
+    import torch
+    import torch.distributed as dist
+
+    import quantized_decode_gemv_block_gb300 as kq
+    from quantized_decode_gemv_block_gb300 import build, inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    if rank == 0 or not os.path.exists(kq.LIB_PATH):
+        build.build()
+    if world > 1:
+        dist.barrier()
+    kq.load_library()
+    dev = torch.device("cuda", local)
+    M = spec["M"]
+    N, K = spec["mats"][0]
+    copies = 2
+    heads, sls, xs, targets = [], [], [], []
+    for c in range(copies):
+        wf = inputs.weights_cuda(N, K, seed=rank, tensor_id=901 + c, device=dev)
+        heads.append(kq.quantize("q8_0", wf))
+        tg = torch.tensor(np.random.default_rng(100 * rank + c).choice(N, M, replace=False), device=dev)
+        xs.append(inputs.planted_activations_cuda(wf[tg], spec["gain"], seed=rank, tensor_id=1000 + c))
+        targets.append(tg)
+        del wf
+        sls.append(kq.shortlist_build(heads[c], N, K))
+    torch.cuda.synchronize()
+    head_bytes = heads[0].numel()
+    small_bytes = N * (K // 256) * 144
+    ws = torch.empty(kq.lib().kq_head_argmax_workspace_size(M, N), dtype=torch.uint8, device=dev)
+    tok = torch.empty(M, dtype=torch.int32, device=dev)
+    sc = torch.empty(M, dtype=torch.float32, device=dev)
+    rs = torch.empty(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(s, xx=None):
+        c = s % copies
+        kq.head_argmax(heads[c], sls[c], xs[c] if xx is None else xx[c], N, K, workspace=ws, token=tok, score=sc,
+                       rows_scored=rs)
+
+    def small_only(s):  # the dominant kernel alone, same launch: the small copy's GEMV
+        c = s % copies
+        kq.gemv("q4_k", sls[c][:small_bytes], xs[c], N, K, y=ws[:M * N * 4].view(torch.float32).view(M, N))
+
+    def plain(s):  # the head's plain GEMV (every Q8_0 byte), for context
+        c = s % copies
+        kq.gemv("q8_0", heads[c], xs[c], N, K, y=ws[:M * N * 4].view(torch.float32).view(M, N))
+
+    def all_rows(s):  # every row scored exactly (the shortlist off)
+        c = s % copies
+        kq.head_argmax(heads[c], None, xs[c], N, K, all_rows=True, workspace=ws, token=tok, score=sc,
+                       rows_scored=rs)
+
+    def capture(n, body):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            body(0)
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for s in range(n):
+                    body(s)
+        return g
+
+    def timed(g, n):
+        with torch.cuda.stream(stream):
+            g.replay()
+            stream.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    # correctness of what is timed: the planted rows win, the same as with every row scored
+    for c in range(copies):
+        t1, s1, r1 = kq.head_argmax(heads[c], sls[c], xs[c], N, K)
+        t0, s0, _ = kq.head_argmax(heads[c], None, xs[c], N, K, all_rows=True)
+        torch.cuda.synchronize()
+        assert torch.equal(t1, targets[c].to(torch.int32)) and torch.equal(t1, t0) and torch.equal(s1, s0)
+    rows_scored = int(r1.item())
+    K_ = args.steps
+    g_warm, g_main = capture(args.warmup, step), capture(K_, step)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        g_warm.replay()
+    stream.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record()
+        g_main.replay()
+        t1.record()
+    torch.cuda.synchronize()
+    ms_step = t0.elapsed_time(t1) / K_
+    clocks = sampler.stop()
+    n_aux = min(K_, 50)
+    small_ms = timed(capture(n_aux, small_only), n_aux)
+    plain_ms = timed(capture(n_aux, plain), n_aux)
+    all_ms = timed(capture(min(n_aux, 10), all_rows), min(n_aux, 10))
+    # e2e: the hidden states in from pinned host memory, tokens and scores out, every step
+    xh = [x.cpu().pin_memory() for x in xs]
+    xd = [torch.empty_like(x) for x in xs]
+    th = torch.empty(M, dtype=torch.int32).pin_memory()
+    sh = torch.empty(M, dtype=torch.float32).pin_memory()
+
+    def e2e_step(s):
+        c = s % copies
+        xd[c].copy_(xh[c], non_blocking=True)
+        step(s, xd)
+        th.copy_(tok, non_blocking=True)
+        sh.copy_(sc, non_blocking=True)
+
+    n_e2e = min(K_, 100)
+    e2e_ms = timed(capture(n_e2e, e2e_step), n_e2e)
+    ms_step, e2e_ms = max_over_ranks([ms_step, e2e_ms], dev, world)
+    peak, peak_kind = measured_peaks()
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, passes, el = cpu_oracle_gbps(dict(spec, mats=[(16384, K)]), args.cpu_budget)
+        cpu = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"exact fp64 scores of 16384 of the head's {N} rows for M={M} ({passes} passes in "
+                         f"{el:.1f} s; the argmax's definition), OpenMP over rows"}
+    if rank == 0:
+        value = replica_rate(world, head_bytes, ms_step) / 1e9
+        achieved = small_bytes / (small_ms * 1e-3) / 1e9
+        line = {
+            "metric": SHORTLIST_METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K_,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "q4_k / q8_0 x bf16 -> fp32", "data": "synthetic",
+            "config": {"workload": spec["name"], "M": M, "head_bytes": head_bytes, "small_copy_bytes": small_bytes,
+                       "rows_scored_exactly": rows_scored,
+                       "l2": f"two heads alternate: 2 x {head_bytes + small_bytes} B >= 4x L2",
+                       "small_copy_gemv_us": small_ms * 1e3, "plain_q8_0_gemv_us": plain_ms * 1e3,
+                       "all_rows_exact_us": all_ms * 1e3,
+                       "parallelism": "replicas" if world > 1 else "single gpu"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak,
+                         "traffic": profile_traffic("shortlist_head.md") if M == 1 else None,
+                         "peak_source": f"{peak_kind} hbm_gbs",
+                         "kernel": "gemv_tma_kernel<FmtQ4KH> over the small Q4_K copy (its own graph, same launch)",
+                         "launch_us": small_ms * 1e3},
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * head_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": xh[0].numel() * 2, "d2h_bytes_per_step": M * 8,
+                    "note": "per step: hidden states in from pinned host memory, kq_head_argmax, tokens and "
+                            "scores out; graph-replayed"},
+            "gpu_launches": 3 * K_,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 def run_decode(args, spec):
     """The dense 28-layer decode step (kq_decode_step) as one CUDA graph, replayed K times."""
     import torch
@@ -756,7 +938,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="kq", choices=["kq", "reference"])
     ap.add_argument("--workload", default="ffn", choices=["ffn", "ffn_q5k", "ffn_q6k", "verify", "q8_0", "head", "decode",
-                                                        "prefill", "attention"])
+                                                        "prefill", "attention", "shortlist"])
     ap.add_argument("--m", type=int, default=16)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -770,6 +952,8 @@ def main():
             spec = dict(spec, fmt="q4_k", mats=[(3072, 2048), (2048, 2048), (12288, 2048), (2048, 6144)])
         if spec.get("prefill"):
             spec = dict(spec, M=16)  # bounded sample: 16 of the 2048 tokens per step
+        if spec.get("shortlist"):
+            spec = dict(spec, mats=[(16384, 2048)])  # bounded sample: 16384 of the 151936 rows per step
         run_reference(args, spec)
         return
     if spec.get("decode"):
@@ -780,6 +964,9 @@ def main():
         return
     if spec.get("prefill"):
         run_prefill(args, spec)
+        return
+    if spec.get("shortlist"):
+        run_shortlist(args, spec)
         return
 
     import torch

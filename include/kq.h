@@ -186,6 +186,50 @@ int kq_attention(const float* q, const void* k_cache, const void* v_cache, float
                  int n_kv, int head_dim, const unsigned int* mask, float scale, void* workspace, size_t ws_bytes,
                  void* stream);
 
+/* ---- Shortlist output head: the greedy next token ----
+ * Kinetic README, "What makes it fast" (choosing the next token): the output layer, up to a
+ * quarter of a million rows, is read for every token; each row's score is first bounded
+ * from a small copy, and exact scores are computed only for the rows that can still win.
+ *
+ * kq_shortlist_build makes the small copy of a Q8_0 head W (N x K, rows of blocks as for
+ * kq_gemv) once, at load time, into one caller-owned buffer of kq_shortlist_bytes(N, K)
+ * bytes (256-byte aligned):
+ *   bytes [0, S)        N rows of K/256 Q4_K blocks (144 bytes): each 256-weight super-block
+ *                       of deq(W) through the Q4_K quantizer of kq_quantize; S is that size
+ *                       rounded up to a multiple of 256;
+ *   bytes [S, S + 4N)   B_n (fp32): ||w_n - w'_n||_2 + K 2^-22 (||w_n||_2 + A_n), rounded up,
+ *                       with A_n = sqrt(32 sum_g (15 d sc_g + dmin m_g)^2) over the row's
+ *                       32-weight sub-blocks g.
+ * For any x, |x.w_n - x.w'_n| <= B_n ||x||_2 (Cauchy-Schwarz), and the second term covers
+ * the fp32 rounding of both the exact and the small-copy products.
+ *
+ * kq_head_argmax gives, for each of M (1..16) hidden states x_j, the row with the largest
+ * exact score (ties: the lowest row) and that score. A row is scored exactly only if its
+ * small-copy score plus B_n ||x_j|| reaches the largest small-copy score minus bound of
+ * some token (bounds evaluated with directed rounding), so the row that wins is never
+ * skipped. The exact score of row n is an fp32 sum in a fixed order (one warp per row: lane
+ * l takes blocks l, l+32, ..., each a sequential FMA chain promoted by d; a fixed butterfly
+ * across lanes). It does not depend on M, on the shortlist or on the other rows scored, so
+ * the result equals the result with KQ_HEAD_ALL_ROWS (every row scored exactly, no
+ * small-copy pass; shortlist may then be NULL). It can differ from the argmax of kq_gemv's
+ * output only between rows whose scores lie within fp32 rounding of each other.
+ *   w_q8        the Q8_0 head (device, 16-byte aligned); N >= 1; K a multiple of 256
+ *   shortlist   from kq_shortlist_build for this head
+ *   x           M x K, fp32 or bf16 (x_dtype), device, 16-byte aligned
+ *   token       M int32 (device): the winning row, or -1 if no score is comparable (NaN)
+ *   score       M fp32 (device): its exact score
+ *   rows_scored NULL or one uint32 (device): the number of rows scored exactly
+ *   workspace   kq_head_argmax_workspace_size(M, N) bytes, 256-byte aligned
+ * Three launches on `stream` (the small-copy GEMV, the bounds, the exact scores), no
+ * synchronisation, no allocation. Errors: KQ_ERR_ARG, KQ_ERR_WORKSPACE, KQ_ERR_CUDA. */
+enum { KQ_HEAD_ALL_ROWS = 1u };
+size_t kq_shortlist_bytes(int N, int K);
+int kq_shortlist_build(const void* w_q8, int N, int K, void* shortlist, size_t bytes, void* stream);
+size_t kq_head_argmax_workspace_size(int M, int N);
+int kq_head_argmax(const void* w_q8, const void* shortlist, int x_dtype, const void* x, int M, int N, int K,
+                   int* token, float* score, unsigned int* rows_scored, void* workspace, size_t ws_bytes,
+                   unsigned flags, void* stream);
+
 /* ---- Decode step (composition of the GEMVs; Kinetic README, "What makes it fast": a
  * decode step is hundreds of small kernels replayed with one launch per token, and a
  * dense model reads all of its weights once per token). ----

@@ -85,6 +85,14 @@ def load_library(path: str = LIB_PATH):
     L.kq_decode_step.restype = I
     L.kq_decode_step_static.argtypes = [ctypes.POINTER(DecodeModelC), P, P, I, P]
     L.kq_decode_step_static.restype = I
+    L.kq_shortlist_bytes.argtypes = [I, I]
+    L.kq_shortlist_bytes.restype = SZ
+    L.kq_shortlist_build.argtypes = [P, I, I, P, SZ, P]
+    L.kq_shortlist_build.restype = I
+    L.kq_head_argmax_workspace_size.argtypes = [I, I]
+    L.kq_head_argmax_workspace_size.restype = SZ
+    L.kq_head_argmax.argtypes = [P, P, I, P, I, I, I, P, P, P, P, SZ, ctypes.c_uint, P]
+    L.kq_head_argmax.restype = I
     _lib = L
     return L
 
@@ -190,6 +198,51 @@ def attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, L: 
                               n_kv, head_dim, mask.data_ptr() if mask is not None else None, scale,
                               workspace.data_ptr(), workspace.numel(), _stream(stream)))
     return out
+
+
+KQ_HEAD_ALL_ROWS = 1
+
+
+def shortlist_build(w_q8: torch.Tensor, N: int, K: int, out: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """The shortlist buffer of a Q8_0 head (kq_shortlist_build): the small Q4_K copy, then
+    N fp32 score bounds (see shortlist_parts)."""
+    need = lib().kq_shortlist_bytes(N, K)
+    if need == 0:
+        raise KQError(KQ_ERR_ARG, "bad head shape for the shortlist")
+    if out is None:
+        out = torch.empty(need, dtype=torch.uint8, device=w_q8.device)
+    _check(lib().kq_shortlist_build(w_q8.data_ptr(), N, K, out.data_ptr(), out.numel(), _stream(stream)))
+    return out
+
+
+def shortlist_parts(buf: torch.Tensor, N: int, K: int):
+    """(small copy bytes N x K/256*144, bounds N fp32): views into a shortlist buffer."""
+    small = N * (K // 256) * 144
+    s = (small + 255) // 256 * 256
+    return buf[:small].view(N, K // 256 * 144), buf[s:s + 4 * N].view(torch.float32)
+
+
+def head_argmax(w_q8: torch.Tensor, shortlist: torch.Tensor | None, x: torch.Tensor, N: int, K: int,
+                all_rows: bool = False, workspace: torch.Tensor | None = None, token: torch.Tensor | None = None,
+                score: torch.Tensor | None = None, rows_scored: torch.Tensor | None = None, stream=None):
+    """Greedy next token of each hidden-state row of x over a Q8_0 head (kq_head_argmax).
+    Returns (token int32 [M], score fp32 [M], rows_scored int32 [1]) device tensors."""
+    M = x.shape[0]
+    dev = x.device
+    if workspace is None:
+        workspace = torch.empty(lib().kq_head_argmax_workspace_size(M, N), dtype=torch.uint8, device=dev)
+    if token is None:
+        token = torch.empty(M, dtype=torch.int32, device=dev)
+    if score is None:
+        score = torch.empty(M, dtype=torch.float32, device=dev)
+    if rows_scored is None:
+        rows_scored = torch.empty(1, dtype=torch.int32, device=dev)
+    _check(lib().kq_head_argmax(w_q8.data_ptr(), shortlist.data_ptr() if shortlist is not None else None,
+                                _x_dtype(x), x.data_ptr(), M, N, K, token.data_ptr(), score.data_ptr(),
+                                rows_scored.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                                KQ_HEAD_ALL_ROWS if all_rows else 0, _stream(stream)))
+    return token, score, rows_scored
 
 
 def device_errors() -> int:

@@ -337,6 +337,65 @@ int kq_quantize(int fmt, const float* w, void* w_blocks, int N, int K, void* str
   return ok();
 }
 
+// ---- Shortlist output head ----
+static bool head_shape_ok(int N, int K) { return N >= 1 && K >= 256 && K % 256 == 0; }
+
+size_t kq_shortlist_bytes(int N, int K) {
+  if (!head_shape_ok(N, K)) return 0;
+  return kq::shortlist_bytes(N, K);
+}
+
+int kq_shortlist_build(const void* w_q8, int N, int K, void* shortlist, size_t bytes, void* stream) {
+  if (!head_shape_ok(N, K)) return fail(KQ_ERR_ARG, "N must be >= 1 and K a positive multiple of 256");
+  if (!w_q8 || !shortlist) return fail(KQ_ERR_ARG, "w_q8 or shortlist is NULL");
+  if (!aligned(w_q8, 16) || !aligned(shortlist, 256))
+    return fail(KQ_ERR_ARG, "w_q8 must be 16-byte aligned and shortlist 256-byte aligned");
+  const size_t need = kq::shortlist_bytes(N, K);
+  if (bytes < need) return fail(KQ_ERR_ARG, "shortlist buffer must be >= " + std::to_string(need) + " bytes");
+  float* bound = reinterpret_cast<float*>(static_cast<uint8_t*>(shortlist) + kq::shortlist_small_bytes(N, K));
+  std::string err;
+  if (kq::launch_shortlist_build(w_q8, shortlist, bound, N, K, static_cast<cudaStream_t>(stream), &err) != 0)
+    return fail(KQ_ERR_CUDA, err);
+  return ok();
+}
+
+size_t kq_head_argmax_workspace_size(int M, int N) {
+  if (M < 1 || M > 16 || N < 1) return 0;
+  return kq::head_argmax_workspace(M, N);
+}
+
+int kq_head_argmax(const void* w_q8, const void* shortlist, int x_dtype, const void* x, int M, int N, int K,
+                   int* token, float* score, unsigned int* rows_scored, void* workspace, size_t ws_bytes,
+                   unsigned flags, void* stream) {
+  if (flags & ~static_cast<unsigned>(KQ_HEAD_ALL_ROWS))
+    return fail(KQ_ERR_ARG, "unknown flag bits " + std::to_string(flags));
+  const bool all = (flags & KQ_HEAD_ALL_ROWS) != 0;
+  if (M < 1 || M > 16) return fail(KQ_ERR_ARG, "M must be in 1..16, got " + std::to_string(M));
+  if (!head_shape_ok(N, K)) return fail(KQ_ERR_ARG, "N must be >= 1 and K a positive multiple of 256");
+  if (x_dtype != KQ_F32 && x_dtype != KQ_BF16)
+    return fail(KQ_ERR_UNSUPPORTED, "unknown activation dtype " + std::to_string(x_dtype));
+  if (!w_q8 || !x || !token || !score || (!all && !shortlist))
+    return fail(KQ_ERR_ARG, "w_q8, shortlist, x, token or score is NULL");
+  if (!aligned(w_q8, 16) || !aligned(x, 16) || (!all && !aligned(shortlist, 256)) || !aligned(token, 4) ||
+      !aligned(score, 4) || (rows_scored && !aligned(rows_scored, 4)))
+    return fail(KQ_ERR_ARG, "misaligned w_q8, shortlist, x, token, score or rows_scored");
+  const size_t need = kq::head_argmax_workspace(M, N);
+  if (!workspace || ws_bytes < need || !aligned(workspace, 256))
+    return fail(KQ_ERR_WORKSPACE, "workspace must be >= " + std::to_string(need) + " bytes, 256-byte aligned");
+  std::string err;
+  const int sms = sm_count(&err);
+  if (sms < 0) return fail(KQ_ERR_CUDA, err);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!all) {  // the small copy's scores into the workspace's first M*N floats
+    const int rc = gemv_impl(KQ_Q4_K, shortlist, x_dtype, x, static_cast<float*>(workspace), M, N, K, s);
+    if (rc != KQ_OK) return rc;
+  }
+  if (kq::launch_head_select(w_q8, shortlist, x_dtype == KQ_BF16, x, M, N, K, token, score, rows_scored, workspace,
+                             all, sms, s, &err) != 0)
+    return fail(KQ_ERR_CUDA, err);
+  return ok();
+}
+
 // ---- Decode step with library-owned scratch (kq_decode_step_static) ----
 // The scratch lives in one file-scope device array, so no call allocates. Host code may
 // not use the array's name as a device address (on the host it names a stand-in object):

@@ -75,6 +75,18 @@ int launch_attention(const float* q, int q_stride, const uint16_t* k, const uint
                      int M, int L, int n_q, int n_kv, int hd, const uint32_t* mask, float scale, void* ws,
                      cudaStream_t s, std::string* err);
 
+// Shortlist output head (shortlist.cu; the small copy's build is in quantize.cu).
+size_t shortlist_small_bytes(int N, int K);
+size_t shortlist_bytes(int N, int K);
+size_t head_argmax_workspace(int M, int N);
+int launch_shortlist_build(const void* wq, void* small, float* bound, int N, int K, cudaStream_t stream,
+                           std::string* err);
+// The bounds and exact passes; the small-copy GEMV into the workspace's first M*N floats is
+// launched before by the caller (unless all_rows).
+int launch_head_select(const void* wq, const void* shortlist, bool x_bf16, const void* x, int M, int N, int K,
+                       int* token, float* score, unsigned int* scored, void* ws, bool all_rows, int num_sms,
+                       cudaStream_t s, std::string* err);
+
 // GPU quantizers (fp64 arithmetic).
 int launch_quantize(int fmt, const float* w, void* blocks, int N, int K, cudaStream_t stream,
                     std::string* err);

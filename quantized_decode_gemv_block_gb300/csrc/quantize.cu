@@ -74,13 +74,12 @@ __global__ void quant_q8_0_kernel(const float* __restrict__ w, uint8_t* __restri
 
 // Q4_K (LEVELS = 15, 144-byte blocks) and Q5_K (LEVELS = 31, 176-byte blocks: the fifth
 // code bit of weight i goes to bit 2c + h of qh[l], c = i/64, h = (i%64 >= 32), l = i%32).
+// One super-block of 256 fp32 weights into dst; the chosen 6-bit scales and mins and the
+// fp16 d and dmin are also returned (sc, m, d16, dmin16).
 template <int LEVELS>
-__global__ void quant_qk_kernel(const float* __restrict__ w, uint8_t* __restrict__ out, long long nblk) {
-  constexpr int kBytes = LEVELS == 15 ? 144 : 176;
+__device__ void qk_block(const float* src, uint8_t* dst, int (&sc)[8], int (&m)[8], uint16_t& d16_out,
+                         uint16_t& dmin16_out) {
   constexpr int kCodes = LEVELS == 15 ? 16 : 48;  // offset of the low-nibble bytes
-  const long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-  if (b >= nblk) return;
-  const float* src = w + b * 256;
   double hi[8], mraw[8];
   double maxm = 0.0;
   for (int j = 0; j < 8; ++j) {
@@ -95,7 +94,6 @@ __global__ void quant_qk_kernel(const float* __restrict__ w, uint8_t* __restrict
     maxm = dmax_of(maxm, mraw[j]);
   }
   uint16_t dmin16 = 0;
-  int m[8];
   for (int j = 0; j < 8; ++j) m[j] = 0;
   if (maxm > 0.0) {
     dmin16 = d2h_up(__ddiv_rn(maxm, 63.0));
@@ -117,7 +115,6 @@ __global__ void quant_qk_kernel(const float* __restrict__ w, uint8_t* __restrict
     maxt = dmax_of(maxt, t[j]);
   }
   uint16_t d16 = 0;
-  int sc[8];
   for (int j = 0; j < 8; ++j) sc[j] = 0;
   if (maxt > 0.0) {
     d16 = d2h_up(__ddiv_rn(maxt, 63.0 * LEVELS));
@@ -133,7 +130,8 @@ __global__ void quant_qk_kernel(const float* __restrict__ w, uint8_t* __restrict
     }
   }
   const double d = h2d(d16);
-  uint8_t* dst = out + b * kBytes;
+  d16_out = d16;
+  dmin16_out = dmin16;
   put16(dst, d16);
   put16(dst + 2, dmin16);
   uint8_t scales[12];
@@ -171,6 +169,16 @@ __global__ void quant_qk_kernel(const float* __restrict__ w, uint8_t* __restrict
   }
   if (LEVELS == 31)
     for (int l = 0; l < 32; ++l) dst[16 + l] = qh[l];
+}
+
+template <int LEVELS>
+__global__ void quant_qk_kernel(const float* __restrict__ w, uint8_t* __restrict__ out, long long nblk) {
+  constexpr int kBytes = LEVELS == 15 ? 144 : 176;
+  const long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (b >= nblk) return;
+  int sc[8], m[8];
+  uint16_t d16, dmin16;
+  qk_block<LEVELS>(w + b * 256, out + b * kBytes, sc, m, d16, dmin16);
 }
 
 // Q6_K (GGUF): per 16-weight sub-block a = max |w|; d = smallest fp16 >= max(a)/(127*31);
@@ -225,11 +233,8 @@ __global__ void quant_q6_k_kernel(const float* __restrict__ w, uint8_t* __restri
   dst[209] = static_cast<uint8_t>(d16 >> 8);
 }
 
-__global__ void quant_affine4_kernel(const float* __restrict__ w, uint8_t* __restrict__ out,
-                                     long long nblk) {
-  const long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-  if (b >= nblk) return;
-  const float* src = w + b * 32;
+// One affine4 block of 32 fp32 weights: b, s by the covering rule, then the codes.
+__device__ void affine4_block(const float* src, uint8_t* dst) {
   double mn = static_cast<double>(src[0]), mx = mn;
   for (int i = 1; i < 32; ++i) {
     const double v = static_cast<double>(src[i]);
@@ -241,7 +246,6 @@ __global__ void quant_affine4_kernel(const float* __restrict__ w, uint8_t* __res
   const double span = __dadd_rn(mx, -bias);
   const uint16_t s16 = span > 0.0 ? d2h_up(__ddiv_rn(span, 15.0)) : 0;
   const double s = h2d(s16);
-  uint8_t* dst = out + b * 20;
   put16(dst, s16);
   put16(dst + 2, b16);
   for (int k = 0; k < 16; ++k) {
@@ -254,6 +258,72 @@ __global__ void quant_affine4_kernel(const float* __restrict__ w, uint8_t* __res
       qq[e] = qv;
     }
     dst[4 + k] = static_cast<uint8_t>(qq[0] | (qq[1] << 4));
+  }
+}
+
+__global__ void quant_affine4_kernel(const float* __restrict__ w, uint8_t* __restrict__ out,
+                                     long long nblk) {
+  const long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (b >= nblk) return;
+  affine4_block(w + b * 32, out + b * 20);
+}
+
+// Small copy of a Q8_0 output head for the shortlist (Kinetic README, "What makes it fast":
+// every row's score is bounded from a small copy): each 256-weight super-block of deq(W)
+// (d * q, exact in fp32) through the Q4_K quantizer, and per row the bound
+//   B_n = ||w_n - w'_n|| + K 2^-22 (||w_n|| + sqrt(32 sum_g (15 d sc_g + dmin m_g)^2)),
+// times (1 + 2^-32) for the fp64 evaluation, rounded up to fp32. The first term bounds the
+// copy's error of a score per unit ||x|| (Cauchy-Schwarz); the second covers the fp32
+// rounding of the exact and the approximate products (at most 4K units of roundoff each,
+// against sum |w x| <= ||w|| ||x|| and the Q4_K terms' scale). One warp per row; each lane
+// sums its super-blocks in fp64 and the lanes meet in a fixed butterfly.
+__global__ void shortlist_build_kernel(const uint8_t* __restrict__ wq, uint8_t* __restrict__ small,
+                                       float* __restrict__ bound, int N, int K) {
+  const int lane = threadIdx.x & 31;
+  const long long n = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+  if (n >= N) return;
+  const int nsb = K / 256;
+  const uint8_t* qrow = wq + n * (long long)(K / 32) * 34;
+  uint8_t* srow = small + n * (long long)nsb * 144;
+  double rr = 0.0, ww = 0.0, aa = 0.0;
+  float w[256];
+  for (int g = lane; g < nsb; g += 32) {
+    for (int b8 = 0; b8 < 8; ++b8) {
+      const uint8_t* blk = qrow + (g * 8 + b8) * 34;
+      const float d = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(blk)));
+      for (int i = 0; i < 32; ++i) w[32 * b8 + i] = d * static_cast<float>(static_cast<int8_t>(blk[2 + i]));  // exact
+    }
+    uint8_t* dst = srow + g * 144;
+    int sc[8], m[8];
+    uint16_t d16, dmin16;
+    qk_block<15>(w, dst, sc, m, d16, dmin16);
+    const double d = h2d(d16), dmin = h2d(dmin16);
+    for (int i = 0; i < 256; ++i) {
+      const int j = i >> 5, c = i >> 6, l = i & 31;
+      const int q = (dst[16 + 32 * c + l] >> (4 * (j & 1))) & 15;
+      // exact in fp64: products of fp16 values and small integers, and their difference
+      const double wc = __dadd_rn(__dmul_rn(__dmul_rn(d, static_cast<double>(sc[j])), static_cast<double>(q)),
+                                  -__dmul_rn(dmin, static_cast<double>(m[j])));
+      const double e = __dadd_rn(static_cast<double>(w[i]), -wc);
+      rr = __dadd_rn(rr, __dmul_rn(e, e));
+      ww = __dadd_rn(ww, __dmul_rn(static_cast<double>(w[i]), static_cast<double>(w[i])));
+    }
+    for (int j = 0; j < 8; ++j) {
+      const double t = __dadd_rn(__dmul_rn(__dmul_rn(15.0, d), static_cast<double>(sc[j])),
+                                 __dmul_rn(dmin, static_cast<double>(m[j])));
+      aa = __dadd_rn(aa, __dmul_rn(t, t));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    rr = __dadd_rn(rr, __shfl_xor_sync(0xffffffffu, rr, off));
+    ww = __dadd_rn(ww, __shfl_xor_sync(0xffffffffu, ww, off));
+    aa = __dadd_rn(aa, __shfl_xor_sync(0xffffffffu, aa, off));
+  }
+  if (lane == 0) {
+    const double cK = static_cast<double>(K) * 0x1p-22;
+    const double B = __dadd_rn(sqrt(rr), __dmul_rn(cK, __dadd_rn(sqrt(ww), sqrt(__dmul_rn(32.0, aa)))));
+    bound[n] = __double2float_ru(__dmul_rn(B, 1.0 + 0x1p-32));
   }
 }
 
@@ -275,6 +345,21 @@ int launch_quantize(int fmt, const float* w, void* blocks, int N, int K, cudaStr
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     *err = std::string("quantize launch: ") + cudaGetErrorString(e);
+    return -1;
+  }
+  return 0;
+}
+
+int launch_shortlist_build(const void* wq, void* small, float* bound, int N, int K, cudaStream_t stream,
+                           std::string* err) {
+  if (N == 0) return 0;
+  const int threads = 128;
+  const long long grid = ((long long)N * 32 + threads - 1) / threads;
+  shortlist_build_kernel<<<(unsigned)grid, threads, 0, stream>>>(static_cast<const uint8_t*>(wq),
+                                                                 static_cast<uint8_t*>(small), bound, N, K);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    *err = std::string("shortlist build launch: ") + cudaGetErrorString(e);
     return -1;
   }
   return 0;

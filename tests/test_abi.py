@@ -96,6 +96,37 @@ def test_argument_errors_before_any_cuda_call(kqlib):
     assert L.kq_attention(None, fake, fake, fake, 8, 100, 16, 4, 128, None, 1.0, fake, need, None) == kqlib.KQ_ERR_ARG
 
 
+def test_shortlist_head_argument_checks(kqlib):
+    L = kqlib.lib()
+    fake = 1 << 20
+    # buffer sizes: the small copy rounded up to 256 bytes, then N fp32 bounds
+    assert L.kq_shortlist_bytes(151936, 2048) == 151936 * 8 * 144 + 151936 * 4
+    assert L.kq_shortlist_bytes(3, 256) == 512 + 256  # 432 bytes of copy, 12 of bounds
+    for N, K in ((0, 256), (4, 0), (4, 300), (-1, 256)):
+        assert L.kq_shortlist_bytes(N, K) == 0
+        assert L.kq_shortlist_build(fake, N, K, fake, 1 << 30, None) == kqlib.KQ_ERR_ARG
+    assert L.kq_shortlist_build(fake, 4, 256, fake, 511, None) == kqlib.KQ_ERR_ARG       # buffer too small
+    assert L.kq_shortlist_build(fake, 4, 256, fake + 16, 1 << 20, None) == kqlib.KQ_ERR_ARG  # not 256-aligned
+    # workspace: M*N scores, 2 x 16 words per chunk of 1024 rows, the state
+    assert L.kq_head_argmax_workspace_size(1, 151936) == 607744 + 19200 + 256  # 149 x 128 B rounded up to 256
+    assert L.kq_head_argmax_workspace_size(0, 100) == 0 and L.kq_head_argmax_workspace_size(17, 100) == 0
+    need = L.kq_head_argmax_workspace_size(2, 1000)
+    ok_args = dict(w=fake, sl=fake, xd=kqlib.BF16, x=fake, M=2, N=1000, K=256, tok=fake, sc=fake, rs=None,
+                   ws=fake, wsn=need, fl=0)
+
+    def call(**kw):
+        a = dict(ok_args, **kw)
+        return L.kq_head_argmax(a["w"], a["sl"], a["xd"], a["x"], a["M"], a["N"], a["K"], a["tok"], a["sc"],
+                                a["rs"], a["ws"], a["wsn"], a["fl"], None)
+    assert call(fl=2) == kqlib.KQ_ERR_ARG
+    assert call(M=0) == kqlib.KQ_ERR_ARG and call(M=17) == kqlib.KQ_ERR_ARG
+    assert call(K=300) == kqlib.KQ_ERR_ARG and call(N=0) == kqlib.KQ_ERR_ARG
+    assert call(xd=7) == kqlib.KQ_ERR_UNSUPPORTED
+    assert call(sl=None) == kqlib.KQ_ERR_ARG
+    assert call(x=fake + 8) == kqlib.KQ_ERR_ARG and call(sl=fake + 16) == kqlib.KQ_ERR_ARG
+    assert call(wsn=need - 1) == kqlib.KQ_ERR_WORKSPACE and call(ws=None) == kqlib.KQ_ERR_WORKSPACE
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     import quantized_decode_gemv_block_gb300 as kq
     with pytest.raises(ImportError):
