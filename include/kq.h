@@ -216,7 +216,8 @@ int kq_attention(const float* q, const void* k_cache, const void* v_cache, float
  *   w_q8        the Q8_0 head (device, 16-byte aligned); N >= 1; K a multiple of 256
  *   shortlist   from kq_shortlist_build for this head
  *   x           M x K, fp32 or bf16 (x_dtype), device, 16-byte aligned
- *   token       M int32 (device): the winning row, or -1 if no score is comparable (NaN)
+ *   token       M int32 (device): the winning row (a row whose score is NaN never wins), or
+ *               -1 if no row has a comparable (non-NaN) score
  *   score       M fp32 (device): its exact score
  *   rows_scored NULL or one uint32 (device): the number of rows scored exactly
  *   workspace   kq_head_argmax_workspace_size(M, N) bytes, 256-byte aligned

@@ -181,9 +181,11 @@ __global__ void __launch_bounds__(kThreads) shortlist_lower_kernel(const float* 
 #pragma unroll
       for (int i = 0; i < 4; ++i)
         if (j < M && nn[i] < N) {
-          const float U = __fmul_ru(bnd[i], nx[j]);
-          m[j] = max(m[j], ordered_bits(__fsub_rd(yv[j][i], U)));
-          u[j] = max(u[j], ordered_bits(__fadd_ru(yv[j][i], U)));
+          // a NaN bound or score is not comparable: that row can never win, and it takes no
+          // part in the maxima
+          const float U = __fmul_ru(bnd[i], nx[j]), lo = __fsub_rd(yv[j][i], U), up = __fadd_ru(yv[j][i], U);
+          if (lo == lo) m[j] = max(m[j], ordered_bits(lo));
+          if (up == up) u[j] = max(u[j], ordered_bits(up));
         }
     }
 #pragma unroll
@@ -375,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 2) shortlist_exact_kernel(
 #pragma unroll
           for (int j = 1; j < MT; ++j)
             if (lane == j) v = acc[j];
-          if (!dry && lane < M) {
+          if (!dry && lane < M && v == v) {  // a NaN score never wins
             const unsigned long long key = (static_cast<unsigned long long>(ordered_bits(v)) << 32) |
                                            static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(row));
             atomicMax(&st->key[lane], key);
@@ -396,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 2) shortlist_exact_kernel(
   __threadfence();
   if (threadIdx.x < M) {
     const unsigned long long key = atomicAdd(&st->key[threadIdx.x], 0ull);
-    if (key == 0ull) {  // no row had a comparable score (NaN everywhere)
+    if (key == 0ull) {  // no row had a comparable (non-NaN) score
       token[threadIdx.x] = -1;
       score[threadIdx.x] = __uint_as_float(0x7FC00000u);
     } else {

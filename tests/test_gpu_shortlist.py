@@ -172,3 +172,44 @@ def test_activations_too_large_for_shared_memory_give_the_same_bits(built, orc):
         assert int(t.item()) == int(t16[j])
         assert np.array_equal(s.cpu().numpy().view(np.uint32), s16[j:j + 1].view(np.uint32))
     check_against_oracle(orc, q8, x, N, K, t16, s16)
+
+
+@pytest.mark.parametrize("N,M", [(2047, 3), (1, 2), (5, 1), (1025, 16)])
+def test_ragged_and_tiny_heads(built, orc, N, M):
+    """N not a multiple of 4 (the exact pass's scalar row loads) or of the 1024-row chunks,
+    a one-row head (its only row wins), a head smaller than one warp's rows."""
+    K = 512
+    w = inputs.weights(N, K, seed=N + 17, tensor_id=900)
+    q8 = orc.quantize(Q8_0, w)
+    w_dev = torch.from_numpy(q8).cuda()
+    sl = kq.shortlist_build(w_dev, N, K)
+    targets = np.random.default_rng(N).integers(0, N, M)
+    xh, xd = x_device(inputs.planted_activations_f32(w[targets], 0.5, seed=N), "bf16")
+    tok, sc, scored = run_both(w_dev, sl, xd, N, K)
+    if N == 1:
+        assert list(tok) == [0] * M
+    else:
+        assert np.array_equal(tok, targets)
+    check_against_oracle(orc, q8, xh, N, K, tok, sc)
+
+
+def test_nan_scores_never_win(built, orc):
+    """A row whose Q8_0 scale is NaN scores NaN: it is never the token, with or without the
+    shortlist; hidden states that are NaN give no comparable score at all: token -1."""
+    N, K, M = 600, 256, 2
+    w = inputs.weights(N, K, seed=21, tensor_id=900)
+    q8 = orc.quantize(Q8_0, w)
+    q8[123, 0:2] = np.frombuffer(np.float16(np.nan).tobytes(), np.uint8)  # d of block 0 = NaN
+    w_dev = torch.from_numpy(q8).cuda()
+    sl = kq.shortlist_build(w_dev, N, K)
+    xh, xd = x_device(inputs.planted_activations_f32(w[[123, 400]], 0.5, seed=22), "bf16")
+    tok, sc, _ = run_both(w_dev, sl, xd, N, K)
+    y, _ = orc.gemv(Q8_0, q8, xh, N, K)
+    assert np.isnan(y[:, 123]).all()
+    assert tok[1] == 400 and tok[0] != 123
+    assert tok[0] == int(np.nanargmax(y[0]))
+    xn = xd.clone()
+    xn[0, 5] = float("nan")
+    tok, sc, _ = run_both(w_dev, sl, xn, N, K)
+    assert tok[0] == -1 and np.isnan(sc[0])
+    assert tok[1] == 400
