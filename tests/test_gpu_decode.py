@@ -1,6 +1,6 @@
 """GPU decode step (kq_decode_step) against the fp64 oracle step, and batch invariance.
 
-Tolerance (derived in the design doc): every GEMV input is rounded to bf16, and the GPU (fp32
+Tolerance, and where it comes from: every GEMV input is rounded to bf16, and the GPU (fp32
 arithmetic) and the oracle (fp64) round an activation lying within the GEMV's ~1e-6
 relative error of a bf16 rounding boundary to neighbouring bf16 values (about 1e-6 / 2^-8,
 i.e. 2.6e-4 of the elements at each rounding point). One flip in the head's input moves a
