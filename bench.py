@@ -10,6 +10,7 @@ Prints ONE JSON line (rank 0). Workloads (synthetic data, seeded):
   q8_0     Q8_0 GEMV, W 1024x1024, one fp32 row.
   ffn_q5k  the ffn pair with Q5_K blocks (176 bytes per 256 weights).
   ffn_q6k  the ffn pair with Q6_K blocks (210 bytes per 256 weights; CUDA-core kernel).
+  ffn_affine4  the ffn pair with affine4 gs32 blocks (20 bytes per 32 weights).
   head     Q8_0 lm-head GEMV, W 151936x2048, M bf16 rows (--m).
   shortlist  greedy next token over the same head (kq_head_argmax): scores from the small
            Q4_K copy, exact Q8_0 scores only for rows that can still win; hidden states
@@ -51,6 +52,9 @@ def workload_spec(name: str, m: int):
                     mats=[(9728, 2560), (2560, 9728)], M=1, dtype="bf16")
     if name == "ffn_q5k":
         return dict(name="q5_k ffn gemv 9728x2560 + 2560x9728, M=1 bf16", fmt="q5_k",
+                    mats=[(9728, 2560), (2560, 9728)], M=1, dtype="bf16")
+    if name == "ffn_affine4":
+        return dict(name="affine4 gs32 ffn gemv 9728x2560 + 2560x9728, M=1 bf16", fmt="affine4",
                     mats=[(9728, 2560), (2560, 9728)], M=1, dtype="bf16")
     if name == "ffn_q6k":
         return dict(name="q6_k ffn gemv 9728x2560 + 2560x9728, M=1 bf16", fmt="q6_k",
@@ -937,7 +941,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="kq", choices=["kq", "reference"])
-    ap.add_argument("--workload", default="ffn", choices=["ffn", "ffn_q5k", "ffn_q6k", "verify", "q8_0", "head", "decode",
+    ap.add_argument("--workload", default="ffn", choices=["ffn", "ffn_q5k", "ffn_q6k", "ffn_affine4", "verify", "q8_0", "head", "decode",
                                                         "prefill", "attention", "shortlist"])
     ap.add_argument("--m", type=int, default=16)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
