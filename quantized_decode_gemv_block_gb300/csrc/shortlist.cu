@@ -30,7 +30,10 @@
 // before they wait for their predecessor's results. While they wait, each runs its own code
 // once on inputs that are not ready yet, storing nothing: run cold after the wait, the
 // unrolled code was measured stalling on instruction fetch for several microseconds (the
-// dry run of the exact pass saves 2.4 us per call at M = 1).
+// dry run of the exact pass saves 2.4 us per call at M = 1). Everything a kernel of the
+// call produced (the scores, the chunk maxima, the norms) is read with L2-only loads
+// (ld.global.cg): a dry pass reads those addresses before they are written, and a line it
+// left in L1 must not answer the real pass.
 #include "kq_device.cuh"
 #include "kq_internal.h"
 
@@ -130,9 +133,11 @@ __device__ void xnorms_up(const XT* __restrict__ x, int M, int K, float (*red)[k
 }
 
 // cta_max[c][0][j]: the largest lower bound of chunk c for token j; cta_max[c][1][j]: the
-// largest upper bound (ordered bit patterns, 0 below everything).
+// largest upper bound (ordered bit patterns, 0 below everything). At most 80 registers a
+// thread, so that a CTA fits beside a GEMV CTA (167 registers x 256 threads) and can start,
+// and run its dry pass, while the GEMV streams.
 template <class XT>
-__global__ void __launch_bounds__(kThreads) shortlist_lower_kernel(const float* __restrict__ ya,
+__global__ void __launch_bounds__(kThreads, 3) shortlist_lower_kernel(const float* __restrict__ ya,
                                                                    const float* __restrict__ bound,
                                                                    const XT* __restrict__ x, int M, int N, int K,
                                                                    uint32_t* __restrict__ cta_max,
@@ -172,7 +177,7 @@ __global__ void __launch_bounds__(kThreads) shortlist_lower_kernel(const float* 
 #pragma unroll
     for (int j = 0; j < kMaxTok; ++j)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) yv[j][i] = (j < M && nn[i] < N) ? ya[(size_t)j * N + nn[i]] : 0.f;
+      for (int i = 0; i < 4; ++i) yv[j][i] = (j < M && nn[i] < N) ? __ldcg(ya + (size_t)j * N + nn[i]) : 0.f;
     uint32_t m[kMaxTok], u[kMaxTok];
 #pragma unroll
     for (int j = 0; j < kMaxTok; ++j) {
@@ -308,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 2) shortlist_exact_kernel(
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
           const int c = c0 + r * (kThreads / kMaxTok);
-          v[r] = c < nchunks ? cta_max[(2 * c) * kMaxTok + j] : 0u;
+          v[r] = c < nchunks ? __ldcg(cta_max + (2 * c) * kMaxTok + j) : 0u;
         }
 #pragma unroll
         for (int r = 0; r < 8; ++r) m = max(m, v[r]);
@@ -318,9 +323,9 @@ __global__ void __launch_bounds__(kThreads, 2) shortlist_exact_kernel(
     __syncthreads();
     if (threadIdx.x < M) {
       L[threadIdx.x] = dry ? __uint_as_float(0x7F800000u) : from_ordered_bits(lb[threadIdx.x]);
-      nx[threadIdx.x] = st->nx[threadIdx.x];
+      nx[threadIdx.x] = __ldcg(&st->nx[threadIdx.x]);
       // this chunk can hold a winner only if its largest upper bound reaches some token's L
-      if (!all_rows && cta_max[(2 * blockIdx.x + 1) * kMaxTok + threadIdx.x] >= lb[threadIdx.x]) open = true;
+      if (!all_rows && __ldcg(cta_max + (2 * blockIdx.x + 1) * kMaxTok + threadIdx.x) >= lb[threadIdx.x]) open = true;
     }
     __syncthreads();
     if (open || dry) {
@@ -340,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 2) shortlist_exact_kernel(
 #pragma unroll
           for (int j = 0; j < kMaxTok; ++j) {
             float4 y4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (j < M) y4 = *reinterpret_cast<const float4*>(ya + (size_t)j * N + nt);
+            if (j < M) y4 = __ldcg(reinterpret_cast<const float4*>(ya + (size_t)j * N + nt));
             yv[j][0] = y4.x; yv[j][1] = y4.y; yv[j][2] = y4.z; yv[j][3] = y4.w;
           }
         } else {
@@ -348,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 2) shortlist_exact_kernel(
           for (int i = 0; i < 4; ++i) {
             bnd[i] = nt + i < N ? bound[nt + i] : 0.f;
 #pragma unroll
-            for (int j = 0; j < kMaxTok; ++j) yv[j][i] = (j < M && nt + i < N) ? ya[(size_t)j * N + nt + i] : 0.f;
+            for (int j = 0; j < kMaxTok; ++j) yv[j][i] = (j < M && nt + i < N) ? __ldcg(ya + (size_t)j * N + nt + i) : 0.f;
           }
         }
 #pragma unroll
