@@ -410,8 +410,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 // The pre-pass, one launch:
 //  blocks [0, M): token j. x'[k] = fp16(x[k] * 2^e) (exact; the token's max |x| lands in
-//    [2^14, 2^15)), then for each sub-block b the fp32 sum S of its 32 x' (k ascending),
-//    S/64 = hi + lo in fp16, written as [x' (K) | hi (K/32) | lo (K/32) | hi (K/32) | 0 ...].
+//    [2^14, 2^15)), then for each sub-block b the fp32 sum S of its 32 x' (four sums of 8,
+//    k ascending, added as (s0 + s1) + (s2 + s3)), S/64 = hi + lo in fp16, written as
+//    [x' (K) | hi (K/32) | lo (K/32) | hi (K/32) | 0 ...].
 //    inv_scale[j] = 2^-e.
 //  blocks [M, ...): one thread per (weight row, super-block): -64*dmin*m_b (exact in fp32)
 //    = hi + lo in fp16, written as [hi (K/32) | hi (K/32) | lo (K/32) | 0 ...].
@@ -422,12 +423,17 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(const uint16_t* __res
   const int G = K / 32;
   if ((int)blockIdx.x < M) {
     __shared__ unsigned int smax;
-    const int tok = blockIdx.x;
+    const int tok = blockIdx.x, nch = K / 8;  // 16-byte chunks of the row; 4 per sub-block
     if (threadIdx.x == 0) smax = 0u;
     __syncthreads();
     const uint16_t* xr = x + (long long)tok * K;
     unsigned int best = 0u;
-    for (int i = threadIdx.x; i < K; i += 256) best = max(best, ((unsigned int)xr[i] & 0x7FFFu) << 16);
+    for (int c = threadIdx.x; c < nch; c += 256) {
+      const uint4 v = ldg128(xr + 8 * c);
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) best = max(best, max((wv[i] & 0x7FFFu) << 16, wv[i] & 0x7FFF0000u));
+    }
     atomicMax(&smax, best);
     __syncthreads();
     const unsigned int mb = smax;
@@ -437,11 +443,13 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(const uint16_t* __res
     const float sc = __int_as_float((e + 127) << 23);
     if (threadIdx.x == 0) inv_scale[tok] = 1.0f / sc;
     __half* xo = xc + (long long)tok * kc_x;
-    for (int g = threadIdx.x; g < G; g += 256) {
+    // every thread converts whole chunks; a sub-block's four chunks sit in four adjacent
+    // lanes, whose sums (each k ascending) meet as (c0 + c1) + (c2 + c3)
+    for (int base = 0; base < nch; base += 256) {
+      const int c = base + threadIdx.x;
       float s = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint4 v = *reinterpret_cast<const uint4*>(xr + 32 * g + 8 * c);
+      if (c < nch) {
+        const uint4 v = ldg128(xr + 8 * c);
         const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
         uint32_t o[4];
 #pragma unroll
@@ -452,14 +460,19 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(const uint16_t* __res
           s += __half2float(b);
           o[i] = (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(b) << 16);
         }
-        *reinterpret_cast<uint4*>(xo + 32 * g + 8 * c) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(xo + 8 * c) = make_uint4(o[0], o[1], o[2], o[3]);
       }
-      const float s64 = s * 0.015625f;
-      const __half hi = __float2half_rn(s64);
-      const __half lo = __float2half_rn(s64 - __half2float(hi));
-      xo[K + g] = hi;
-      xo[K + G + g] = lo;
-      xo[K + 2 * G + g] = hi;
+      s += __shfl_xor_sync(0xffffffffu, s, 1);
+      s += __shfl_xor_sync(0xffffffffu, s, 2);
+      if (c < nch && (c & 3) == 0) {
+        const int g = c >> 2;
+        const float s64 = s * 0.015625f;
+        const __half hi = __float2half_rn(s64);
+        const __half lo = __float2half_rn(s64 - __half2float(hi));
+        xo[K + g] = hi;
+        xo[K + G + g] = lo;
+        xo[K + 2 * G + g] = hi;
+      }
     }
     for (int i = K + 3 * G + threadIdx.x; i < kc_x; i += 256) xo[i] = __ushort_as_half(0);
   } else {
