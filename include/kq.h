@@ -13,6 +13,9 @@
  *  - Same section: long prompts run as tiled matrix products so that each weight
  *    block is unpacked once and used for many tokens. kq_gemm with M > 16 is that
  *    prefill product, on the tensor cores.
+ *  - Same section: the next token is chosen from an output layer of up to a quarter of
+ *    a million rows by bounding every row's score from a small copy and scoring exactly
+ *    only the rows that can still win. kq_shortlist_build / kq_head_argmax are that head.
  *  - Kinetic README, "Switching from llama.cpp": GGUF files work unchanged, so
  *    Q8_0 and Q4_K blocks use GGUF's byte layouts. Kipp README, "How fast": its
  *    4-bit scheme is affine (scale + bias) with groups of 32 (layout below).
@@ -21,7 +24,9 @@
  * (GGUF order). X is M x K row-major (fp32 or bf16). Y is M x N fp32 row-major and
  * is overwritten, never accumulated. All pointers are DEVICE pointers unless a
  * function says otherwise. The caller owns every buffer; the library allocates
- * nothing per call and keeps no state besides a thread-local error string.
+ * nothing per call. Its only state: a thread-local error string, per-device caches of
+ * the SM count and of kernel attributes, the device error words read by
+ * kq_device_errors(), and the fixed scratch array of kq_decode_step_static.
  * Every call is asynchronous on `stream` (a cudaStream_t passed as void*, NULL =
  * the legacy default stream) and never synchronises. There is no CPU fallback:
  * a call either launches the sm_103a kernels or returns an error.
