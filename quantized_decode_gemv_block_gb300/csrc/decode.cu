@@ -55,7 +55,13 @@ __device__ float block_sum(float v, float* red) {
 }
 
 // h[j] = x[j] (bf16 -> fp32) if x != null; then, if add != null, h[j] += add[j]; then
-// out[j] = bf16(h[j] / sqrt(mean(h[j]^2) + eps)). One CTA per token.
+// out[j] = bf16(h[j] / sqrt(mean(h[j]^2) + eps)). One CTA per token; D % 4 == 0 (the hidden
+// size is a multiple of 256). Thread t takes the 4-element chunks t, t + 256, ... of the row;
+// the first kNormChunks of them stay in registers, so every load of a row up to 4096 wide is
+// in flight at once (this kernel sits between two GEMVs on the decode step's critical path)
+// and the normalisation reads nothing back. Sum of squares: per thread in chunk order,
+// elements in order, then a fixed block tree.
+constexpr int kNormChunks = 4;
 __global__ void __launch_bounds__(kGlueThreads) add_rmsnorm_kernel(float* __restrict__ h,
                                                                    const uint16_t* __restrict__ x,
                                                                    const float* __restrict__ add,
@@ -64,18 +70,80 @@ __global__ void __launch_bounds__(kGlueThreads) add_rmsnorm_kernel(float* __rest
   pdl_trigger();
   pdl_wait();
   __shared__ float red[kGlueThreads / 32];
-  const int j = blockIdx.x;
+  const int j = blockIdx.x, nch = D / 4;
   float* hj = h + (long long)j * D;
+  const float* aj = add ? add + (long long)j * D : nullptr;
+  const uint16_t* xj = x ? x + (long long)j * D : nullptr;
+  float4 v[kNormChunks], a[kNormChunks];
+#pragma unroll
+  for (int r = 0; r < kNormChunks; ++r) {
+    const int c = threadIdx.x + r * kGlueThreads;
+    v[r] = a[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c < nch) {
+      if (xj) {
+        const uint2 u = *reinterpret_cast<const uint2*>(xj + 4 * c);
+        v[r] = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                           __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+      } else {
+        v[r] = *reinterpret_cast<const float4*>(hj + 4 * c);
+      }
+      if (aj) a[r] = *reinterpret_cast<const float4*>(aj + 4 * c);
+    }
+  }
   float ss = 0.f;
-  for (int i = threadIdx.x; i < D; i += kGlueThreads) {
-    float v = x ? __uint_as_float((uint32_t)x[(long long)j * D + i] << 16) : hj[i];
-    if (add) v = v + add[(long long)j * D + i];
-    hj[i] = v;
-    ss = __fmaf_rn(v, v, ss);
+#pragma unroll
+  for (int r = 0; r < kNormChunks; ++r) {
+    const int c = threadIdx.x + r * kGlueThreads;
+    if (c < nch) {
+      if (aj) {
+        v[r].x = v[r].x + a[r].x;
+        v[r].y = v[r].y + a[r].y;
+        v[r].z = v[r].z + a[r].z;
+        v[r].w = v[r].w + a[r].w;
+      }
+      *reinterpret_cast<float4*>(hj + 4 * c) = v[r];
+      ss = __fmaf_rn(v[r].x, v[r].x, ss);
+      ss = __fmaf_rn(v[r].y, v[r].y, ss);
+      ss = __fmaf_rn(v[r].z, v[r].z, ss);
+      ss = __fmaf_rn(v[r].w, v[r].w, ss);
+    }
+  }
+  for (int c = threadIdx.x + kNormChunks * kGlueThreads; c < nch; c += kGlueThreads) {  // rows > 4096
+    float4 w = xj ? make_float4(0.f, 0.f, 0.f, 0.f) : *reinterpret_cast<const float4*>(hj + 4 * c);
+    if (xj) {
+      const uint2 u = *reinterpret_cast<const uint2*>(xj + 4 * c);
+      w = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+                      __uint_as_float(u.y & 0xFFFF0000u));
+    }
+    if (aj) {
+      const float4 b = *reinterpret_cast<const float4*>(aj + 4 * c);
+      w.x = w.x + b.x;
+      w.y = w.y + b.y;
+      w.z = w.z + b.z;
+      w.w = w.w + b.w;
+    }
+    *reinterpret_cast<float4*>(hj + 4 * c) = w;
+    ss = __fmaf_rn(w.x, w.x, ss);
+    ss = __fmaf_rn(w.y, w.y, ss);
+    ss = __fmaf_rn(w.z, w.z, ss);
+    ss = __fmaf_rn(w.w, w.w, ss);
   }
   const float tot = block_sum(ss, red);
   const float inv = 1.0f / sqrtf(tot / (float)D + eps);
-  for (int i = threadIdx.x; i < D; i += kGlueThreads) out[(long long)j * D + i] = f2bf(hj[i] * inv);
+#pragma unroll
+  for (int r = 0; r < kNormChunks; ++r) {
+    const int c = threadIdx.x + r * kGlueThreads;
+    if (c < nch)
+      *reinterpret_cast<uint2*>(out + (long long)j * D + 4 * c) =
+          make_uint2((uint32_t)f2bf(v[r].x * inv) | ((uint32_t)f2bf(v[r].y * inv) << 16),
+                     (uint32_t)f2bf(v[r].z * inv) | ((uint32_t)f2bf(v[r].w * inv) << 16));
+  }
+  for (int c = threadIdx.x + kNormChunks * kGlueThreads; c < nch; c += kGlueThreads) {
+    const float4 w = *reinterpret_cast<const float4*>(hj + 4 * c);
+    *reinterpret_cast<uint2*>(out + (long long)j * D + 4 * c) =
+        make_uint2((uint32_t)f2bf(w.x * inv) | ((uint32_t)f2bf(w.y * inv) << 16),
+                   (uint32_t)f2bf(w.z * inv) | ((uint32_t)f2bf(w.w * inv) << 16));
+  }
 }
 
 // out[j][hq*hd + d] = bf16(qkv[j][q_dim + kv_dim + (hq / group)*hd + d]): the attention
