@@ -218,7 +218,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_chunk_kernel(const AttnP
 // out[i][hq][d] = sum_c e_c o_c[d] / sum_c e_c l_c, e_c = exp(m_c - max_c m_c); zeros when
 // the token sees no position. One CTA per (row, kv head) of kCombGroups x HD threads: group
 // g adds the chunks c = g (mod kCombGroups) in index order (eight chunks' loads in flight at
-// once), then the groups' sums are added in group order. The chunks' (m, l) pass through
+// once; the first eight leave with the loads of the chunks' maxima), then the groups' sums
+// are added in group order. The chunks' (m, l) pass through
 // shared memory. The order depends on L alone.
 constexpr int kMaxChunks = 1024;
 constexpr int kCombGroups = 4;
@@ -231,6 +232,14 @@ __global__ void __launch_bounds__(HD * kCombGroups) attn_combine_kernel(const At
   const int grp = t / HD, d = t - grp * HD;
   const float* base = p.part + (long long)kvh * p.nchunks * p.R * PW + (long long)r * PW;
   const long long cs = (long long)p.R * PW;
+  // the partials of this thread's first eight chunks: their loads do not depend on the
+  // maxima, so they leave with the (m, l) loads instead of one round trip later
+  float ov0[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int cc = grp + j * kCombGroups;
+    ov0[j] = cc < p.nchunks ? base[cc * cs + d] : 0.f;
+  }
   float mloc = -INFINITY;
   for (int c = t; c < p.nchunks; c += NT) {
     const float2 ml = *reinterpret_cast<const float2*>(base + c * cs + HD);
@@ -247,21 +256,38 @@ __global__ void __launch_bounds__(HD * kCombGroups) attn_combine_kernel(const At
   for (int w = 1; w < NT / 32; ++w) mt = fmaxf(mt, sm_red[w]);  // a maximum: exact in any order
   for (int c = t; c < p.nchunks; c += NT) sm_m[c] = (mt == -INFINITY || sm_m[c] == -INFINITY) ? 0.f : expf(sm_m[c] - mt);
   __syncthreads();
+  // chunks grp, grp + 4, ... in index order, one FMA each (the first eight from ov0)
   float num = 0.f, den = 0.f;
   int c = grp;
-  for (; c + 7 * kCombGroups < p.nchunks; c += 8 * kCombGroups) {
-    float ov[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) ov[j] = base[(c + j * kCombGroups) * cs + d];
+  if (c + 7 * kCombGroups < p.nchunks) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      num = __fmaf_rn(sm_m[c + j * kCombGroups], ov[j], num);
+      num = __fmaf_rn(sm_m[c + j * kCombGroups], ov0[j], num);
       den = __fmaf_rn(sm_m[c + j * kCombGroups], sm_l[c + j * kCombGroups], den);
     }
-  }
-  for (; c < p.nchunks; c += kCombGroups) {
-    num = __fmaf_rn(sm_m[c], base[c * cs + d], num);
-    den = __fmaf_rn(sm_m[c], sm_l[c], den);
+    c += 8 * kCombGroups;
+    for (; c + 7 * kCombGroups < p.nchunks; c += 8 * kCombGroups) {
+      float ov[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ov[j] = base[(c + j * kCombGroups) * cs + d];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        num = __fmaf_rn(sm_m[c + j * kCombGroups], ov[j], num);
+        den = __fmaf_rn(sm_m[c + j * kCombGroups], sm_l[c + j * kCombGroups], den);
+      }
+    }
+    for (; c < p.nchunks; c += kCombGroups) {
+      num = __fmaf_rn(sm_m[c], base[c * cs + d], num);
+      den = __fmaf_rn(sm_m[c], sm_l[c], den);
+    }
+  } else {  // at most eight chunks for this group: all prefetched
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (c + j * kCombGroups < p.nchunks) {
+        num = __fmaf_rn(sm_m[c + j * kCombGroups], ov0[j], num);
+        den = __fmaf_rn(sm_m[c + j * kCombGroups], sm_l[c + j * kCombGroups], den);
+      }
+    }
   }
   sm_num[grp][d] = num;
   if (d == 0) sm_den[grp] = den;
