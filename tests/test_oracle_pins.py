@@ -50,7 +50,8 @@ def test_fp16_rn_matches_numpy(orc):
     vals += [65504.0, 65519.99, 65520.0, 65536.0, 1e300, -1e300, 2.0 ** -25, 2.0 ** -25 * 1.0000001,
              3 * 2.0 ** -26, 2.0 ** -26, 0.0, -0.0, float("inf"), float("-inf")]
     for v in vals:
-        ref = int(np.array([v], dtype=np.float64).astype(np.float16).view(np.uint16)[0])
+        with np.errstate(over="ignore"):  # values past fp16's range round to inf, as intended
+            ref = int(np.array([v], dtype=np.float64).astype(np.float16).view(np.uint16)[0])
         assert orc.double_to_half_rn(float(v)) == ref, v
 
 
