@@ -35,6 +35,21 @@ def test_header_declares_the_boundary():
         assert n in names
 
 
+def test_header_is_plain_c(tmp_path):
+    """The boundary is a C ABI: the header compiles as strict C99 and links against the library's
+    symbols by name only (no C++ types, no torch)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_kq.c"
+    src.write_text('#include "kq.h"\nint main(void) { return kq_block_bytes(KQ_Q4_K) == 144 ? 0 : 1; }\n')
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        "-fsyntax-only", str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_library_exports_every_declared_symbol(kqlib):
     L = ctypes.CDLL(kqlib.LIB_PATH)
     missing = [n for n in declared_functions() if not hasattr(L, n)]
