@@ -50,6 +50,39 @@ def test_header_is_plain_c(tmp_path):
     assert r.returncode == 0, r.stderr
 
 
+def test_c_program_links_and_calls_the_library(kqlib, tmp_path):
+    """A plain C caller links libkq.so and gets sizes, the version and argument errors (every
+    call below returns before any CUDA work, so no GPU is needed)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "call_kq.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include <string.h>
+#include "kq.h"
+int main(void) {
+  if (kq_row_bytes(KQ_Q4_K, 2560) != 1440 || kq_row_bytes(KQ_Q8_0, 2048) != 2176) return 1;
+  if (strstr(kq_version(), "sm_103a") == NULL) return 2;
+  if (kq_gemv(KQ_Q4_K, NULL, KQ_BF16, NULL, NULL, 1, 8, 300, NULL) != KQ_ERR_ARG) return 3;
+  if (strlen(kq_last_error()) == 0) return 4;
+  if (kq_gemv(KQ_Q4_K, NULL, KQ_BF16, NULL, NULL, 0, 8, 256, NULL) != KQ_OK) return 5;
+  if (kq_shortlist_bytes(151936, 2048) != (size_t)151936 * 8 * 144 + (size_t)151936 * 4) return 6;
+  puts("ok");
+  return 0;
+}
+""")
+    lib_dir = os.path.dirname(kqlib.LIB_PATH)
+    exe = tmp_path / "call_kq"
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe),
+                        "-L", lib_dir, "-lkq", "-Wl,-rpath," + lib_dir], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert run.returncode == 0 and run.stdout.strip() == "ok", (run.returncode, run.stdout, run.stderr)
+
+
 def test_library_exports_every_declared_symbol(kqlib):
     L = ctypes.CDLL(kqlib.LIB_PATH)
     missing = [n for n in declared_functions() if not hasattr(L, n)]
