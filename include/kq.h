@@ -182,9 +182,12 @@ int kq_quantize(int fmt, const float* w, void* w_blocks, int N, int K, void* str
  *   o = sum_p softmax_p(scale q.k_p) v_p over the visible positions (zeros if none).
  * Scores and sums are fp32 (products of bf16 on the tensor cores, the softmax weights
  * carried as bf16 hi + lo pairs), so o is within about 1e-5 of sum_p w_p |v_p| of the exact
- * value. The cached positions are cut into chunks by L alone and added in a fixed order: a
- * token's output is bit-identical for every M and every position in the batch (given its
- * own mask row). workspace: kq_attention_workspace_size() bytes, 256-byte aligned.
+ * value. Positions 0..L+M-1 are cut into chunks of 128 by absolute position and added in a
+ * fixed order, and positions a token may not see add exact zeros: a token's output is
+ * bit-identical for every M and every position in the batch (given its own mask row), and
+ * (causal) equals the output of the same token alone at cache length L + i with the window's
+ * earlier rows cached -- verifying guesses gives the bits plain decoding gives.
+ * workspace: kq_attention_workspace_size() bytes, 256-byte aligned.
  * Errors: KQ_ERR_ARG, KQ_ERR_WORKSPACE, KQ_ERR_CUDA. */
 size_t kq_attention_workspace_size(int M, int L, int n_q, int n_kv, int head_dim);
 int kq_attention(const float* q, const void* k_cache, const void* v_cache, float* o, int M, int L, int n_q,

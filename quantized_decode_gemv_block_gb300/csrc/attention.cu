@@ -6,11 +6,15 @@
 // mask). Query head hq reads kv head hq / group. q (fp32) is rounded to bf16, K and V are
 // bf16, scores and sums are fp32.
 //
-// Work split (a function of L, never of M): the cached positions are cut into chunks of 128;
-// the window is one more chunk of its own. One CTA per (chunk, kv head) holds the chunk's
-// K and V rows and the Q rows of its head group in shared memory; row r = i*group + g is
-// query head kvh*group + g of token i, so a token's row sits in the same MMA slot whatever
-// M is. Each warp owns 16 rows: S = Q K^T on mma.sync (bf16 in, fp32 out), the chunk's
+// Work split (by absolute position, never by M): positions 0..L+M-1 of the cache arrays (the
+// cached ones, then the window's own at L..L+M-1) are cut into chunks of 128. One CTA per
+// (chunk, kv head) holds the chunk's K and V rows and the Q rows of its head group in shared
+// memory; row r = i*group + g is query head kvh*group + g of token i, so a token's row sits
+// in the same MMA slot whatever M is. A position a token may not see adds exact zeros to its
+// chunk's sums and to the combine, so a token's output depends on its own position and what
+// it sees only: verified in a window of M at cache length L, or decoded alone at cache length
+// L + i with the earlier window rows cached, it gets the same bits (tested).
+// Each warp owns 16 rows: S = Q K^T on mma.sync (bf16 in, fp32 out), the chunk's
 // row maximum m and p = exp(s - m), l = sum p, and o = P V on mma.sync with P split into
 // bf16 hi + lo parts (P = hi + lo to 2^-16 relative), so o carries fp32 rounding only.
 // A second kernel adds the chunks in index order, each weighted by exp(m_c - max m).
@@ -69,10 +73,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_chunk_kernel(const AttnP
   uint16_t* Ks = Qs + kAttnMaxRows * LD;  // [kChunk][LD]
   uint16_t* Vs = Ks + kChunk * LD;        // [kChunk][LD]
   const int c = blockIdx.x, kvh = blockIdx.y;
-  const int nc = p.nchunks - 1;           // cached chunks; chunk nc is the window
-  const bool win = c == nc;
-  const int pos0 = win ? p.L : c * kChunk;
-  const int npos = win ? p.M : min(kChunk, p.L - pos0);
+  const int pos0 = c * kChunk;
+  const int npos = min(kChunk, p.L + p.M - pos0);
+  const int wcol = p.L - pos0;  // column of window position 0: columns before it are cached positions
   const int kvw = p.n_kv * HD, qw = p.q_stride;
   const int rows16 = (p.R + 15) & ~15;
 
@@ -138,16 +141,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_chunk_kernel(const AttnP
   // scale, visibility, row maxima (rows g and g+8 of the block; a quad shares a row)
   const int ra = r0 + g, rb = r0 + g + 8;
   const int ia = ra / p.group, ib = rb / p.group;
-  const uint32_t ma = win ? (p.mask ? __ldg(p.mask + min(ia, p.M - 1)) : (ia >= 31 ? 0xFFFFFFFFu : ((2u << ia) - 1u))) : 0u;
-  const uint32_t mb = win ? (p.mask ? __ldg(p.mask + min(ib, p.M - 1)) : (ib >= 31 ? 0xFFFFFFFFu : ((2u << ib) - 1u))) : 0u;
+  // window positions each row's token may see: bit j for window position j
+  const uint32_t ma = p.mask ? __ldg(p.mask + min(ia, p.M - 1)) : (ia >= 31 ? 0xFFFFFFFFu : ((2u << ia) - 1u));
+  const uint32_t mb = p.mask ? __ldg(p.mask + min(ib, p.M - 1)) : (ib >= 31 ? 0xFFFFFFFFu : ((2u << ib) - 1u));
   float mxa = -INFINITY, mxb = -INFINITY;
 #pragma unroll
   for (int nt = 0; nt < kChunk / 8; ++nt)
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const int col = nt * 8 + 2 * q4 + e;
-      const bool va = ra < p.R && col < npos && (!win || ((ma >> col) & 1u));
-      const bool vb = rb < p.R && col < npos && (!win || ((mb >> col) & 1u));
+      const int col = nt * 8 + 2 * q4 + e, jw = col - wcol;  // jw: window position, if >= 0
+      const bool va = ra < p.R && col < npos && (jw < 0 || ((ma >> jw) & 1u));
+      const bool vb = rb < p.R && col < npos && (jw < 0 || ((mb >> jw) & 1u));
       s[nt][e] = va ? s[nt][e] * p.scale : -INFINITY;
       s[nt][2 + e] = vb ? s[nt][2 + e] * p.scale : -INFINITY;
       mxa = fmaxf(mxa, s[nt][e]);
@@ -307,7 +311,7 @@ __global__ void __launch_bounds__(HD * kCombGroups) attn_combine_kernel(const At
   }
 }
 
-int attn_chunks(int L) { return (L + kChunk - 1) / kChunk + 1; }
+int attn_chunks(int L, int M) { return (L + M + kChunk - 1) / kChunk; }
 
 template <int HD>
 int launch_attn(const AttnParams& prm, cudaStream_t s, std::string* err) {
@@ -341,7 +345,7 @@ int launch_attn(const AttnParams& prm, cudaStream_t s, std::string* err) {
 
 size_t attention_workspace(int M, int L, int n_q, int n_kv, int hd) {
   const int R = (n_q / n_kv) * M;
-  return (size_t)n_kv * attn_chunks(L) * R * (hd + 2) * sizeof(float);
+  return (size_t)n_kv * attn_chunks(L, M) * R * (hd + 2) * sizeof(float);
 }
 
 int launch_attention(const float* q, int q_stride, const uint16_t* k, const uint16_t* v, float* o, uint16_t* o16,
@@ -362,7 +366,7 @@ int launch_attention(const float* q, int q_stride, const uint16_t* k, const uint
   prm.n_kv = n_kv;
   prm.group = n_q / n_kv;
   prm.R = prm.group * M;
-  prm.nchunks = attn_chunks(L);
+  prm.nchunks = attn_chunks(L, M);
   prm.scale = scale;
   if (hd == 128) return launch_attn<128>(prm, s, err);
   if (hd == 64) return launch_attn<64>(prm, s, err);

@@ -138,7 +138,7 @@ def test_argument_errors_before_any_cuda_call(kqlib):
         assert L.kq_attention(fake, fake, fake, fake, M, Lc, nq, nkv, hd, None, 1.0, fake, 1 << 30, None) \
             == kqlib.KQ_ERR_ARG, (M, Lc, nq, nkv, hd)
     need = L.kq_attention_workspace_size(8, 100, 16, 4, 128)
-    assert need == 4 * 2 * 32 * 130 * 4  # kv heads x (one 128-position chunk + the window) x rows x (d + m, l)
+    assert need == 4 * 1 * 32 * 130 * 4  # kv heads x (108 positions: one 128-position chunk) x rows x (d + m, l)
     assert L.kq_attention(fake, fake, fake, fake, 8, 100, 16, 4, 128, None, 1.0, fake, need - 1, None) \
         == kqlib.KQ_ERR_WORKSPACE
     assert L.kq_attention(None, fake, fake, fake, 8, 100, 16, 4, 128, None, 1.0, fake, need, None) == kqlib.KQ_ERR_ARG

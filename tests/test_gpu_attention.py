@@ -88,3 +88,15 @@ def test_a_tokens_output_is_the_same_for_every_window_size(built):
     for M in (1, 3, 5, 8):
         o = run(q[:M], k[:L + M], v[:L + M], L, n_q, n_kv, hd, 0.0883)
         assert np.array_equal(o.view(np.uint32), full[:M].view(np.uint32)), f"M={M}"
+
+
+@pytest.mark.parametrize("M,L,hd", [(8, 300, 128), (5, 125, 64), (3, 0, 128), (4, 128, 128)])
+def test_window_equals_one_token_at_a_time(built, M, L, hd):
+    """Token i of a window over L cached positions equals token i alone over L + i cached
+    positions (the window's earlier rows now part of the cache), bit for bit."""
+    n_q, n_kv = 16, 4
+    q, k, v = make(M, L, n_q, n_kv, hd, seed=M + L + hd)
+    win = run(q, k, v, L, n_q, n_kv, hd, 0.0883)
+    for i in range(M):
+        o = run(q[i:i + 1], k[:L + i + 1], v[:L + i + 1], L + i, n_q, n_kv, hd, 0.0883)
+        assert np.array_equal(o.view(np.uint32), win[i:i + 1].view(np.uint32)), f"token {i}"

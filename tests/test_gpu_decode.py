@@ -140,6 +140,24 @@ def test_tiny_decode_with_attention_matches_oracle_and_is_batch_invariant(built,
     assert kq.device_errors() == 0
 
 
+@pytest.mark.parametrize("M,L", [(6, 125), (4, 0), (3, 256)])
+def test_verify_window_equals_plain_decoding(built, orc, M, L):
+    """The rule the pages' speed-ups rest on (Kinetic README, "What makes it fast"): checking M
+    guesses in one pass gives the bits plain decoding gives. One step over a window of M tokens
+    at cache length L against M steps of one token each, the cache growing by one row per step:
+    the same logits, bit for bit (the window may cross a 128-position chunk boundary)."""
+    model, hl, head, od = make(orc, TINY, seed=37 + L)
+    cache, _, _ = make_cache(TINY, L, M, seed=38 + L)
+    x = inputs.activations_bf16(M, TINY["hidden"], seed=39 + L)
+    xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+    win = model.step_attn(xd, cache).cpu().numpy()
+    for i in range(M):
+        cache.length = L + i  # the earlier guesses are now cached (their rows were just written)
+        y = model.step_attn(xd[i:i + 1].contiguous(), cache).cpu().numpy()
+        assert np.array_equal(y.view(np.uint32), win[i:i + 1].view(np.uint32)), f"token {i}"
+    assert kq.device_errors() == 0
+
+
 def test_decode_with_attention_and_no_context_is_the_stand_in_step(built, orc):
     """L = 0 and each token seeing only itself: the same logits as kq_decode_step (both
     paths round the same values the same way)."""
