@@ -153,3 +153,18 @@ def test_rejects_bad_arguments():
     with pytest.raises(ValueError):
         orc.attention(np.zeros((33, 8), np.float32), np.zeros((33, 8), np.uint16),
                       np.zeros((33, 8), np.uint16), 0, 1, 1, 8, 1.0)  # window longer than 32
+
+
+def test_window_token_equals_the_token_decoded_alone():
+    """Token i of a causal window over L cached positions sees the same positions, in the same
+    order, as the token alone over L + i cached positions (the window's earlier rows cached):
+    the same fp64 result (the pages' rule that checking guesses gives plain decoding's output)."""
+    rng = np.random.default_rng(6)
+    hd, nq, nkv, L, M = 16, 4, 2, 9, 5
+    q = rng.standard_normal((M, nq * hd)).astype(np.float32)
+    k = rand_bf16(rng, (L + M, nkv * hd))
+    v = rand_bf16(rng, (L + M, nkv * hd))
+    o, base = orc.attention(q, k, v, L, nq, nkv, hd, 0.3)
+    for i in range(M):
+        oi, bi = orc.attention(q[i:i + 1], k[:L + i + 1], v[:L + i + 1], L + i, nq, nkv, hd, 0.3)
+        assert np.array_equal(oi[0], o[i]) and np.array_equal(bi[0], base[i]), i
