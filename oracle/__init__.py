@@ -60,6 +60,8 @@ def lib():
         L.orc_double_to_bf16_rn.argtypes = [ctypes.c_double]
         L.orc_double_to_bf16_rn.restype = ctypes.c_uint16
         L.orc_rmsnorm.argtypes = [P, P, I64, I64, ctypes.c_double]
+        L.orc_bf16_rn_n.argtypes = [P, I64, P]
+        L.orc_swiglu.argtypes = [P, I64, I64, P]
         L.orc_decode_step.argtypes = [I, I, I, I, I, I, I, I, I, ctypes.c_double, P, P, P, P, P, P, I64,
                                       P, I, P]
         L.orc_attention.argtypes = [I, I, I, I, I, P, P, P, P, ctypes.c_float, P, P]
@@ -173,6 +175,23 @@ def gemv_sampled(fmt: int, blocks: np.ndarray, x: np.ndarray, N: int, K: int, js
 
 def double_to_bf16_rn(v: float) -> int:
     return lib().orc_double_to_bf16_rn(v)
+
+
+def bf16_rn(v: np.ndarray) -> np.ndarray:
+    """bf16 bits of every value of v (fp64 in, nearest, ties to even), same shape."""
+    a = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(a.shape, dtype=np.uint16)
+    lib().orc_bf16_rn_n(_ptr(a), a.size, _ptr(out))
+    return out
+
+
+def swiglu_bf16(gu: np.ndarray) -> np.ndarray:
+    """bf16 bits of silu(g) * u for gu = [g | u] (M x 2F, fp64 arithmetic) -> M x F."""
+    gu = np.ascontiguousarray(gu, dtype=np.float64)
+    M, F2 = gu.shape
+    out = np.empty((M, F2 // 2), dtype=np.uint16)
+    lib().orc_swiglu(_ptr(gu), M, F2 // 2, _ptr(out))
+    return out
 
 
 def rmsnorm_bf16(h: np.ndarray, eps: float) -> np.ndarray:

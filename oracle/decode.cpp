@@ -63,11 +63,33 @@ void rmsnorm_bf16(const std::vector<double>& h, int64_t M, int64_t D, double eps
   }
 }
 
+// act[j][i] = bf16(silu(g) * u), g = gu[j][i], u = gu[j][F + i], silu(g) = g / (1 + exp(-g)):
+// the gated activation that feeds the down projection.
+void swiglu_bf16(const double* gu, int64_t M, int64_t F, uint16_t* act) {
+  for (int64_t j = 0; j < M; ++j)
+    for (int64_t i = 0; i < F; ++i) {
+      const double g = gu[j * 2 * F + i], u = gu[j * 2 * F + F + i];
+      act[j * F + i] = double_to_bf16_rn(g / (1.0 + std::exp(-g)) * u);
+    }
+}
+
 }  // namespace
 
 extern "C" {
 
 uint16_t orc_double_to_bf16_rn(double v) { return double_to_bf16_rn(v); }
+
+// out[i] = bf16(v[i]) (nearest, ties to even) for n values.
+int orc_bf16_rn_n(const double* v, int64_t n, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = double_to_bf16_rn(v[i]);
+  return 0;
+}
+
+// The SwiGLU of the decode step for M rows (gu: M x 2F, gate then up; act: M x F bf16 bits).
+int orc_swiglu(const double* gu, int64_t M, int64_t F, uint16_t* act) {
+  swiglu_bf16(gu, M, F, act);
+  return 0;
+}
 
 // out = bf16(RMSNorm(h)) for M rows of D values.
 int orc_rmsnorm(const double* h, uint16_t* out, int64_t M, int64_t D, double eps) {
@@ -121,11 +143,7 @@ int orc_decode_step_attn(int n_layers, int hidden, int q_dim, int kv_dim, int he
     for (int64_t i = 0; i < M * D; ++i) h[(size_t)i] += y[(size_t)i];
     rmsnorm_bf16(h, M, D, eps, xb);
     if (orc_gemv(layer_fmt, w_gu[l], BF16, xb.data(), M, 2 * F, D, gu.data(), nullptr, nthreads)) return -1;
-    for (int64_t j = 0; j < M; ++j)
-      for (int64_t i = 0; i < F; ++i) {
-        const double g = gu[(size_t)(j * 2 * F + i)], u = gu[(size_t)(j * 2 * F + F + i)];
-        act[(size_t)(j * F + i)] = double_to_bf16_rn(g / (1.0 + std::exp(-g)) * u);
-      }
+    swiglu_bf16(gu.data(), M, F, act.data());
     if (orc_gemv(layer_fmt, w_down[l], BF16, act.data(), M, D, F, y.data(), nullptr, nthreads)) return -1;
     for (int64_t i = 0; i < M * D; ++i) h[(size_t)i] += y[(size_t)i];
   }
@@ -161,11 +179,7 @@ int orc_decode_step(int n_layers, int hidden, int q_dim, int kv_dim, int head_di
     for (int64_t i = 0; i < M * D; ++i) h[(size_t)i] += y[(size_t)i];
     rmsnorm_bf16(h, M, D, eps, xb);
     if (orc_gemv(layer_fmt, w_gu[l], BF16, xb.data(), M, 2 * F, D, gu.data(), nullptr, nthreads)) return -1;
-    for (int64_t j = 0; j < M; ++j)
-      for (int64_t i = 0; i < F; ++i) {
-        const double g = gu[(size_t)(j * 2 * F + i)], u = gu[(size_t)(j * 2 * F + F + i)];
-        act[(size_t)(j * F + i)] = double_to_bf16_rn(g / (1.0 + std::exp(-g)) * u);
-      }
+    swiglu_bf16(gu.data(), M, F, act.data());
     if (orc_gemv(layer_fmt, w_down[l], BF16, act.data(), M, D, F, y.data(), nullptr, nthreads)) return -1;
     for (int64_t i = 0; i < M * D; ++i) h[(size_t)i] += y[(size_t)i];
   }

@@ -30,6 +30,39 @@ def test_bf16_rounding_matches_torch(orc):
     assert np.array_equal(got, ref)
 
 
+def test_bf16_rounding_of_arrays_matches_torch(orc):
+    """The array form rounds exactly like the scalar one, which torch's converter pins above
+    (the same midpoints, their neighbours, signed zeros, the top of the range)."""
+    rng = np.random.default_rng(4)
+    bits = np.arange(0, 0x7F7F, 53, dtype=np.uint32)
+    lo = (bits << 16).view(np.float32).astype(np.float64)
+    hi = ((bits + 1) << 16).view(np.float32).astype(np.float64)
+    mid = ((lo + hi) / 2).astype(np.float32)
+    vals = np.concatenate([mid, np.nextafter(mid, np.float32(0)), np.nextafter(mid, np.float32(np.inf)), -mid,
+                           (rng.standard_normal(5000) * np.exp2(rng.uniform(-130, 120, 5000))).astype(np.float32),
+                           np.array([0.0, -0.0, 3.39e38, 1e-41], np.float32)])
+    ref = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = orc.bf16_rn(vals.astype(np.float64).reshape(2, -1)).reshape(-1)
+    assert np.array_equal(got, ref)
+
+
+def test_swiglu_closed_forms(orc):
+    """silu(0) * u = 0; silu(g) = g once exp(-g) vanishes against 1 (g = 40), so act = bf16(g u)
+    (a swap of gate and up gives silu(1.5) * 40 = 49.1 there instead of 60); silu of a very
+    negative gate is -0; and random rows equal the formula in numpy fp64 rounded by the pinned
+    scalar rounding."""
+    gu = np.array([[0.0, 40.0, -800.0, 5.0, 1.5, 3.0]], dtype=np.float64)  # g = [0, 40, -800], u = [5, 1.5, 3]
+    act = orc.swiglu_bf16(gu)
+    assert act[0, 0] == 0x0000
+    assert act[0, 1] == orc.double_to_bf16_rn(60.0) == 0x4270
+    assert act[0, 2] == 0x8000
+    rng = np.random.default_rng(8)
+    gu = rng.standard_normal((3, 2 * 96)) * 3.0
+    g, u = gu[:, :96], gu[:, 96:]
+    expect = np.vectorize(orc.double_to_bf16_rn, otypes=[np.uint16])(g / (1.0 + np.exp(-g)) * u)
+    assert np.array_equal(orc.swiglu_bf16(gu), expect)
+
+
 def test_rmsnorm_closed_form(orc):
     eps = 1e-6
     h = np.array([[2.0] * 256, [-0.5] * 256], dtype=np.float64)
