@@ -87,6 +87,22 @@ def workload_spec(name: str, m: int):
     raise SystemExit(f"unknown workload {name}")
 
 
+def shared_config(spec):
+    """The `config` both arms print for a workload (the driver compares the two): what the
+    workload is, its token rows, and how the timed steps keep their inputs out of the L2."""
+    if spec.get("decode"):
+        l2 = "inputs larger than L2: every step streams the model's 1.09 GB of weights"
+    elif spec.get("prefill"):
+        l2 = "inputs larger than L2: rotating W/X/workspace/Y sets totalling >= 4x the L2 size"
+    elif spec.get("attention"):
+        l2 = "inputs larger than L2: rotating KV caches totalling >= 4x the L2 size"
+    elif spec.get("shortlist"):
+        l2 = "inputs larger than L2: two heads and their small copies alternate (> 4x the L2 size)"
+    else:
+        l2 = "inputs larger than L2: rotating weight copies totalling >= 4x the L2 size"
+    return {"workload": spec["name"], "M": spec["M"], "l2": l2}
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -280,7 +296,7 @@ def run_reference(args, spec):
         print(json.dumps({"impl": "reference", "metric": ATTN_METRIC, "value": v_, "unit": "GB/s", "n_gpus": args.gpus,
                           "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
                           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                          "data": "synthetic", "config": {"workload": spec["name"], "M": spec["M"]},
+                          "data": "synthetic", "config": spec["config"],
                           "cpu_baseline": {"value": v_, "unit": "GB/s", "cores": 1, "kind": "oracle",
                                            "sample": "one attention call per step over the full shape, fp64 "
                                                      "scalar oracle, one thread"},
@@ -317,7 +333,7 @@ def run_reference(args, spec):
     line = {"impl": "reference", "metric": metric, "value": v, "unit": unit, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": spec["name"], "M": spec["M"]},
+            "data": "synthetic", "config": spec["config"],
             "cpu_baseline": {"value": v, "unit": unit, "cores": cores, "kind": "oracle",
                              "sample": (f"exact fp64 scores of {spec['mats'][0][0]} of the head's 151936 rows for "
                                         f"M={spec['M']} per step ({nbytes} weight bytes; the argmax's definition), "
@@ -467,7 +483,8 @@ def run_prefill(args, spec):
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp16 x fp16 -> fp32 (bf16 X and Q4_K W converted in-kernel)",
             "data": "synthetic",
-            "config": {"workload": spec["name"], "M": M, "N": N, "K": K, "flop_per_step": flops,
+            "config": spec["config"],
+            "detail": {"workload": spec["name"], "M": M, "N": N, "K": K, "flop_per_step": flops,
                        "weight_bytes_per_step": wq.numel(),
                        "weight_gbs_equivalent": world * wq.numel() / (ms_step * 1e-3) / 1e9,
                        "l2": f"rotating W/X/workspace/Y sets: {copies} x {per_set} B >= 4x L2 ({l2} B)",
@@ -599,7 +616,8 @@ def run_attention(args, spec):
             "metric": ATTN_METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K_,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16 x bf16 -> fp32", "data": "synthetic",
-            "config": {"workload": spec["name"], "M": M, "L": L, "kv_bytes_per_step": step_bytes,
+            "config": spec["config"],
+            "detail": {"workload": spec["name"], "M": M, "L": L, "kv_bytes_per_step": step_bytes,
                        "l2": f"rotating KV caches: {copies} x {step_bytes} B >= 4x L2 ({l2} B)",
                        "parallelism": "replicas" if world > 1 else "single gpu"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -768,7 +786,8 @@ def run_shortlist(args, spec):
             "metric": SHORTLIST_METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K_,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "q4_k / q8_0 x bf16 -> fp32", "data": "synthetic",
-            "config": {"workload": spec["name"], "M": M, "head_bytes": head_bytes, "small_copy_bytes": small_bytes,
+            "config": spec["config"],
+            "detail": {"workload": spec["name"], "M": M, "head_bytes": head_bytes, "small_copy_bytes": small_bytes,
                        "rows_scored_exactly": rows_scored,
                        "l2": f"two heads alternate: 2 x {head_bytes + small_bytes} B >= 4x L2",
                        "small_copy_gemv_us": small_ms * 1e3, "plain_q8_0_gemv_us": plain_ms * 1e3,
@@ -912,11 +931,13 @@ def run_decode(args, spec):
         if cache is not None:
             spec = dict(spec, name=spec["name"] + f", attention over L={L} cached positions (bf16 KV, "
                                                   f"{kv_bytes} B per step)")
+            spec["config"] = dict(spec["config"], workload=spec["name"])
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": spec["name"], "M": M, "weight_bytes_per_step": wbytes,
+            "config": spec["config"],
+            "detail": {"workload": spec["name"], "M": M, "weight_bytes_per_step": wbytes,
                        "tokens_per_s_equivalent": world * M / (ms_step * 1e-3),
                        "l2": f"weights per step {wbytes} B > 4x L2 ({l2} B): every step streams from HBM",
                        "launches_per_step": (10 if cache is not None else 8) * d["n_layers"] + 2,
@@ -940,6 +961,120 @@ def run_decode(args, spec):
         dist.destroy_process_group()
 
 
+def sub_records(args, dev, l2):
+    """The rest of the metric, measured in the same run after the headline: the verify GEMV at
+    every M, the small Q8_0 GEMV, the Q8_0 head, the 28-layer decode step and the prefill GEMM.
+    Each entry: CUDA-graph replays of `sub_steps` calls after `warmup` untimed ones, inputs out
+    of L2 as in the headline (rotating weight copies >= 4x L2; the step streams 1.09 GB)."""
+    import torch
+
+    import quantized_decode_gemv_block_gb300 as kq
+    from quantized_decode_gemv_block_gb300 import decode as kqd
+    from quantized_decode_gemv_block_gb300 import inputs
+
+    peak, _ = measured_peaks()
+    stream = torch.cuda.Stream(device=dev)
+    n, w = args.sub_steps, max(3, args.warmup)
+
+    def timed(body, steps):
+        """ms per call of body(i), i = 0..steps-1, from one graph replay (after a warm replay)."""
+        with torch.cuda.stream(stream):
+            body(0)
+            stream.synchronize()
+        gw, gm = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gw, stream=stream):
+            for i in range(w):
+                body(i)
+        with torch.cuda.graph(gm, stream=stream):
+            for i in range(steps):
+                body(i)
+        with torch.cuda.stream(stream):
+            gw.replay()
+        stream.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record()
+            gm.replay()
+            b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    def gemv_entry(fmt, N, K, Ms, xdt):
+        base = kq.quantize(fmt, inputs.weights_cuda(N, K, seed=0, tensor_id=0, device=str(dev)))
+        nb = base.numel()
+        copies = max(2, math.ceil(4 * l2 / nb))
+        ws = [base] + [base.clone() for _ in range(copies - 1)]
+        out = {"weight_bytes": nb}
+        for M in Ms:
+            x = inputs.activations_cuda(M, K, seed=0, tensor_id=1000, dtype=xdt, device=str(dev))
+            y = torch.empty((M, N), dtype=torch.float32, device=dev)
+            ms = timed(lambda i: kq.gemv(fmt, ws[i % copies], x, N, K, y=y, overlap=xdt == torch.bfloat16), n)
+            gbs = nb / (ms * 1e-3) / 1e9
+            out[f"M={M}"] = {"us": ms * 1e3, "GB/s": gbs, "frac": gbs / peak, "pct_of_8tbs": gbs / 8000.0}
+        del ws
+        return out
+
+    rec = {"peak_hbm_gbs": peak, "steps": n, "warmup": w,
+           "timing": "CUDA-graph replay of `steps` calls / steps; consecutive GEMVs may overlap (programmatic "
+                     "dependent launch), as in the headline"}
+    rec["q4_k_verify_12288x4096_bf16"] = gemv_entry("q4_k", 12288, 4096, [1, 2, 4, 8, 16], torch.bfloat16)
+    rec["q8_0_gemv_1024x1024_f32"] = gemv_entry("q8_0", 1024, 1024, [1], torch.float32)
+    rec["q8_0_head_151936x2048_bf16"] = gemv_entry("q8_0", 151936, 2048, [1, 8], torch.bfloat16)
+    torch.cuda.empty_cache()
+
+    # the dense 28-layer decode step (kq_decode_step) replayed as one graph per step
+    d = kqd.DENSE_28L
+    model = kqd.random_model(d, seed=0, device=str(dev))
+    wbytes = kqd.weight_bytes(model)
+    dec = {"weight_bytes": wbytes, "launches_per_step": 8 * d["n_layers"] + 2}
+    for M in (1, 8):
+        g = kqd.GraphStep(model, M, stream=stream)
+        g.x.copy_(torch.randn((M, d["hidden"]), device=dev).to(torch.bfloat16))
+        for _ in range(w):
+            g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        steps = max(5, n // 5)
+        with torch.cuda.stream(stream):
+            a.record()
+        for _ in range(steps):
+            g.replay()
+        with torch.cuda.stream(stream):
+            b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / steps
+        gbs = wbytes / (ms * 1e-3) / 1e9
+        dec[f"M={M}"] = {"us": ms * 1e3, "GB/s": gbs, "frac": gbs / peak, "pct_of_8tbs": gbs / 8000.0,
+                         "tokens_per_s": M / (ms * 1e-3)}
+        del g
+    rec["decode_step_dense_28l"] = dec
+    del model
+    torch.cuda.empty_cache()
+
+    # the prefill GEMM on the tensor cores (kq_gemm, M = 2048)
+    N, K, M = 9728, 2560, 2048
+    wq = kq.quantize("q4_k", inputs.weights_cuda(N, K, seed=0, tensor_id=0, device=str(dev)))
+    x0 = inputs.activations_cuda(M, K, seed=0, tensor_id=1000, dtype=torch.bfloat16, device=str(dev))
+    need = kq.gemm_workspace_size("q4_k", torch.bfloat16, M, N, K)
+    per_set = wq.numel() + x0.numel() * 2 + need + M * N * 4
+    copies = max(2, math.ceil(4 * l2 / per_set))
+    sets = [(wq.clone(), x0.clone(), torch.empty(need, dtype=torch.uint8, device=dev),
+             torch.empty((M, N), dtype=torch.float32, device=dev)) for _ in range(copies)]
+    ms = timed(lambda i: kq.gemm("q4_k", sets[i % copies][0], sets[i % copies][1], N, K, y=sets[i % copies][3],
+                                 workspace=sets[i % copies][2]), max(10, n // 4))
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tpeak = float(json.load(f)["bf16_tflops"])
+    except Exception:
+        tpeak = 1900.0
+    tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+    rec["prefill_q4_k_9728x2560_m2048"] = {"us": ms * 1e3, "TFLOP/s": tf, "frac": tf / tpeak,
+                                           "peak_bf16_tflops": tpeak}
+    del sets
+    torch.cuda.empty_cache()
+    return rec
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -951,11 +1086,15 @@ def main():
     ap.add_argument("--m", type=int, default=16)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sub-records", action="store_true",
+                    help="default workload: skip the other configs' measurements after the headline")
+    ap.add_argument("--sub-steps", type=int, default=100)
     ap.add_argument("--attn-ctx", type=int, default=0,
                     help="decode workload: attention over this many cached positions instead of the stand-in")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     spec = workload_spec(args.workload, args.m)
+    spec["config"] = shared_config(spec)  # fixed before the reference arm narrows its sample
     if args.impl == "reference":
         if spec.get("decode"):
             spec = dict(spec, fmt="q4_k", mats=[(3072, 2048), (2048, 2048), (12288, 2048), (2048, 6144)])
@@ -1163,6 +1302,10 @@ def main():
     else:
         traffic = profile_traffic(f"gemv_tma_{args.workload}.md")
 
+    subs = None
+    if world == 1 and args.workload == "ffn" and not args.no_sub_records:
+        subs = sub_records(args, dev, l2)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, passes, el = cpu_oracle_gbps(spec, args.cpu_budget)
@@ -1175,7 +1318,8 @@ def main():
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K_,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": spec["dtype"], "data": "synthetic",
-            "config": {"workload": spec["name"], "M": M, "weight_bytes_per_step": step_bytes,
+            "config": spec["config"],
+            "detail": {"workload": spec["name"], "M": M, "weight_bytes_per_step": step_bytes,
                        "l2": f"rotating weight copies: {copies} x {step_bytes} B >= 4x L2 ({l2} B)",
                        "parallelism": "replicas" if world > 1 else "single gpu",
                        "pct_of_8tbs": value / world / 8000.0},
@@ -1194,6 +1338,8 @@ def main():
             "gpu_launches": K_ * len(spec["mats"]) * (-(-M // 16) if M <= 32 else 2),
             "clocks": clocks,
         }
+        if subs is not None:
+            line["sub_records"] = subs
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

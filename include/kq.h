@@ -186,7 +186,9 @@ int kq_quantize(int fmt, const float* w, void* w_blocks, int N, int K, void* str
  * fixed order, and positions a token may not see add exact zeros: a token's output is
  * bit-identical for every M and every position in the batch (given its own mask row), and
  * (causal) equals the output of the same token alone at cache length L + i with the window's
- * earlier rows cached -- verifying guesses gives the bits plain decoding gives.
+ * earlier rows cached -- verifying guesses gives the bits plain decoding gives. Both
+ * guarantees need finite keys and values: every row of a chunk enters its P V product, a
+ * position the token may not see with weight 0, and 0 * Inf is NaN.
  * workspace: kq_attention_workspace_size() bytes, 256-byte aligned.
  * Errors: KQ_ERR_ARG, KQ_ERR_WORKSPACE, KQ_ERR_CUDA. */
 size_t kq_attention_workspace_size(int M, int L, int n_q, int n_kv, int head_dim);
@@ -280,6 +282,22 @@ size_t kq_decode_workspace_size(const kq_decode_model* model, int M);
 int kq_decode_step(const kq_decode_model* model, const void* x, float* logits, int M, void* workspace,
                    size_t ws_bytes, void* stream);
 
+/* The decode step with a trace: the same launches as kq_decode_step, with a device-to-device
+ * copy of every op's output into `trace` after the op, so that each op can be checked on its
+ * own inputs (a test gives the oracle the GPU's input of every GEMV, RMSNorm and SwiGLU).
+ * trace: kq_decode_trace_size(model, M) bytes of device memory, 256-byte aligned, owned by
+ * the caller. Layout (every field starts on a 256-byte boundary, rows of M tokens):
+ *   h0 (M x hidden fp32: the input as the residual stream), x0 (M x hidden bf16: its RMSNorm,
+ *   the first qkv GEMV's input); then per layer, in order: qkv (M x (q_dim + 2 kv_dim) fp32),
+ *   o_in (M x q_dim bf16: the Wo GEMV's input), y_o (M x hidden fp32), h_mid (fp32: h after
+ *   the attention block), x_mid (bf16: its RMSNorm), gu (M x 2 ffn fp32), act (M x ffn bf16),
+ *   y_d (M x hidden fp32), h_out (fp32), x_out (bf16: the next GEMV's input, the head's after
+ *   the last layer). The logits are bit-identical to kq_decode_step's.
+ * Errors: as kq_decode_step; KQ_ERR_ARG for a NULL, short or misaligned trace. */
+size_t kq_decode_trace_size(const kq_decode_model* model, int M);
+int kq_decode_step_trace(const kq_decode_model* model, const void* x, float* logits, int M, void* workspace,
+                         size_t ws_bytes, void* trace, size_t trace_bytes, void* stream);
+
 /* ---- Decode step with attention over a KV cache (a true speculative step) ----
  * kq_decode_step with its attention stand-in replaced by kq_attention's attention: per layer
  * the window's k and v (rounded to bf16) are written to rows L..L+M-1 of the layer's cache,
@@ -315,7 +333,9 @@ int kq_decode_step_attn(const kq_decode_model* model, const kq_kv_cache* cache, 
  *  - Models whose kq_decode_workspace_size(model, M) exceeds the array are rejected with
  *    KQ_ERR_WORKSPACE and a message giving both sizes.
  *  - The first call on a device looks up the array's device address (with that device
- *    current) and caches it; make that first call before capturing any stream.
+ *    current) and caches it with the device's current context; make that first call
+ *    before capturing any stream. A call that finds another context current (the old
+ *    one was destroyed, e.g. by cudaDeviceReset) looks the address up again.
  *  - Every call on a device shares the one array and leaves the last step's intermediate
  *    values in it; the step writes each value before reading it, so nothing needs
  *    clearing. Two calls that run at the same time on one device (for example on two

@@ -84,6 +84,10 @@ def load_library(path: str = LIB_PATH):
     L.kq_decode_step.argtypes = [ctypes.POINTER(DecodeModelC), P, P, I, P, SZ, P]
     L.kq_decode_step.restype = I
     L.kq_decode_step_static.argtypes = [ctypes.POINTER(DecodeModelC), P, P, I, P]
+    L.kq_decode_trace_size.argtypes = [ctypes.POINTER(DecodeModelC), I]
+    L.kq_decode_trace_size.restype = SZ
+    L.kq_decode_step_trace.argtypes = [ctypes.POINTER(DecodeModelC), P, P, I, P, SZ, P, SZ, P]
+    L.kq_decode_step_trace.restype = I
     L.kq_decode_step_static.restype = I
     L.kq_shortlist_bytes.argtypes = [I, I]
     L.kq_shortlist_bytes.restype = SZ
@@ -317,6 +321,38 @@ class DecodeModel:
         _check(lib().kq_decode_step(ctypes.byref(self.c), x.data_ptr(), logits.data_ptr(), M,
                                     workspace.data_ptr(), workspace.numel(), _stream(stream)))
         return logits
+
+    def step_trace(self, x: torch.Tensor, stream=None):
+        """kq_decode_step_trace: (logits, trace) where trace holds every op's output as torch
+        device tensors: "h0", "x0", and per layer l a dict "layers"[l] with "qkv", "o_in", "y_o",
+        "h_mid", "x_mid", "gu", "act", "y_d", "h_out", "x_out" (bf16 fields as int16 bits)."""
+        M = x.shape[0]
+        c = self.c
+        D, Q, KV, F = c.hidden, c.q_dim, c.kv_dim, c.ffn
+        logits = torch.empty((M, self.vocab), dtype=torch.float32, device=x.device)
+        ws = torch.empty(self.workspace_size(M), dtype=torch.uint8, device=x.device)
+        need = lib().kq_decode_trace_size(ctypes.byref(c), M)
+        buf = torch.empty(need, dtype=torch.uint8, device=x.device)
+        _check(lib().kq_decode_step_trace(ctypes.byref(c), x.data_ptr(), logits.data_ptr(), M, ws.data_ptr(),
+                                          ws.numel(), buf.data_ptr(), buf.numel(), _stream(stream)))
+        al = lambda n: (n + 255) // 256 * 256
+        off = 0
+
+        def take(cols, f32):
+            nonlocal off
+            nb = M * cols * (4 if f32 else 2)
+            t = buf[off:off + nb].view(torch.float32 if f32 else torch.int16).view(M, cols)
+            off = al(off + nb)
+            return t
+
+        tr = {"h0": take(D, True), "x0": take(D, False), "layers": []}
+        for _ in range(c.n_layers):
+            tr["layers"].append({"qkv": take(Q + 2 * KV, True), "o_in": take(Q, False), "y_o": take(D, True),
+                                 "h_mid": take(D, True), "x_mid": take(D, False), "gu": take(2 * F, True),
+                                 "act": take(F, False), "y_d": take(D, True), "h_out": take(D, True),
+                                 "x_out": take(D, False)})
+        assert off <= need
+        return logits, tr
 
     def attn_workspace_size(self, M: int, L: int) -> int:
         return lib().kq_decode_attn_workspace_size(ctypes.byref(self.c), M, L)

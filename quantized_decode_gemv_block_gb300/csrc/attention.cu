@@ -224,7 +224,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_chunk_kernel(const AttnP
 // g adds the chunks c = g (mod kCombGroups) in index order (eight chunks' loads in flight at
 // once; the first eight leave with the loads of the chunks' maxima), then the groups' sums
 // are added in group order. The chunks' (m, l) pass through
-// shared memory. The order depends on L alone.
+// shared memory. Chunks are added in index order, and their number, ceil((L + M) / 128),
+// depends on L + M; a chunk holding no position the token may see has m = -inf, so its
+// weight e_c is exactly 0 and its o_c and l_c are exact zeros: it adds nothing. That is
+// what keeps a window token's bits equal to those of the same token decoded alone (whose
+// sum has fewer chunks), given finite cached keys and values (a masked position still
+// enters the P V product with P = 0, and 0 * Inf is NaN).
 constexpr int kMaxChunks = 1024;
 constexpr int kCombGroups = 4;
 template <int HD>

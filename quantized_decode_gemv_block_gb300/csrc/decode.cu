@@ -239,7 +239,40 @@ Ws carve(const kq_decode_model* m, int M, void* base) {
   return w;
 }
 
+// The trace buffer of kq_decode_step_trace: h0 and x0, then per layer qkv, o_in, y_o, h_mid,
+// x_mid, gu, act, y_d, h_out, x_out, each field 256-byte aligned, in that order.
+struct TraceLayout {
+  size_t h0, x0, layer0, layer_bytes, bytes;
+  size_t qkv, o_in, y_o, h_mid, x_mid, gu, act, y_d, h_out, x_out;  // offsets within a layer
+};
+
+TraceLayout trace_layout(const kq_decode_model* m, int M) {
+  TraceLayout t;
+  const size_t D = m->hidden, QKV = m->q_dim + 2 * m->kv_dim, F = m->ffn, Q = m->q_dim;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { const size_t o = off; off = al256(off + bytes); return o; };
+  t.h0 = take(4 * M * D);
+  t.x0 = take(2 * M * D);
+  t.layer0 = off;
+  off = 0;
+  t.qkv = take(4 * M * QKV);
+  t.o_in = take(2 * M * Q);
+  t.y_o = take(4 * M * D);
+  t.h_mid = take(4 * M * D);
+  t.x_mid = take(2 * M * D);
+  t.gu = take(4 * M * 2 * F);
+  t.act = take(2 * M * F);
+  t.y_d = take(4 * M * D);
+  t.h_out = take(4 * M * D);
+  t.x_out = take(2 * M * D);
+  t.layer_bytes = off;
+  t.bytes = t.layer0 + (size_t)m->n_layers * t.layer_bytes;
+  return t;
+}
+
 }  // namespace
+
+size_t decode_trace_size(const kq_decode_model* m, int M) { return trace_layout(m, M).bytes; }
 
 int decode_check(const kq_decode_model* m, int M, std::string* err) {
   if (!m) { *err = "model is NULL"; return -1; }
@@ -257,8 +290,18 @@ int decode_check(const kq_decode_model* m, int M, std::string* err) {
 size_t decode_workspace_size(const kq_decode_model* m, int M) { return carve(m, M, nullptr).bytes; }
 
 int decode_step(const kq_decode_model* m, const uint16_t* x, float* logits, int M, void* ws, int num_sms,
-                cudaStream_t s, std::string* err) {
+                cudaStream_t s, std::string* err, void* trace) {
   const Ws w = carve(m, M, ws);
+  const TraceLayout tl = trace_layout(m, M);
+  // trace: after an op, a device-to-device copy of what it wrote (stream-ordered; the kernels
+  // and their arguments are those of the untraced step)
+  auto keep = [&](size_t off, const void* src, size_t bytes) -> int {
+    if (!trace) return 0;
+    const cudaError_t e = cudaMemcpyAsync(static_cast<uint8_t*>(trace) + off, src, bytes, cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) { *err = std::string("trace copy: ") + cudaGetErrorString(e); return -1; }
+    return 0;
+  };
+  const size_t MD = (size_t)M * m->hidden;
   const int qkv_dim = m->q_dim + 2 * m->kv_dim;
   const int group = (m->q_dim / m->head_dim) / (m->kv_dim / m->head_dim);
   auto rowb = [](int fmt, int K) { return (long long)kq_row_bytes(fmt, K); };
@@ -274,26 +317,36 @@ int decode_step(const kq_decode_model* m, const uint16_t* x, float* logits, int 
   if (ck(launch_pdl(add_rmsnorm_kernel, M, s, false, w.h, x, (const float*)nullptr, w.x, m->hidden, m->rms_eps),
          "add_rmsnorm"))
     return -1;
+  if (keep(tl.h0, w.h, 4 * MD) || keep(tl.x0, w.x, 2 * MD)) return -1;
   for (int l = 0; l < m->n_layers; ++l) {
+    const size_t L0 = tl.layer0 + (size_t)l * tl.layer_bytes;
     if (gemv(m->layer_fmt, m->w_qkv[l], w.x, w.qkv, qkv_dim, m->hidden)) return -1;
+    if (keep(L0 + tl.qkv, w.qkv, 4 * (size_t)M * qkv_dim)) return -1;
     if (ck(launch_pdl(gqa_expand_kernel, ew_grid((long long)M * m->q_dim), s, true, (const float*)w.qkv, w.x, M,
                       m->q_dim, m->kv_dim, m->head_dim, group),
            "gqa_expand"))
       return -1;
+    if (keep(L0 + tl.o_in, w.x, 2 * (size_t)M * m->q_dim)) return -1;
     if (gemv(m->layer_fmt, m->w_o[l], w.x, w.y, m->hidden, m->q_dim)) return -1;
+    if (keep(L0 + tl.y_o, w.y, 4 * MD)) return -1;
     if (ck(launch_pdl(add_rmsnorm_kernel, M, s, true, w.h, (const uint16_t*)nullptr, (const float*)w.y, w.x,
                       m->hidden, m->rms_eps),
            "add_rmsnorm"))
       return -1;
+    if (keep(L0 + tl.h_mid, w.h, 4 * MD) || keep(L0 + tl.x_mid, w.x, 2 * MD)) return -1;
     if (gemv(m->layer_fmt, m->w_gate_up[l], w.x, w.gu, 2 * m->ffn, m->hidden)) return -1;
+    if (keep(L0 + tl.gu, w.gu, 4 * (size_t)M * 2 * m->ffn)) return -1;
     if (ck(launch_pdl(swiglu_kernel, ew_grid((long long)M * m->ffn), s, true, (const float*)w.gu, w.x, M, m->ffn),
            "swiglu"))
       return -1;
+    if (keep(L0 + tl.act, w.x, 2 * (size_t)M * m->ffn)) return -1;
     if (gemv(m->layer_fmt, m->w_down[l], w.x, w.y, m->hidden, m->ffn)) return -1;
+    if (keep(L0 + tl.y_d, w.y, 4 * MD)) return -1;
     if (ck(launch_pdl(add_rmsnorm_kernel, M, s, true, w.h, (const uint16_t*)nullptr, (const float*)w.y, w.x,
                       m->hidden, m->rms_eps),
            "add_rmsnorm"))
       return -1;
+    if (keep(L0 + tl.h_out, w.h, 4 * MD) || keep(L0 + tl.x_out, w.x, 2 * MD)) return -1;
   }
   return gemv(m->head_fmt, m->w_head, w.x, logits, m->vocab, m->hidden);
 }

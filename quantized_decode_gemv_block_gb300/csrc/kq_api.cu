@@ -214,8 +214,28 @@ size_t kq_decode_workspace_size(const kq_decode_model* model, int M) {
   return kq::decode_workspace_size(model, M);
 }
 
+static int decode_step_impl(const kq_decode_model* model, const void* x, float* logits, int M, void* workspace,
+                            size_t ws_bytes, void* trace, size_t trace_bytes, void* stream);
+
 int kq_decode_step(const kq_decode_model* model, const void* x, float* logits, int M, void* workspace,
                    size_t ws_bytes, void* stream) {
+  return decode_step_impl(model, x, logits, M, workspace, ws_bytes, nullptr, 0, stream);
+}
+
+size_t kq_decode_trace_size(const kq_decode_model* model, int M) {
+  std::string err;
+  if (kq::decode_check(model, M, &err) != 0) return 0;
+  return kq::decode_trace_size(model, M);
+}
+
+int kq_decode_step_trace(const kq_decode_model* model, const void* x, float* logits, int M, void* workspace,
+                         size_t ws_bytes, void* trace, size_t trace_bytes, void* stream) {
+  if (!trace) return fail(KQ_ERR_ARG, "trace is NULL");
+  return decode_step_impl(model, x, logits, M, workspace, ws_bytes, trace, trace_bytes, stream);
+}
+
+static int decode_step_impl(const kq_decode_model* model, const void* x, float* logits, int M, void* workspace,
+                            size_t ws_bytes, void* trace, size_t trace_bytes, void* stream) {
   std::string err;
   if (kq::decode_check(model, M, &err) != 0) return fail(KQ_ERR_ARG, err);
   if (!fmt_known(model->layer_fmt) || !fmt_known(model->head_fmt))
@@ -231,10 +251,15 @@ int kq_decode_step(const kq_decode_model* model, const void* x, float* logits, i
       if (!p || !aligned(p, 16)) return fail(KQ_ERR_ARG, "layer " + std::to_string(l) + ": NULL or misaligned weights");
   }
   if (!aligned(model->w_head, 16)) return fail(KQ_ERR_ARG, "misaligned w_head");
+  if (trace) {
+    const size_t tneed = kq::decode_trace_size(model, M);
+    if (trace_bytes < tneed || !aligned(trace, 256))
+      return fail(KQ_ERR_ARG, "trace must be >= " + std::to_string(tneed) + " bytes, 256-byte aligned");
+  }
   const int sms = sm_count(&err);
   if (sms < 0) return fail(KQ_ERR_CUDA, err);
   if (kq::decode_step(model, static_cast<const uint16_t*>(x), logits, M, workspace, sms,
-                      static_cast<cudaStream_t>(stream), &err) != 0)
+                      static_cast<cudaStream_t>(stream), &err, trace) != 0)
     return fail(KQ_ERR_CUDA, err);
   return ok();
 }
@@ -399,13 +424,33 @@ int kq_head_argmax(const void* w_q8, const void* shortlist, int x_dtype, const v
 // ---- Decode step with library-owned scratch (kq_decode_step_static) ----
 // The scratch lives in one file-scope device array, so no call allocates. Host code may
 // not use the array's name as a device address (on the host it names a stand-in object):
-// the address comes from cudaGetSymbolAddress, looked up once per device by the first
-// call on that device (with that device current) and cached.
+// the address comes from cudaGetSymbolAddress, looked up by the first call on a device
+// (with that device current) and cached together with the context that was current. A
+// context torn down and created again (cudaDeviceReset) loads the module afresh and the
+// array may move, so a call that finds a different current context looks it up again.
 static __device__ __align__(256) unsigned char g_decode_scratch[KQ_DECODE_STATIC_SCRATCH_BYTES];
 
 namespace {
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[64] = {nullptr};
+void* g_scratch_ctx[64] = {nullptr};
+
+// The driver's cuCtxGetCurrent, reached through the runtime (the library does not link
+// libcuda directly); null if the entry point cannot be found.
+using CtxGetCurrentFn = int (*)(void**);
+CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = nullptr;
+  static bool looked = false;
+  if (!looked) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    looked = true;
+  }
+  return fn;
+}
 }  // namespace
 
 int kq_decode_step_static(const kq_decode_model* model, const void* x, float* logits, int M, void* stream) {
@@ -434,12 +479,17 @@ int kq_decode_step_static(const kq_decode_model* model, const void* x, float* lo
   void* scratch = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
+    void* ctx = nullptr;
+    const CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+    if (get_ctx && get_ctx(&ctx) != 0) ctx = nullptr;
+    if (!g_scratch_ptr[dev] || !ctx || ctx != g_scratch_ctx[dev]) {
       void* p = nullptr;
-      e = cudaGetSymbolAddress(&p, g_decode_scratch);
+      e = cudaGetSymbolAddress(&p, g_decode_scratch);  // makes the primary context current if none is
       if (e != cudaSuccess || !p)
         return fail(KQ_ERR_CUDA, std::string("cudaGetSymbolAddress of the decode scratch: ") + cudaGetErrorString(e));
+      if (get_ctx && get_ctx(&ctx) != 0) ctx = nullptr;
       g_scratch_ptr[dev] = p;
+      g_scratch_ctx[dev] = ctx;  // null (context unknown): looked up again on every call
     }
     scratch = g_scratch_ptr[dev];
   }

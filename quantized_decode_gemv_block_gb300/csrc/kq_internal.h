@@ -65,8 +65,10 @@ size_t decode_workspace_size(const kq_decode_model* m, int M);
 size_t decode_attn_workspace_size(const kq_decode_model* m, int M, int L);
 int decode_step_attn(const kq_decode_model* m, const kq_kv_cache* c, const uint16_t* x, float* logits, int M,
                      const uint32_t* mask, void* ws, int num_sms, cudaStream_t s, std::string* err);
+// trace: null, or decode_trace_size(m, M) bytes that receive a copy of every op's output
 int decode_step(const kq_decode_model* m, const uint16_t* x, float* logits, int M, void* ws, int num_sms,
-                cudaStream_t s, std::string* err);
+                cudaStream_t s, std::string* err, void* trace = nullptr);
+size_t decode_trace_size(const kq_decode_model* m, int M);
 
 // Decode attention of a verify window over a KV cache (attention.cu).
 size_t attention_workspace(int M, int L, int n_q, int n_kv, int hd);

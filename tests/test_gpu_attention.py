@@ -100,3 +100,21 @@ def test_window_equals_one_token_at_a_time(built, M, L, hd):
     for i in range(M):
         o = run(q[i:i + 1], k[:L + i + 1], v[:L + i + 1], L + i, n_q, n_kv, hd, 0.0883)
         assert np.array_equal(o.view(np.uint32), win[i:i + 1].view(np.uint32)), f"token {i}"
+
+
+def test_extreme_finite_values_in_a_later_guess_leave_earlier_tokens_unchanged(built):
+    """A later guess's key and value rows at the largest finite bf16 magnitude (0x7F7F, about
+    3.39e38) enter the chunk's products with weight 0 for the earlier tokens: those tokens keep
+    the bits they get decoded alone. (Non-finite keys or values are outside the guarantee, as
+    the header states: 0 * Inf is NaN.)"""
+    M, L, n_q, n_kv, hd = 4, 130, 16, 4, 128
+    q, k, v = make(M, L, n_q, n_kv, hd, seed=21)
+    k = k.copy()
+    v = v.copy()
+    k[L + 3, ::2] = 0x7F7F   # +max finite bf16 in half of the last guess's key
+    v[L + 3, ::3] = 0xFF7F   # -max finite bf16 in a third of its value
+    win = run(q, k, v, L, n_q, n_kv, hd, 0.0883)
+    assert np.all(np.isfinite(win[:3]))
+    for i in range(3):
+        o = run(q[i:i + 1], k[:L + i + 1], v[:L + i + 1], L + i, n_q, n_kv, hd, 0.0883)
+        assert np.array_equal(o.view(np.uint32), win[i:i + 1].view(np.uint32)), f"token {i}"

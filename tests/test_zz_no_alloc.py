@@ -58,3 +58,22 @@ def test_static_scratch_refuses_models_beyond_its_size(kq):
     rc = kq.lib().kq_decode_step_static(ctypes.byref(model.c), x.data_ptr(), out.data_ptr(), 16, None)
     assert rc == kq.KQ_ERR_WORKSPACE
     assert "static scratch" in kq.lib().kq_last_error().decode()
+
+
+def test_static_scratch_holds_the_dense_28_layer_model_at_16_tokens(kq):
+    """The 4 MiB array is sized for the dense 28-layer decoder (hidden 2048, ffn 6144, vocab
+    151936) up to 16 tokens: its step runs from the array and gives kq_decode_step's bits."""
+    from quantized_decode_gemv_block_gb300 import decode as kqd
+    model = kqd.random_model(kqd.DENSE_28L, seed=9)
+    M = 16
+    assert model.workspace_size(M) <= 4 * 2**20
+    x = torch.randn((M, kqd.DENSE_28L["hidden"]), device="cuda").to(torch.bfloat16)
+    ref = model.step(x).clone()
+    out = torch.full((M, kqd.DENSE_28L["vocab"]), float("nan"), device="cuda")
+    L = kq.lib()
+    rc = L.kq_decode_step_static(ctypes.byref(model.c), x.data_ptr(), out.data_ptr(), M,
+                                 torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, L.kq_last_error().decode()
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.cpu().numpy().view(np.uint32))
+    assert kq.device_errors() == 0
