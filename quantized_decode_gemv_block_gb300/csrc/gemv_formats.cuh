@@ -479,40 +479,55 @@ struct FmtQ4KH {
     }
   }
 
-  // acc += d*ps - 64*dmin*mn, rows g (elements 0, 1) and g+8 (elements 2, 3)
+  // acc += (d*ps - 64*dmin*mn) * 2^-e, rows g (elements 0, 1) and g+8 (elements 2, 3); iv[t]
+  // holds 2^-e of this super-block's activations for the thread's tokens 8t+2q and 8t+2q+1
+  // (the products above are in units of 2^e; removing it is exact unless the result is
+  // subnormal)
   template <int NT>
   __device__ static void promote(float (&acc)[NT][4], const float (&ps)[NT][4], const float (&mnv)[NT][4],
-                                 const float (&d)[2], const float (&dmin)[2]) {
+                                 const float (&d)[2], const float (&dmin)[2], const float2 (&iv)[NT]) {
     const float nd0 = -64.f * dmin[0], nd1 = -64.f * dmin[1];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-      acc[t][0] = __fmaf_rn(nd0, mnv[t][0], __fmaf_rn(d[0], ps[t][0], acc[t][0]));
-      acc[t][1] = __fmaf_rn(nd0, mnv[t][1], __fmaf_rn(d[0], ps[t][1], acc[t][1]));
-      acc[t][2] = __fmaf_rn(nd1, mnv[t][2], __fmaf_rn(d[1], ps[t][2], acc[t][2]));
-      acc[t][3] = __fmaf_rn(nd1, mnv[t][3], __fmaf_rn(d[1], ps[t][3], acc[t][3]));
+      acc[t][0] = __fmaf_rn(__fmaf_rn(d[0], ps[t][0], nd0 * mnv[t][0]), iv[t].x, acc[t][0]);
+      acc[t][1] = __fmaf_rn(__fmaf_rn(d[0], ps[t][1], nd0 * mnv[t][1]), iv[t].y, acc[t][1]);
+      acc[t][2] = __fmaf_rn(__fmaf_rn(d[1], ps[t][2], nd1 * mnv[t][2]), iv[t].x, acc[t][2]);
+      acc[t][3] = __fmaf_rn(__fmaf_rn(d[1], ps[t][3], nd1 * mnv[t][3]), iv[t].y, acc[t][3]);
     }
   }
 
+  // iv_unit: 2^-e of token 0 for this super-block (16 tokens per super-block, 16 floats apart);
+  // io[t]: this thread's first token of tile t within it (8t + 2q)
   template <int NT>
   __device__ static void compute(const Raw& r, float (&acc)[NT][4], const uint8_t* xh_unit,
                                  const int (&xo)[NT], const uint8_t* s2_unit, const int (&so)[NT],
-                                 int lane) {
+                                 const float* iv_unit, const int (&io)[NT], int lane) {
     float ps[NT][4], mnv[NT][4], d[2], dmin[2];
+    float2 iv[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) iv[t] = lds_f2(iv_unit + io[t]);
     sums<NT>(r, xh_unit, xo, s2_unit, so, lane, ps, mnv, d, dmin);
-    promote<NT>(acc, ps, mnv, d, dmin);
+    promote<NT>(acc, ps, mnv, d, dmin, iv);
   }
 
   // Two consecutive super-blocks (x and min-term operands of the second 512 and 32 bytes
-  // further on); the same arithmetic, in the same order, as two compute() calls.
+  // further on, scales 16 floats on); the same arithmetic, in the same order, as two
+  // compute() calls.
   template <int NT>
   __device__ static void compute2(const Raw& r0, const Raw& r1, float (&acc)[NT][4],
                                   const uint8_t* xh_unit, const int (&xo)[NT], const uint8_t* s2_unit,
-                                  const int (&so)[NT], int lane) {
+                                  const int (&so)[NT], const float* iv_unit, const int (&io)[NT], int lane) {
     float ps0[NT][4], mn0[NT][4], d0[2], dm0[2], ps1[NT][4], mn1[NT][4], d1[2], dm1[2];
+    float2 iv0[NT], iv1[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      iv0[t] = lds_f2(iv_unit + io[t]);
+      iv1[t] = lds_f2(iv_unit + 16 + io[t]);
+    }
     sums<NT>(r0, xh_unit, xo, s2_unit, so, lane, ps0, mn0, d0, dm0);
     sums<NT>(r1, xh_unit + 512, xo, s2_unit + 32, so, lane, ps1, mn1, d1, dm1);
-    promote<NT>(acc, ps0, mn0, d0, dm0);
-    promote<NT>(acc, ps1, mn1, d1, dm1);
+    promote<NT>(acc, ps0, mn0, d0, dm0, iv0);
+    promote<NT>(acc, ps1, mn1, d1, dm1, iv1);
   }
 };
 
@@ -642,48 +657,64 @@ struct FmtQ5KH {
     }
   }
 
-  // acc += d*ps - 64*dmin*mn, rows g (elements 0, 1) and g+8 (elements 2, 3)
+  // acc += (d*ps - 64*dmin*mn) * 2^-e, rows g (elements 0, 1) and g+8 (elements 2, 3); iv[t]
+  // holds 2^-e of this super-block's activations for the thread's tokens 8t+2q and 8t+2q+1
+  // (the products above are in units of 2^e; removing it is exact unless the result is
+  // subnormal)
   template <int NT>
   __device__ static void promote(float (&acc)[NT][4], const float (&ps)[NT][4], const float (&mnv)[NT][4],
-                                 const float (&d)[2], const float (&dmin)[2]) {
+                                 const float (&d)[2], const float (&dmin)[2], const float2 (&iv)[NT]) {
     const float nd0 = -64.f * dmin[0], nd1 = -64.f * dmin[1];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-      acc[t][0] = __fmaf_rn(nd0, mnv[t][0], __fmaf_rn(d[0], ps[t][0], acc[t][0]));
-      acc[t][1] = __fmaf_rn(nd0, mnv[t][1], __fmaf_rn(d[0], ps[t][1], acc[t][1]));
-      acc[t][2] = __fmaf_rn(nd1, mnv[t][2], __fmaf_rn(d[1], ps[t][2], acc[t][2]));
-      acc[t][3] = __fmaf_rn(nd1, mnv[t][3], __fmaf_rn(d[1], ps[t][3], acc[t][3]));
+      acc[t][0] = __fmaf_rn(__fmaf_rn(d[0], ps[t][0], nd0 * mnv[t][0]), iv[t].x, acc[t][0]);
+      acc[t][1] = __fmaf_rn(__fmaf_rn(d[0], ps[t][1], nd0 * mnv[t][1]), iv[t].y, acc[t][1]);
+      acc[t][2] = __fmaf_rn(__fmaf_rn(d[1], ps[t][2], nd1 * mnv[t][2]), iv[t].x, acc[t][2]);
+      acc[t][3] = __fmaf_rn(__fmaf_rn(d[1], ps[t][3], nd1 * mnv[t][3]), iv[t].y, acc[t][3]);
     }
   }
 
+  // iv_unit: 2^-e of token 0 for this super-block (16 tokens per super-block, 16 floats apart);
+  // io[t]: this thread's first token of tile t within it (8t + 2q)
   template <int NT>
   __device__ static void compute(const Raw& r, float (&acc)[NT][4], const uint8_t* xh_unit,
                                  const int (&xo)[NT], const uint8_t* s2_unit, const int (&so)[NT],
-                                 int lane) {
+                                 const float* iv_unit, const int (&io)[NT], int lane) {
     float ps[NT][4], mnv[NT][4], d[2], dmin[2];
+    float2 iv[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) iv[t] = lds_f2(iv_unit + io[t]);
     sums<NT>(r, xh_unit, xo, s2_unit, so, lane, ps, mnv, d, dmin);
-    promote<NT>(acc, ps, mnv, d, dmin);
+    promote<NT>(acc, ps, mnv, d, dmin, iv);
   }
 
   // Two consecutive super-blocks (x and min-term operands of the second 512 and 32 bytes
-  // further on); the same arithmetic, in the same order, as two compute() calls.
+  // further on, scales 16 floats on); the same arithmetic, in the same order, as two
+  // compute() calls.
   template <int NT>
   __device__ static void compute2(const Raw& r0, const Raw& r1, float (&acc)[NT][4],
                                   const uint8_t* xh_unit, const int (&xo)[NT], const uint8_t* s2_unit,
-                                  const int (&so)[NT], int lane) {
+                                  const int (&so)[NT], const float* iv_unit, const int (&io)[NT], int lane) {
     float ps0[NT][4], mn0[NT][4], d0[2], dm0[2], ps1[NT][4], mn1[NT][4], d1[2], dm1[2];
+    float2 iv0[NT], iv1[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      iv0[t] = lds_f2(iv_unit + io[t]);
+      iv1[t] = lds_f2(iv_unit + 16 + io[t]);
+    }
     sums<NT>(r0, xh_unit, xo, s2_unit, so, lane, ps0, mn0, d0, dm0);
     sums<NT>(r1, xh_unit + 512, xo, s2_unit + 32, so, lane, ps1, mn1, d1, dm1);
-    promote<NT>(acc, ps0, mn0, d0, dm0);
-    promote<NT>(acc, ps1, mn1, d1, dm1);
+    promote<NT>(acc, ps0, mn0, d0, dm0, iv0);
+    promote<NT>(acc, ps1, mn1, d1, dm1, iv1);
   }
 };
 
-// Stage the activations of one CTA's K-slice for FmtQ4KH (all threads of the CTA take
-// part; two __syncthreads inside). x: M x K bf16. Slice = units [k0, k0+S).
-// smax/inv: T-entry scratch in shared memory (max |x| bits, then 2^-e per token).
-// Per-token power-of-two scale 2^e with max|x| * 2^e in [2^14, 2^15), from the bits of
-// max|x| (an fp32 pattern); zero, Inf and NaN keep 2^0.
+// Staging of one CTA's K-slice of the activations for FmtQ4KH / FmtQ5KH (all threads of the
+// CTA take part). x: M x K bf16. Slice = super-blocks [k0, k0+S).
+// Every (token, super-block) gets its own power-of-two scale 2^e with max|x| * 2^e in
+// [2^14, 2^15) over its 256 values (from the bits of max|x|, an fp32 pattern; zero, Inf and
+// NaN keep 2^0): every bf16 value within a factor 2^28 of that maximum converts to fp16
+// exactly, and the scale depends on the token's own values only (never on M).
 __device__ __forceinline__ float token_scale(uint32_t mb) {
   const int E = static_cast<int>(mb >> 23);
   int e = 0;
@@ -694,19 +725,21 @@ __device__ __forceinline__ float token_scale(uint32_t mb) {
   return __int_as_float((e + 127) << 23);
 }
 
-// Activation staging for FmtQ4KH in two phases, so the loads of x leave before the
-// weight copies flood the memory system: load() reads this thread's items into
-// registers (and clears the zero row and the maxima); finish() reduces the per-token
-// maxima, converts, stores, and writes the min-term operands. The caller places one
-// __syncthreads between them (and one after finish()).
+// Two phases, so the loads of x leave before any conversion work: load() reads this thread's
+// items into registers (and clears the zero row and the scales of absent tokens); finish()
+// takes each (token, super-block) maximum across the eight lanes that hold its 256 values
+// (no shared-memory atomics, no barrier), converts, stores, and writes the min-term operands
+// and 2^-e. The caller places one __syncthreads after finish().
 // Rows 0..M-1 of the staged x hold the tokens, row M zeros (absent token slots read it).
+// iv: 2^-e per (super-block, token), 16 floats per super-block.
 template <int NTHREADS>
 struct StageQ4KH {
-  static constexpr int kItems = 5;  // 16 tokens x 10 units x 8 groups / 256 threads
+  static_assert(NTHREADS % 32 == 0, "an item's eight lanes must share a warp");
+  static constexpr int kItems = 5;  // 16 tokens x 10 super-blocks x 8 groups / 256 threads
   uint4 u[kItems][4];
 
   __device__ void load(const uint16_t* x, int M, int K, int k0, int S, uint8_t* xh, int xts, uint8_t* s2,
-                       int s2ts, unsigned int* smax) {
+                       int s2ts, float* iv) {
     const int items = M * S * 8;
 #pragma unroll
     for (int it = 0; it < kItems; ++it) {
@@ -722,36 +755,35 @@ struct StageQ4KH {
       *reinterpret_cast<uint4*>(xh + M * xts + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
     for (int i = threadIdx.x; i < S * 4; i += NTHREADS)
       *reinterpret_cast<uint2*>(s2 + M * s2ts + 8 * i) = make_uint2(0u, 0u);
-    for (int t = threadIdx.x; t < M; t += NTHREADS) smax[t] = 0u;
+    for (int i = threadIdx.x; i < S * 16; i += NTHREADS)
+      if ((i & 15) >= M) iv[i] = 0.f;
   }
 
-  __device__ void finish(int M, int S, uint8_t* xh, int xts, uint8_t* s2, int s2ts, unsigned int* smax,
-                         float* inv) {
+  __device__ void finish(int M, int S, uint8_t* xh, int xts, uint8_t* s2, int s2ts, float* iv) {
     const int items = M * S * 8;
 #pragma unroll
     for (int it = 0; it < kItems; ++it) {
+      if (it * NTHREADS >= items) break;  // uniform over the CTA
       const int idx = threadIdx.x + it * NTHREADS;
-      if (idx < items) {
-        const int tok = idx / (S * 8);
-        uint32_t best = 0u;
+      const bool act = idx < items;
+      uint32_t best = 0u;
+      if (act) {
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           const uint32_t w4[4] = {u[it][v].x, u[it][v].y, u[it][v].z, u[it][v].w};
 #pragma unroll
           for (int k = 0; k < 4; ++k) best = max(best, max((w4[k] & 0x7FFFu) << 16, w4[k] & 0x7FFF0000u));
         }
-        atomicMax(&smax[tok], best);
       }
-    }
-    __syncthreads();
-    for (int t = threadIdx.x; t < M; t += NTHREADS) inv[t] = 1.0f / token_scale(smax[t]);
-#pragma unroll
-    for (int it = 0; it < kItems; ++it) {
-      const int idx = threadIdx.x + it * NTHREADS;
-      if (idx < items) {
+      // lanes 8a..8a+7 hold groups 0..7 of one (token, super-block): S * 8 items per token
+      best = max(best, __shfl_xor_sync(0xFFFFFFFFu, best, 1));
+      best = max(best, __shfl_xor_sync(0xFFFFFFFFu, best, 2));
+      best = max(best, __shfl_xor_sync(0xFFFFFFFFu, best, 4));
+      if (act) {
         const int tok = idx / (S * 8), grp = idx - tok * (S * 8);
         const int ul = grp >> 3, j = grp & 7, q = j >> 1, half = j & 1;
-        const float sc = token_scale(smax[tok]);
+        const float sc = token_scale(best);
+        if (j == 0) iv[ul * 16 + tok] = 1.0f / sc;  // exact: a power of two
         float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int v = 0; v < 4; ++v) {

@@ -255,6 +255,7 @@ int launch_chunked(const Params& prm, size_t smem, cudaStream_t stream, std::str
 // are added in rank order (= K order). Every cut depends on (N, K, SM count) only.
 // ============================================================================
 constexpr int kMaxSliceUnits = 10;     // K-units of activations a CTA stages
+constexpr int kAuxScaleBytes = kMaxSliceUnits * 16 * 4;  // 2^-e per (staged unit, token)
 constexpr int kMaxClusterTiles = 32;   // tiles per cluster when partials meet across CTAs
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded waits give up after 2 s
 
@@ -281,8 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
   float* pbuf = reinterpret_cast<float*>(smem + p.off_pb);  // [warp][2][16][T]
   float* res = reinterpret_cast<float*>(smem + p.off_res);  // [tile][16][T], C > 1
-  unsigned int* smax = reinterpret_cast<unsigned int*>(smem + p.off_aux);
-  float* inv = reinterpret_cast<float*>(smem + p.off_aux + 64);
+  float* ivs = reinterpret_cast<float*>(smem + p.off_aux);  // [super-block][16]: 2^-e (fp16 path)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
@@ -336,11 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   [[maybe_unused]] StageQ4KH<kThreads> stq;
   if constexpr (F::kHalfX) {
-    if (S > 0) stq.load(p.x, p.M, p.K, k0, S, smem, p.xts, smem + p.off_ss, p.s2ts, smax);
+    if (S > 0) stq.load(p.x, p.M, p.K, k0, S, smem, p.xts, smem + p.off_ss, p.s2ts, ivs);
   }
 
   // This warp's first and last tile, and whether each is partial (kept for the combine).
-  int* meta = reinterpret_cast<int*>(smem + p.off_aux + 128);  // [warp][4]
+  int* meta = reinterpret_cast<int*>(smem + p.off_aux + kAuxScaleBytes);  // [warp][4]
   const int w_first = l0 / fdiv, w_last = l1 > l0 ? (l1 - 1) / fdiv : -1;
   if (lane == 0) {
     meta[warp * 4 + 0] = l1 > l0 ? w_first : -1;
@@ -349,15 +349,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     meta[warp * 4 + 3] = (l1 > l0) && !(w_last * S >= l0 && (w_last + 1) * S <= l1);    // last partial
   }
 
-  int xo[NT], so[NT];  // this thread's token rows in the staged activations (fp16 path)
+  int xo[NT], so[NT], io[NT];  // this thread's token rows in the staged activations (fp16 path)
   if constexpr (F::kHalfX) {
-    __syncthreads();
-    if (S > 0) stq.finish(p.M, S, smem, p.xts, smem + p.off_ss, p.s2ts, smax, inv);
+    if (S > 0) stq.finish(p.M, S, smem, p.xts, smem + p.off_ss, p.s2ts, ivs);
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const int tok = 8 * t + g, row = tok < p.M ? tok : p.M;
       xo[t] = row * p.xts + 16 * q;
       so[t] = row * p.s2ts + 8 * q;
+      io[t] = 8 * t + 2 * q;
     }
   } else {
     if (S > 0) stage_x<F, T>(p.x, p.M, p.K, p.xstride, xs, ss, k0, S);
@@ -368,19 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
   for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
 
-  // a finished CTA partial of local tile tl (fp16 path: still in 2^e-scaled units)
+  // a finished CTA partial of local tile tl
   auto emit = [&](int tl, float (&a)[NT][4]) {
-    if constexpr (F::kHalfX) {
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const int j0 = 8 * t + 2 * q;
-        const float i0 = j0 < p.M ? inv[j0] : 0.f, i1 = j0 + 1 < p.M ? inv[j0 + 1] : 0.f;
-        a[t][0] *= i0;
-        a[t][1] *= i1;
-        a[t][2] *= i0;
-        a[t][3] *= i1;
-      }
-    }
     if (p.C == 1) {
       const int na = (t0 + tl) * 16 + g, nb = na + 8;
 #pragma unroll
@@ -430,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           F::template load<LdShared>(r0, sa + i * p.unit_bytes, sb + i * p.unit_bytes, q);
           F::template load<LdShared>(r1, sa + (i + 1) * p.unit_bytes, sb + (i + 1) * p.unit_bytes, q);
           F::template compute2<NT>(r0, r1, acc, smem + (ul + i) * 512, xo,
-                                   smem + p.off_ss + (ul + i) * 32, so, lane);
+                                   smem + p.off_ss + (ul + i) * 32, so, ivs + (ul + i) * 16, io, lane);
         }
       }
       for (; i < nu; ++i) {
@@ -438,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         F::template load<LdShared>(raw, sa + i * p.unit_bytes, sb + i * p.unit_bytes, q);
         if constexpr (F::kHalfX)
           F::template compute<NT>(raw, acc, smem + (ul + i) * 512, xo, smem + p.off_ss + (ul + i) * 32,
-                                  so, lane);
+                                  so, ivs + (ul + i) * 16, io, lane);
         else
           F::template compute<NT>(raw, acc, xs + (ul + i) * kUnit, p.xstride, ss + (ul + i) * 8 * T,
                                   lane, p.M);
@@ -497,7 +486,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int slot = meta[ww * 4 + 0] == t ? 0 : 1;
         v += pbuf[((size_t)(ww * 2 + slot) * 16 + row) * T + tok];
       }
-      if constexpr (F::kHalfX) v *= inv[tok];
       if (p.C == 1) {
         const int n = (t0 + t) * 16 + row;
         if (n < p.N) p.y[(long long)tok * p.N + n] = v;
@@ -602,7 +590,7 @@ bool tma_layout(int fmt, const TmaPlan& pl, int M, TmaParams* prm, size_t* smem)
   const size_t off_ss = off;
   off = al(off + sbytes);
   const size_t off_aux = off;
-  off = al(off + 64 + 64 + 128);
+  off = al(off + kAuxScaleBytes + 128);
   const size_t off_pb = off;
   off = al(off + (size_t)kWarps * 2 * 16 * T * 4);
   const size_t off_res = off;
