@@ -173,9 +173,7 @@ __global__ void __launch_bounds__(kGlueThreads) swiglu_kernel(const float* __res
   for (long long e = blockIdx.x * (long long)kGlueThreads + threadIdx.x; e < total;
        e += (long long)gridDim.x * kGlueThreads) {
     const int j = (int)(e / F), i = (int)(e - (long long)j * F);
-    const float g = gu[(long long)j * 2 * F + i], u = gu[(long long)j * 2 * F + F + i];
-    const float s = g / (1.0f + expf(-g));
-    out[e] = f2bf(s * u);
+    out[e] = silu_mul_bf16(gu[(long long)j * 2 * F + i], gu[(long long)j * 2 * F + F + i]);
   }
 }
 
@@ -215,6 +213,7 @@ size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
 struct Ws {  // workspace carve-up
   float* h;     // M x hidden      residual stream
   uint16_t* x;  // M x max(hidden, q_dim, ffn) bf16 GEMV input
+  uint16_t* x2; // M x max(q_dim, ffn) bf16: the input of Wo and of the down projection
   float* qkv;   // M x (q_dim + 2 kv_dim)
   float* y;     // M x hidden      o / down outputs
   float* gu;    // M x 2 ffn
@@ -232,6 +231,7 @@ Ws carve(const kq_decode_model* m, int M, void* base) {
   };
   w.h = static_cast<float*>(take(sizeof(float) * (size_t)M * m->hidden));
   w.x = static_cast<uint16_t*>(take(sizeof(uint16_t) * (size_t)M * xw));
+  w.x2 = static_cast<uint16_t*>(take(sizeof(uint16_t) * (size_t)M * std::max(m->q_dim, m->ffn)));
   w.qkv = static_cast<float*>(take(sizeof(float) * (size_t)M * (m->q_dim + 2 * m->kv_dim)));
   w.y = static_cast<float*>(take(sizeof(float) * (size_t)M * m->hidden));
   w.gu = static_cast<float*>(take(sizeof(float) * (size_t)M * 2 * m->ffn));
@@ -310,9 +310,25 @@ int decode_step(const kq_decode_model* m, const uint16_t* x, float* logits, int 
     if (e != cudaSuccess) { *err = std::string(what) + ": " + cudaGetErrorString(e); return -1; }
     return 0;
   };
-  auto gemv = [&](int fmt, const void* wt, const uint16_t* xin, float* y, int N, int K) {
-    return launch_gemv_mma(fmt, wt, xin, y, M, N, K, rowb(fmt, K), num_sms, s, true, err);
+  auto gemv = [&](int fmt, const void* wt, const uint16_t* xin, float* y, int N, int K,
+                  const GemvEpilogue* epi = nullptr) {
+    return launch_gemv_mma(fmt, wt, xin, y, M, N, K, rowb(fmt, K), num_sms, s, true, err, epi);
   };
+  // The attention stand-in and the SwiGLU run inside the GEMVs that produce their inputs when
+  // the streaming kernel takes those shapes (its epilogue writes the bf16 input of Wo, resp. of
+  // the down projection); otherwise as separate kernels. Both give the same bits.
+  GemvEpilogue expand, swiglu;
+  expand.kind = 1;
+  expand.out = w.x2;
+  expand.v0 = m->q_dim + m->kv_dim;
+  expand.vn = m->kv_dim;
+  expand.hd = m->head_dim;
+  expand.group = group;
+  expand.out_w = m->q_dim;
+  swiglu.kind = 2;
+  swiglu.out = w.x2;
+  const bool fuse_expand = gemv_epilogue_ok(m->layer_fmt, qkv_dim, m->hidden, 1, num_sms);
+  const bool fuse_swiglu = gemv_epilogue_ok(m->layer_fmt, 2 * m->ffn, m->hidden, 2, num_sms);
   // h = x (bf16 -> fp32); x_norm = RMSNorm(h)
   if (ck(launch_pdl(add_rmsnorm_kernel, M, s, false, w.h, x, (const float*)nullptr, w.x, m->hidden, m->rms_eps),
          "add_rmsnorm"))
@@ -320,27 +336,33 @@ int decode_step(const kq_decode_model* m, const uint16_t* x, float* logits, int 
   if (keep(tl.h0, w.h, 4 * MD) || keep(tl.x0, w.x, 2 * MD)) return -1;
   for (int l = 0; l < m->n_layers; ++l) {
     const size_t L0 = tl.layer0 + (size_t)l * tl.layer_bytes;
-    if (gemv(m->layer_fmt, m->w_qkv[l], w.x, w.qkv, qkv_dim, m->hidden)) return -1;
+    if (gemv(m->layer_fmt, m->w_qkv[l], w.x, w.qkv, qkv_dim, m->hidden, fuse_expand ? &expand : nullptr)) return -1;
     if (keep(L0 + tl.qkv, w.qkv, 4 * (size_t)M * qkv_dim)) return -1;
-    if (ck(launch_pdl(gqa_expand_kernel, ew_grid((long long)M * m->q_dim), s, true, (const float*)w.qkv, w.x, M,
+    if (!fuse_expand &&
+        ck(launch_pdl(gqa_expand_kernel, ew_grid((long long)M * m->q_dim), s, true, (const float*)w.qkv, w.x2, M,
                       m->q_dim, m->kv_dim, m->head_dim, group),
            "gqa_expand"))
       return -1;
-    if (keep(L0 + tl.o_in, w.x, 2 * (size_t)M * m->q_dim)) return -1;
-    if (gemv(m->layer_fmt, m->w_o[l], w.x, w.y, m->hidden, m->q_dim)) return -1;
+    if (keep(L0 + tl.o_in, w.x2, 2 * (size_t)M * m->q_dim)) return -1;
+    if (gemv(m->layer_fmt, m->w_o[l], w.x2, w.y, m->hidden, m->q_dim)) return -1;
     if (keep(L0 + tl.y_o, w.y, 4 * MD)) return -1;
     if (ck(launch_pdl(add_rmsnorm_kernel, M, s, true, w.h, (const uint16_t*)nullptr, (const float*)w.y, w.x,
                       m->hidden, m->rms_eps),
            "add_rmsnorm"))
       return -1;
     if (keep(L0 + tl.h_mid, w.h, 4 * MD) || keep(L0 + tl.x_mid, w.x, 2 * MD)) return -1;
-    if (gemv(m->layer_fmt, m->w_gate_up[l], w.x, w.gu, 2 * m->ffn, m->hidden)) return -1;
-    if (keep(L0 + tl.gu, w.gu, 4 * (size_t)M * 2 * m->ffn)) return -1;
-    if (ck(launch_pdl(swiglu_kernel, ew_grid((long long)M * m->ffn), s, true, (const float*)w.gu, w.x, M, m->ffn),
-           "swiglu"))
-      return -1;
-    if (keep(L0 + tl.act, w.x, 2 * (size_t)M * m->ffn)) return -1;
-    if (gemv(m->layer_fmt, m->w_down[l], w.x, w.y, m->hidden, m->ffn)) return -1;
+    if (fuse_swiglu) {  // gate|up outputs in fp32 only when traced
+      if (gemv(m->layer_fmt, m->w_gate_up[l], w.x, trace ? w.gu : nullptr, 2 * m->ffn, m->hidden, &swiglu)) return -1;
+      if (keep(L0 + tl.gu, w.gu, 4 * (size_t)M * 2 * m->ffn)) return -1;
+    } else {
+      if (gemv(m->layer_fmt, m->w_gate_up[l], w.x, w.gu, 2 * m->ffn, m->hidden)) return -1;
+      if (keep(L0 + tl.gu, w.gu, 4 * (size_t)M * 2 * m->ffn)) return -1;
+      if (ck(launch_pdl(swiglu_kernel, ew_grid((long long)M * m->ffn), s, true, (const float*)w.gu, w.x2, M, m->ffn),
+             "swiglu"))
+        return -1;
+    }
+    if (keep(L0 + tl.act, w.x2, 2 * (size_t)M * m->ffn)) return -1;
+    if (gemv(m->layer_fmt, m->w_down[l], w.x2, w.y, m->hidden, m->ffn)) return -1;
     if (keep(L0 + tl.y_d, w.y, 4 * MD)) return -1;
     if (ck(launch_pdl(add_rmsnorm_kernel, M, s, true, w.h, (const uint16_t*)nullptr, (const float*)w.y, w.x,
                       m->hidden, m->rms_eps),
@@ -369,9 +391,14 @@ int decode_step_attn(const kq_decode_model* m, const kq_kv_cache* c, const uint1
     if (e != cudaSuccess) { *err = std::string(what) + ": " + cudaGetErrorString(e); return -1; }
     return 0;
   };
-  auto gemv = [&](int fmt, const void* wt, const uint16_t* xin, float* y, int N, int K) {
-    return launch_gemv_mma(fmt, wt, xin, y, M, N, K, rowb(fmt, K), num_sms, s, true, err);
+  auto gemv = [&](int fmt, const void* wt, const uint16_t* xin, float* y, int N, int K,
+                  const GemvEpilogue* epi = nullptr) {
+    return launch_gemv_mma(fmt, wt, xin, y, M, N, K, rowb(fmt, K), num_sms, s, true, err, epi);
   };
+  GemvEpilogue swiglu;  // the SwiGLU inside the gate|up GEMV when its plan allows (see decode_step)
+  swiglu.kind = 2;
+  swiglu.out = w.x2;
+  const bool fuse_swiglu = gemv_epilogue_ok(m->layer_fmt, 2 * m->ffn, m->hidden, 2, num_sms);
   if (ck(launch_pdl(add_rmsnorm_kernel, M, s, false, w.h, x, (const float*)nullptr, w.x, m->hidden, m->rms_eps),
          "add_rmsnorm"))
     return -1;
@@ -392,11 +419,15 @@ int decode_step_attn(const kq_decode_model* m, const kq_kv_cache* c, const uint1
                       m->hidden, m->rms_eps),
            "add_rmsnorm"))
       return -1;
-    if (gemv(m->layer_fmt, m->w_gate_up[l], w.x, w.gu, 2 * m->ffn, m->hidden)) return -1;
-    if (ck(launch_pdl(swiglu_kernel, ew_grid((long long)M * m->ffn), s, true, (const float*)w.gu, w.x, M, m->ffn),
-           "swiglu"))
-      return -1;
-    if (gemv(m->layer_fmt, m->w_down[l], w.x, w.y, m->hidden, m->ffn)) return -1;
+    if (fuse_swiglu) {
+      if (gemv(m->layer_fmt, m->w_gate_up[l], w.x, nullptr, 2 * m->ffn, m->hidden, &swiglu)) return -1;
+    } else {
+      if (gemv(m->layer_fmt, m->w_gate_up[l], w.x, w.gu, 2 * m->ffn, m->hidden)) return -1;
+      if (ck(launch_pdl(swiglu_kernel, ew_grid((long long)M * m->ffn), s, true, (const float*)w.gu, w.x2, M, m->ffn),
+             "swiglu"))
+        return -1;
+    }
+    if (gemv(m->layer_fmt, m->w_down[l], w.x2, w.y, m->hidden, m->ffn)) return -1;
     if (ck(launch_pdl(add_rmsnorm_kernel, M, s, true, w.h, (const uint16_t*)nullptr, (const float*)w.y, w.x,
                       m->hidden, m->rms_eps),
            "add_rmsnorm"))

@@ -510,25 +510,6 @@ struct FmtQ4KH {
     promote<NT>(acc, ps, mnv, d, dmin, iv);
   }
 
-  // Two consecutive super-blocks (x and min-term operands of the second 512 and 32 bytes
-  // further on, scales 16 floats on); the same arithmetic, in the same order, as two
-  // compute() calls.
-  template <int NT>
-  __device__ static void compute2(const Raw& r0, const Raw& r1, float (&acc)[NT][4],
-                                  const uint8_t* xh_unit, const int (&xo)[NT], const uint8_t* s2_unit,
-                                  const int (&so)[NT], const float* iv_unit, const int (&io)[NT], int lane) {
-    float ps0[NT][4], mn0[NT][4], d0[2], dm0[2], ps1[NT][4], mn1[NT][4], d1[2], dm1[2];
-    float2 iv0[NT], iv1[NT];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      iv0[t] = lds_f2(iv_unit + io[t]);
-      iv1[t] = lds_f2(iv_unit + 16 + io[t]);
-    }
-    sums<NT>(r0, xh_unit, xo, s2_unit, so, lane, ps0, mn0, d0, dm0);
-    sums<NT>(r1, xh_unit + 512, xo, s2_unit + 32, so, lane, ps1, mn1, d1, dm1);
-    promote<NT>(acc, ps0, mn0, d0, dm0, iv0);
-    promote<NT>(acc, ps1, mn1, d1, dm1, iv1);
-  }
 };
 
 // ------------------------------------------------------- Q5_K, fp16 path --
@@ -688,25 +669,6 @@ struct FmtQ5KH {
     promote<NT>(acc, ps, mnv, d, dmin, iv);
   }
 
-  // Two consecutive super-blocks (x and min-term operands of the second 512 and 32 bytes
-  // further on, scales 16 floats on); the same arithmetic, in the same order, as two
-  // compute() calls.
-  template <int NT>
-  __device__ static void compute2(const Raw& r0, const Raw& r1, float (&acc)[NT][4],
-                                  const uint8_t* xh_unit, const int (&xo)[NT], const uint8_t* s2_unit,
-                                  const int (&so)[NT], const float* iv_unit, const int (&io)[NT], int lane) {
-    float ps0[NT][4], mn0[NT][4], d0[2], dm0[2], ps1[NT][4], mn1[NT][4], d1[2], dm1[2];
-    float2 iv0[NT], iv1[NT];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      iv0[t] = lds_f2(iv_unit + io[t]);
-      iv1[t] = lds_f2(iv_unit + 16 + io[t]);
-    }
-    sums<NT>(r0, xh_unit, xo, s2_unit, so, lane, ps0, mn0, d0, dm0);
-    sums<NT>(r1, xh_unit + 512, xo, s2_unit + 32, so, lane, ps1, mn1, d1, dm1);
-    promote<NT>(acc, ps0, mn0, d0, dm0, iv0);
-    promote<NT>(acc, ps1, mn1, d1, dm1, iv1);
-  }
 };
 
 // Staging of one CTA's K-slice of the activations for FmtQ4KH / FmtQ5KH (all threads of the

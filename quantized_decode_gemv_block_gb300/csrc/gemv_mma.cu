@@ -269,6 +269,10 @@ struct TmaParams {
   int su, depth, row_stride, unit_bytes, xstride, max_tiles;
   int off_ss, off_ring, off_bar, off_pb, off_res, off_aux;
   int xts, s2ts;  // fp16 path: row strides (bytes) of the staged x and min-term operands
+  // epilogue (GemvEpilogue): 0 y only; 1 y plus the bf16 GQA copies of rows [e_v0, e_v0 + e_vn);
+  // 2 paired rows (tile t = gate rows 8t.. and up rows half + 8t..), out2 = bf16(silu(g) * u)
+  int epi, e_v0, e_vn, e_hd, e_group, e_w, half;
+  uint16_t* out2;
 };
 
 template <class F, int NT>
@@ -322,8 +326,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nu = min(p.su, min(l1 - lp, S - pul));
     if (lane == 0) {
       mbar_arrive_expect_tx(&mybar[slot], stage_bytes);
-      tma_load_2d(myring + (size_t)slot * 16 * p.row_stride, &tmap, (k0 + pul) * ucol,
-                  (t0 + ptl) * 16, &mybar[slot]);
+      uint8_t* dst = myring + (size_t)slot * 16 * p.row_stride;
+      if (p.epi == 2) {  // 8-row boxes: the tile's gate rows, then the matching up rows
+        tma_load_2d(dst, &tmap, (k0 + pul) * ucol, (t0 + ptl) * 8, &mybar[slot]);
+        tma_load_2d(dst + (size_t)8 * p.row_stride, &tmap, (k0 + pul) * ucol, p.half + (t0 + ptl) * 8, &mybar[slot]);
+      } else {
+        tma_load_2d(dst, &tmap, (k0 + pul) * ucol, (t0 + ptl) * 16, &mybar[slot]);
+      }
     }
     lp += nu;
     pul += nu;
@@ -368,6 +377,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
   for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
 
+  // Final value v of output row n (< N) for token tok: y, and in epilogue 1 the bf16 copies of
+  // the GQA rows (row v0 + h*hd + d goes to columns (h*group + i)*hd + d, i < group).
+  auto put = [&](int n, int tok, float v) {
+    if (n >= p.N) return;
+    p.y[(long long)tok * p.N + n] = v;
+    if (p.epi == 1 && n >= p.e_v0 && n < p.e_v0 + p.e_vn) {
+      const int h = (n - p.e_v0) / p.e_hd, d = (n - p.e_v0) - h * p.e_hd;
+      const uint16_t b = f32_to_bf16_rn(v);
+      uint16_t* o = p.out2 + (long long)tok * p.e_w + (long long)h * p.e_group * p.e_hd + d;
+      for (int i = 0; i < p.e_group; ++i) o[i * p.e_hd] = b;
+    }
+  };
+  // Epilogue 2: gate row i and up row half + i (paired in one tile) for token tok.
+  auto put2 = [&](int i, int tok, float vg, float vu) {
+    if (p.y) {
+      p.y[(long long)tok * p.N + i] = vg;
+      p.y[(long long)tok * p.N + p.half + i] = vu;
+    }
+    p.out2[(long long)tok * p.half + i] = silu_mul_bf16(vg, vu);
+  };
+
   // a finished CTA partial of local tile tl
   auto emit = [&](int tl, float (&a)[NT][4]) {
     if (p.C == 1) {
@@ -375,13 +405,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
         const int j0 = 8 * t + 2 * q;
+        if (p.epi == 2) {
+          const int i = (t0 + tl) * 8 + g;
+          if (j0 < p.M) put2(i, j0, a[t][0], a[t][2]);
+          if (j0 + 1 < p.M) put2(i, j0 + 1, a[t][1], a[t][3]);
+          continue;
+        }
         if (j0 < p.M) {
-          if (na < p.N) p.y[(long long)j0 * p.N + na] = a[t][0];
-          if (nb < p.N) p.y[(long long)j0 * p.N + nb] = a[t][2];
+          put(na, j0, a[t][0]);
+          put(nb, j0, a[t][2]);
         }
         if (j0 + 1 < p.M) {
-          if (na < p.N) p.y[(long long)(j0 + 1) * p.N + na] = a[t][1];
-          if (nb < p.N) p.y[(long long)(j0 + 1) * p.N + nb] = a[t][3];
+          put(na, j0 + 1, a[t][1]);
+          put(nb, j0 + 1, a[t][3]);
         }
       }
     } else {
@@ -411,18 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       const uint8_t* sa = myring + ((size_t)slot * 16 + g) * p.row_stride;
       const uint8_t* sb = sa + (size_t)8 * p.row_stride;
-      int i = 0;
-      if constexpr (F::kHalfX) {
-        // two super-blocks per step: independent MMA chains the scheduler can interleave
-        for (; i + 1 < nu; i += 2) {
-          typename F::Raw r0, r1;
-          F::template load<LdShared>(r0, sa + i * p.unit_bytes, sb + i * p.unit_bytes, q);
-          F::template load<LdShared>(r1, sa + (i + 1) * p.unit_bytes, sb + (i + 1) * p.unit_bytes, q);
-          F::template compute2<NT>(r0, r1, acc, smem + (ul + i) * 512, xo,
-                                   smem + p.off_ss + (ul + i) * 32, so, ivs + (ul + i) * 16, io, lane);
-        }
-      }
-      for (; i < nu; ++i) {
+      for (int i = 0; i < nu; ++i) {
         typename F::Raw raw;
         F::template load<LdShared>(raw, sa + i * p.unit_bytes, sb + i * p.unit_bytes, q);
         if constexpr (F::kHalfX)
@@ -478,19 +503,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (meta[ww * 4 + 1] != t) break;
       wa = ww;
     }
-    for (int e = lane; e < 16 * p.M; e += 32) {
-      const int row = e / p.M, tok = e - row * p.M;
+    auto cut_sum = [&](int row, int tok) {
       float v = 0.f;
       for (int ww = wa; ww <= warp; ++ww) {
         if (meta[ww * 4 + 0] < 0) continue;
         const int slot = meta[ww * 4 + 0] == t ? 0 : 1;
         v += pbuf[((size_t)(ww * 2 + slot) * 16 + row) * T + tok];
       }
-      if (p.C == 1) {
-        const int n = (t0 + t) * 16 + row;
-        if (n < p.N) p.y[(long long)tok * p.N + n] = v;
-      } else {
-        res[((size_t)t * 16 + row) * T + tok] = v;
+      return v;
+    };
+    if (p.epi == 2) {  // C == 1 here: rows r and r + 8 are a gate / up pair
+      for (int e = lane; e < 8 * p.M; e += 32) {
+        const int row = e / p.M, tok = e - row * p.M;
+        put2((t0 + t) * 8 + row, tok, cut_sum(row, tok), cut_sum(row + 8, tok));
+      }
+    } else {
+      for (int e = lane; e < 16 * p.M; e += 32) {
+        const int row = e / p.M, tok = e - row * p.M;
+        const float v = cut_sum(row, tok);
+        if (p.C == 1)
+          put((t0 + t) * 16 + row, tok, v);
+        else
+          res[((size_t)t * 16 + row) * T + tok] = v;
       }
     }
   }
@@ -506,8 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tok = e % p.M, rt = e / p.M;  // rt = tile * 16 + row
     float v = 0.f;
     for (int r = 0; r < p.C; ++r) v += cluster.map_shared_rank(res, r)[(size_t)rt * T + tok];
-    const int n = t0 * 16 + rt;
-    if (n < p.N) p.y[(long long)tok * p.N + n] = v;
+    put(t0 * 16 + rt, tok, v);
   }
   cluster.sync();
 }
@@ -742,11 +775,25 @@ size_t gemv_mma_smem(const GemvPlan& pl, int M) {
   return s;
 }
 
+bool gemv_epilogue_ok(int fmt, int N, int K, int kind, int num_sms) {
+  if (kind == 0) return true;
+  if (fmt != FMT_Q4_K && fmt != FMT_Q5_K && fmt != FMT_Q8_0 && fmt != FMT_AFFINE4) return false;
+  const TmaPlan tp = plan_gemv_tma(fmt, N, K, num_sms);
+  if (!tp.ok || !encode_tiled_fn()) return false;
+  return kind == 1 || (kind == 2 && tp.C == 1 && N % 16 == 0);
+}
+
 int launch_gemv_mma(int fmt, const void* w, const void* x, float* y, int M, int N, int K,
-                    long long row_bytes, int num_sms, cudaStream_t stream, bool overlap, std::string* err) {
+                    long long row_bytes, int num_sms, cudaStream_t stream, bool overlap, std::string* err,
+                    const GemvEpilogue* epi) {
   const bool two = M > 8;
   const TmaPlan tp = plan_gemv_tma(fmt, N, K, num_sms);
   EncodeTiledFn enc = encode_tiled_fn();
+  const int kind = epi ? epi->kind : 0;
+  if (kind != 0 && !gemv_epilogue_ok(fmt, N, K, kind, num_sms)) {
+    *err = "internal: this GEMV shape cannot run the fused epilogue";
+    return -1;
+  }
   if (tp.ok && enc) {
     TmaParams prm;
     prm.x = static_cast<const uint16_t*>(x);
@@ -759,6 +806,14 @@ int launch_gemv_mma(int fmt, const void* w, const void* x, float* y, int M, int 
     prm.C = tp.C;
     prm.G = tp.G;
     prm.max_tiles = tp.max_tiles;
+    prm.epi = kind;
+    prm.out2 = epi ? epi->out : nullptr;
+    prm.e_v0 = epi ? epi->v0 : 0;
+    prm.e_vn = epi ? epi->vn : 0;
+    prm.e_hd = epi ? epi->hd : 1;
+    prm.e_group = epi ? epi->group : 1;
+    prm.e_w = epi ? epi->out_w : 0;
+    prm.half = N / 2;
     size_t smem = 0;
     if (!tma_layout(fmt, tp, M, &prm, &smem)) {
       *err = "internal: streaming plan does not fit shared memory";
@@ -768,7 +823,7 @@ int launch_gemv_mma(int fmt, const void* w, const void* x, float* y, int M, int 
     CUtensorMap tm;
     const cuuint64_t gdim[2] = {(cuuint64_t)(row_bytes / 4), (cuuint64_t)N};
     const cuuint64_t gstride[1] = {(cuuint64_t)row_bytes};
-    const cuuint32_t box[2] = {(cuuint32_t)(prm.row_stride / 4), 16u};
+    const cuuint32_t box[2] = {(cuuint32_t)(prm.row_stride / 4), kind == 2 ? 8u : 16u};
     const cuuint32_t estride[2] = {1u, 1u};
     const CUresult cr = enc(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(w), gdim, gstride, box,
                             estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,

@@ -1,6 +1,7 @@
 // Device helpers shared by the kq CUDA kernels (sm_103a).
 #pragma once
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -11,6 +12,16 @@ constexpr int FMT_Q4_K = 2;
 constexpr int FMT_AFFINE4 = 3;
 constexpr int FMT_Q5_K = 4;
 constexpr int FMT_Q6_K = 5;
+
+// fp32 -> bf16 bits, round to nearest even.
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
+
+// The decode step's gated activation: bf16(silu(g) * u), silu(g) = g / (1 + exp(-g)). One
+// definition for every kernel that forms it, so they agree bit for bit.
+__device__ __forceinline__ uint16_t silu_mul_bf16(float g, float u) {
+  const float s = g / (1.0f + expf(-g));
+  return f32_to_bf16_rn(s * u);
+}
 
 // Read-only global loads (weights and activations are never written by a kernel
 // that reads them).

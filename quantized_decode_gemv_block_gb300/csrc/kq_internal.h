@@ -37,11 +37,28 @@ TmaPlan plan_gemv_tma(int fmt, int N, int K, int num_sms);
 unsigned int take_device_errors(std::string* err);
 size_t gemv_mma_smem(const GemvPlan& pl, int M);
 
+// Epilogue of the streaming GEMV for the decode step's glue (fused into the GEMV's stores):
+//  kind 1 (GQA expand): y as usual, and each row n of [v0, v0 + vn) is also written as bf16 to
+//         out[tok][(h * group + i) * hd + d], i < group, with h = (n - v0) / hd, d = (n - v0) % hd
+//         (out rows out_w wide): the attention stand-in's output feeding Wo;
+//  kind 2 (SwiGLU): W's rows pair up (row i is a gate row, row N/2 + i its up row; each 16-row tile
+//         takes 8 of each); out[tok][i] = bf16(silu(y_i) * y_(N/2+i)), rows N/2 wide; y is written
+//         only if not null.
+struct GemvEpilogue {
+  int kind = 0;
+  uint16_t* out = nullptr;
+  int v0 = 0, vn = 0, hd = 1, group = 1, out_w = 0;
+};
+// Whether the streaming kernel runs this shape with this epilogue kind (kind 2 needs a plan
+// without a K-split and N a multiple of 16).
+bool gemv_epilogue_ok(int fmt, int N, int K, int kind, int num_sms);
+
 // bf16 activations, tensor-core path. Returns 0 or -1 with *err set.
 // overlap: launch with programmatic stream serialization (the caller guarantees the
-// previous kernel in the stream does not write w).
+// previous kernel in the stream does not write w). epi: null or a fused epilogue.
 int launch_gemv_mma(int fmt, const void* w, const void* x, float* y, int M, int N, int K,
-                    long long row_bytes, int num_sms, cudaStream_t stream, bool overlap, std::string* err);
+                    long long row_bytes, int num_sms, cudaStream_t stream, bool overlap, std::string* err,
+                    const GemvEpilogue* epi = nullptr);
 
 // Q6_K with bf16 activations, CUDA-core path (its rows are only 2-byte aligned).
 int launch_gemv_q6k_bf16(const void* w, const uint16_t* x, float* y, int M, int N, int K, long long row_bytes,
