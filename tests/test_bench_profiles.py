@@ -42,5 +42,9 @@ def test_committed_profiles_parse():
 
 
 def test_the_headline_profile_matches_the_current_sources():
-    """The default workload's roofline traffic comes from this capture."""
-    assert bench.profile_traffic("gemv_tma_ffn.md") == 14087040.0
+    """The default workload's roofline traffic comes from a capture of the current kernel
+    sources, and that capture read the weights once (14 008 320 algorithmic bytes per launch,
+    plus the tensor-copy row pad and x: well under 2 % more)."""
+    t = bench.profile_traffic("gemv_tma_ffn.md")
+    assert t is not None
+    assert 14008320 <= t <= 1.02 * 14008320
