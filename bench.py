@@ -9,7 +9,7 @@ Prints ONE JSON line (rank 0). Workloads (synthetic data, seeded):
   verify   Q4_K speculative-verify GEMM, W 12288x4096, M bf16 rows (--m, default 16).
   q8_0     Q8_0 GEMV, W 1024x1024, one fp32 row.
   ffn_q5k  the ffn pair with Q5_K blocks (176 bytes per 256 weights).
-  ffn_q6k  the ffn pair with Q6_K blocks (210 bytes per 256 weights; CUDA-core kernel).
+  ffn_q6k  the ffn pair with Q6_K blocks (210 bytes per 256 weights; per-row copies).
   ffn_affine4  the ffn pair with affine4 gs32 blocks (20 bytes per 32 weights).
   head     Q8_0 lm-head GEMV, W 151936x2048, M bf16 rows (--m).
   shortlist  greedy next token over the same head (kq_head_argmax): scores from the small
@@ -1346,7 +1346,7 @@ def main():
     launch_ms = ms_step / len(spec["mats"])
     achieved = step_bytes / len(spec["mats"]) / (launch_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
-    if spec["fmt"] == "q6_k" or spec["dtype"] == "f32":
+    if spec["dtype"] == "f32":
         traffic = profile_traffic(f"gemv_f32_{args.workload}.md", F32_SOURCES)
     else:
         traffic = profile_traffic(f"gemv_tma_{args.workload}.md")
@@ -1375,8 +1375,7 @@ def main():
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_source": f"{peak_kind} hbm_gbs", "kernel": ("gemm_q4k_tc_kernel" if M > 32 else
-                                    ("gemv_tma_kernel" if spec["dtype"] == "bf16" and spec["fmt"] != "q6_k"
-                                     else "gemv_f32_kernel") + (" (16-row passes)" if M > 16 else "")),
+                                    ("gemv_tma_kernel" if spec["dtype"] == "bf16" else "gemv_f32_kernel") + (" (16-row passes)" if M > 16 else "")),
                          "launch_us": launch_ms * 1e3, "launch_us_isolated": isolated_ms * 1e3,
                          "timing": "timed region (graph of K steps) / launches; isolated = event pair per launch"},
             "cpu_baseline": cpu,

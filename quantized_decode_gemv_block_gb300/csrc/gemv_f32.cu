@@ -1,6 +1,7 @@
 // CUDA-core GEMV for fp32 activations (every format) and for bf16 activations of Q6_K
-// blocks, M = 1..16. (Q6_K's 210-byte blocks leave rows only 2-byte aligned, which no tensor
-// copy accepts, so Q6_K is read with 16-bit loads here for both activation types.)
+// blocks whose shape the tensor-core streaming kernel does not take (a K-slice too long for
+// its shared memory, or a weight buffer whose size is not a multiple of 16 bytes), M = 1..16.
+// Q6_K's 210-byte blocks leave rows only 2-byte aligned, so Q6_K is read with 16-bit loads here.
 //
 // Same product as the tensor-core path, Y[j][n] = sum_k deq(W)[n][k] * X[j][k]
 // (Kinetic README, "What makes it fast"), for callers whose activations are fp32

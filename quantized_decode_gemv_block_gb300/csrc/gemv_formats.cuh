@@ -201,6 +201,7 @@ struct FmtQ5K {
 // the quad with shuffles.
 struct FmtQ8_0 {
   static constexpr bool kHalfX = false;
+  static constexpr bool kRowCopies = false;
   static constexpr int kUnitBytes = 272;
   static constexpr bool kPerm0213 = true;
   static constexpr bool kNeedsSum = false;
@@ -282,6 +283,7 @@ struct FmtQ8_0 {
 // the low nibble).
 struct FmtAffine4 {
   static constexpr bool kHalfX = false;
+  static constexpr bool kRowCopies = false;
   static constexpr int kUnitBytes = 160;
   static constexpr bool kPerm0213 = true;
   static constexpr bool kNeedsSum = true;
@@ -369,8 +371,10 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // same way within groups of four, so B fragments are plain 16-byte loads.
 struct FmtQ4KH {
   static constexpr bool kHalfX = true;
+  static constexpr bool kRowCopies = false;
   static constexpr bool kPerm0213 = false;
   static constexpr bool kNeedsSum = false;
+  static constexpr int kXq = 16;  // bytes between threads q of a token's staged super-block
   static constexpr int kUnitBytes = 144;
   struct Raw {
     uint4 h[2];
@@ -389,6 +393,9 @@ struct FmtQ4KH {
   // (0..7) of thread q: the quad's four chunks i sit side by side (64 bytes), and tokens
   // are 64 bytes apart modulo 128, so a quarter-warp's loads hit 32 distinct banks.
   __device__ static int chunk_off(int q, int i) { return 64 * i + 16 * q; }
+  // Byte offset, within a token's 512-byte super-block slot, of the staged 16-byte chunk holding
+  // values 32j + 8v .. +7 (pairs (0,2) (1,3) (4,6) (5,7)): sub-block j belongs to thread j / 2.
+  __device__ static int stage_chunk(int j, int v) { return chunk_off(j >> 1, 4 * (j & 1) + v); }
 
   // xh_unit: token 0's slot of this super-block; xts: token stride (bytes).
   // s2_unit: token 0's min-term operands of this super-block; s2ts: their token stride.
@@ -518,8 +525,10 @@ struct FmtQ4KH {
 // integer; the fused fma rounds once, so (1024 + 31)*63 never has to fit fp16).
 struct FmtQ5KH {
   static constexpr bool kHalfX = true;
+  static constexpr bool kRowCopies = false;
   static constexpr bool kPerm0213 = false;
   static constexpr bool kNeedsSum = false;
+  static constexpr int kXq = 16;  // bytes between threads q of a token's staged super-block
   static constexpr int kUnitBytes = 176;
   struct Raw {
     uint4 h[2];
@@ -543,6 +552,9 @@ struct FmtQ5KH {
   // (0..7) of thread q: the quad's four chunks i sit side by side (64 bytes), and tokens
   // are 64 bytes apart modulo 128, so a quarter-warp's loads hit 32 distinct banks.
   __device__ static int chunk_off(int q, int i) { return 64 * i + 16 * q; }
+  // Byte offset, within a token's 512-byte super-block slot, of the staged 16-byte chunk holding
+  // values 32j + 8v .. +7 (pairs (0,2) (1,3) (4,6) (5,7)): sub-block j belongs to thread j / 2.
+  __device__ static int stage_chunk(int j, int v) { return chunk_off(j >> 1, 4 * (j & 1) + v); }
 
   // xh_unit: token 0's slot of this super-block; xts: token stride (bytes).
   // s2_unit: token 0's min-term operands of this super-block; s2ts: their token stride.
@@ -671,6 +683,109 @@ struct FmtQ5KH {
 
 };
 
+
+// ------------------------------------------------------- Q6_K, fp16 path --
+// One unit = one 210-byte super-block: ql[128], qh[64], int8 scales[16], fp16 d. Weight w:
+// half n = w / 128, quarter kq = (w % 128) / 32, l = w % 32; code q = (ql[64n + 32(kq % 2) + l]
+// >> 4 (kq >= 2)) & 15 | ((qh[32n + l] >> 2kq) & 3) << 4; w = d * scales[w / 16] * (q - 32).
+// Rows are only 2-byte aligned (210-byte blocks), so the streaming kernel copies each row's
+// 16-byte-aligned covering span into its stage row (kRowCopies) and a unit starts at an even
+// offset there; a 4-byte word is read as the two aligned words around it joined by a permute.
+// MMA s (0..15) is sub-block s (16 weights, one scale): n = s / 8, kq = (s / 2) % 4, l = 16 (s % 2)
+// + 4q + {0..3} for thread q, whose slots (2q, 2q+1) take the weights (+0, +2) and (2q+8, 2q+9)
+// the weights (+1, +3); the staged x of every group of four is in the order (0 2 1 3) (what the
+// staging's pair packing gives in natural chunk order), so a B fragment is one 8-byte load.
+// A = q - 32 is exact in fp16; sc * (q - 32) is not (up to 127 * 32), so each sub-block's fp32
+// MMA result is promoted by its scale, and d and 2^-e once per super-block.
+__device__ __forceinline__ uint32_t lds_u32_a2(uint32_t a) {  // a: 2-byte aligned shared address
+  uint32_t w0, w1;
+  asm("ld.shared.u32 %0, [%1];" : "=r"(w0) : "r"(a & ~3u));
+  asm("ld.shared.u32 %0, [%1];" : "=r"(w1) : "r"((a & ~3u) + 4u));
+  return prmt(w0, w1, (a & 2u) ? 0x5432u : 0x3210u);
+}
+
+struct FmtQ6KH {
+  static constexpr bool kHalfX = true;
+  static constexpr bool kRowCopies = true;
+  static constexpr int kUnitBytes = 210;
+  static constexpr int kXq = 8;  // bytes between threads q of a token's staged super-block
+  struct Raw {
+    uint32_t ql[2][8];  // [row][4n + 2(kq % 2) + s % 2]: ql bytes 64n + 32(kq % 2) + 16(s % 2) + 4q .. +3
+    uint32_t qh[2][4];  // [row][2n + s % 2]: qh bytes 32n + 16(s % 2) + 4q .. +3
+    uint32_t sc[2][4];  // [row][i]: scales 4i .. 4i+3
+    uint32_t d[2];      // [row]: fp16 d in the low half
+  };
+  // pa / pb: the unit of rows g / g+8 in shared memory (2-byte aligned)
+  template <class Ld>
+  __device__ static void load(Raw& r, const uint8_t* pa, const uint8_t* pb, int q) {
+    const uint32_t a[2] = {smem_addr(pa), smem_addr(pb)};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int k2 = 0; k2 < 2; ++k2) r.ql[i][4 * n + 2 * k2 + h] = lds_u32_a2(a[i] + 64 * n + 32 * k2 + 16 * h + 4 * q);
+          r.qh[i][2 * n + h] = lds_u32_a2(a[i] + 128 + 32 * n + 16 * h + 4 * q);
+        }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) r.sc[i][k] = lds_u32_a2(a[i] + 192 + 4 * k);
+      r.d[i] = lds_u32_a2(a[i] + 208);
+    }
+  }
+  __device__ static int stage_chunk(int j, int v) { return 64 * j + 16 * v; }
+
+  template <int NT>
+  __device__ static void compute(const Raw& r, float (&acc)[NT][4], const uint8_t* xh_unit, const int (&xo)[NT],
+                                 const uint8_t* /*s2_unit*/, const int (&/*so*/)[NT], const float* iv_unit,
+                                 const int (&io)[NT], int lane) {
+    const int q = lane & 3;
+    float u[NT][4];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) u[t][0] = u[t][1] = u[t][2] = u[t][3] = 0.f;
+#pragma unroll
+    for (int sb = 0; sb < 16; ++sb) {
+      const int n = sb >> 3, kq = (sb >> 1) & 3, h = sb & 1;
+      uint32_t a[4];
+      float scf[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint32_t ql = r.ql[i][4 * n + 2 * (kq & 1) + h], qh = r.qh[i][2 * n + h];
+        const uint32_t nib = (kq >= 2 ? ql >> 4 : ql) & 0x0F0F0F0Fu;
+        const uint32_t hb = kq == 0 ? (qh << 4) : kq == 1 ? (qh << 2) : kq == 2 ? qh : (qh >> 2);
+        const uint32_t qw = nib | (hb & 0x30303030u);  // the four 6-bit codes, one per byte
+        // (1024 + q) per half from bytes 0, 2 and 1, 3, minus 1056: q - 32, exact
+        a[i] = h2_sub(and_or(qw, 0x003F003Fu, 0x64006400u), 0x64206420u);
+        a[i + 2] = h2_sub(and_or(qw >> 8, 0x003F003Fu, 0x64006400u), 0x64206420u);
+        // the sub-block's int8 scale as fp32: (b ^ 0x80) in the mantissa of 2^23, minus 2^23 + 128
+        const uint32_t sbyte = prmt(r.sc[i][sb >> 2] ^ 0x80808080u, 0x4B000000u, 0x7650u | (sb & 3));
+        scf[i] = __fsub_rn(__uint_as_float(sbyte), 8388736.f);
+      }
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const uint2 b = *reinterpret_cast<const uint2*>(xh_unit + xo[t] + 32 * sb);
+        const float z[4] = {0.f, 0.f, 0.f, 0.f};
+        float p[4];
+        mma_f16_16816(p, a, b.x, b.y, z);
+        u[t][0] = __fmaf_rn(scf[0], p[0], u[t][0]);
+        u[t][1] = __fmaf_rn(scf[0], p[1], u[t][1]);
+        u[t][2] = __fmaf_rn(scf[1], p[2], u[t][2]);
+        u[t][3] = __fmaf_rn(scf[1], p[3], u[t][3]);
+      }
+    }
+    const float d0 = half_bits_to_float(r.d[0]), d1 = half_bits_to_float(r.d[1]);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const float2 iv = lds_f2(iv_unit + io[t]);
+      acc[t][0] = __fmaf_rn(d0 * u[t][0], iv.x, acc[t][0]);
+      acc[t][1] = __fmaf_rn(d0 * u[t][1], iv.y, acc[t][1]);
+      acc[t][2] = __fmaf_rn(d1 * u[t][2], iv.x, acc[t][2]);
+      acc[t][3] = __fmaf_rn(d1 * u[t][3], iv.y, acc[t][3]);
+    }
+  }
+};
+
 // Staging of one CTA's K-slice of the activations for FmtQ4KH / FmtQ5KH (all threads of the
 // CTA take part). x: M x K bf16. Slice = super-blocks [k0, k0+S).
 // Every (token, super-block) gets its own power-of-two scale 2^e with max|x| * 2^e in
@@ -694,7 +809,7 @@ __device__ __forceinline__ float token_scale(uint32_t mb) {
 // and 2^-e. The caller places one __syncthreads after finish().
 // Rows 0..M-1 of the staged x hold the tokens, row M zeros (absent token slots read it).
 // iv: 2^-e per (super-block, token), 16 floats per super-block.
-template <int NTHREADS>
+template <int NTHREADS, class F>
 struct StageQ4KH {
   static_assert(NTHREADS % 32 == 0, "an item's eight lanes must share a warp");
   static constexpr int kItems = 5;  // 16 tokens x 10 super-blocks x 8 groups / 256 threads
@@ -755,7 +870,7 @@ struct StageQ4KH {
           const float f4 = __uint_as_float(w.z << 16) * sc, f5 = __uint_as_float(w.z & 0xFFFF0000u) * sc;
           const float f6 = __uint_as_float(w.w << 16) * sc, f7 = __uint_as_float(w.w & 0xFFFF0000u) * sc;
           const uint4 o = make_uint4(f2_to_h2(f0, f2), f2_to_h2(f1, f3), f2_to_h2(f4, f6), f2_to_h2(f5, f7));
-          *reinterpret_cast<uint4*>(xh + tok * xts + ul * 512 + FmtQ4KH::chunk_off(q, 4 * half + v)) = o;
+          *reinterpret_cast<uint4*>(xh + tok * xts + ul * 512 + F::stage_chunk(j, v)) = o;
           // the sum of what the MMA will see (the fp16 values), four partial sums in a fixed order
           const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll

@@ -32,6 +32,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <cstring>
 
 #include "kq_device.cuh"
 #include "kq_internal.h"
@@ -246,8 +247,10 @@ int launch_chunked(const Params& prm, size_t smem, cudaStream_t stream, std::str
 // per warp, so every warp streams the same number of units. Each warp keeps a
 // private ring of `depth` stages in shared memory; one stage holds up to `su`
 // consecutive units of one tile for its 16 rows and is filled by ONE tensor copy (a
-// 16-row box, rows past N arriving as zeros) completing on the stage's mbarrier. The
-// whole ring is requested before the activations are staged.
+// 16-row box, rows past N arriving as zeros) completing on the stage's mbarrier. Q6_K rows
+// are only 2-byte aligned, which no tensor map takes: there each row of a stage is its own
+// 1-D bulk copy of the 16-byte-aligned span around its units (rows past N copy nothing and
+// are never stored). The whole ring is requested before the activations are staged.
 //
 // A tile whose units one warp covers entirely is finished by that warp. A tile cut
 // between warps leaves one partial per warp, added at the end in warp order (= K
@@ -273,6 +276,9 @@ struct TmaParams {
   // 2 paired rows (tile t = gate rows 8t.. and up rows half + 8t..), out2 = bf16(silu(g) * u)
   int epi, e_v0, e_vn, e_hd, e_group, e_w, half;
   uint16_t* out2;
+  // formats with per-row copies (F::kRowCopies): the weight rows, row_bytes apart
+  const uint8_t* w;
+  long long row_bytes;
 };
 
 template <class F, int NT>
@@ -290,7 +296,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
-  if (threadIdx.x == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap) : "memory");
+  if constexpr (!F::kRowCopies) {
+    if (threadIdx.x == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap) : "memory");
+  }
   int rank = 0;
   if (p.C > 1) rank = static_cast<int>(cg::this_cluster().block_rank());
   // all index math in 32-bit unsigned (every product below stays under 2^31)
@@ -324,7 +332,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ucol = p.unit_bytes / 4;  // tensor map elements are 4-byte words
   auto issue = [&](int slot) {
     const int nu = min(p.su, min(l1 - lp, S - pul));
-    if (lane == 0) {
+    if constexpr (F::kRowCopies) {
+      // one bulk copy per row (lanes 0..15): the 16-byte-aligned span covering the row's nu
+      // units; rows past N copy nothing (the buffer's end is 16-byte aligned: host check)
+      const int row = (t0 + ptl) * 16 + lane;
+      uint32_t bytes = 0;
+      long long a0 = 0;
+      if (lane < 16 && row < p.N) {
+        const long long a = (long long)row * p.row_bytes + (long long)(k0 + pul) * F::kUnitBytes;
+        a0 = a & ~15ll;
+        bytes = static_cast<uint32_t>(((a + (long long)nu * F::kUnitBytes + 15) & ~15ll) - a0);
+      }
+      const uint32_t total = __reduce_add_sync(0xFFFFFFFFu, bytes);
+      if (lane == 0) mbar_arrive_expect_tx(&mybar[slot], total);
+      __syncwarp();
+      if (bytes) bulk_g2s(myring + ((size_t)slot * 16 + lane) * p.row_stride, p.w + a0, bytes, &mybar[slot]);
+    } else if (lane == 0) {
       mbar_arrive_expect_tx(&mybar[slot], stage_bytes);
       uint8_t* dst = myring + (size_t)slot * 16 * p.row_stride;
       if (p.epi == 2) {  // 8-row boxes: the tile's gate rows, then the matching up rows
@@ -343,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // The weights may stream before the previous grid in the stream has finished (when this
   // launch was allowed to overlap it); the activations it produced may not: wait here.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  [[maybe_unused]] StageQ4KH<kThreads> stq;
+  [[maybe_unused]] StageQ4KH<kThreads, F> stq;
   if constexpr (F::kHalfX) {
     if (S > 0) stq.load(p.x, p.M, p.K, k0, S, smem, p.xts, smem + p.off_ss, p.s2ts, ivs);
   }
@@ -364,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const int tok = 8 * t + g, row = tok < p.M ? tok : p.M;
-      xo[t] = row * p.xts + 16 * q;
+      xo[t] = row * p.xts + F::kXq * q;
       so[t] = row * p.s2ts + 8 * q;
       io[t] = 8 * t + 2 * q;
     }
@@ -444,9 +467,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = false;
       if (lane == 0) atomicOr(&g_device_errors, 1u);
     }
+    ok = __all_sync(0xFFFFFFFFu, ok);  // the warp's MMAs and copies need every lane
     if (ok) {
       const uint8_t* sa = myring + ((size_t)slot * 16 + g) * p.row_stride;
       const uint8_t* sb = sa + (size_t)8 * p.row_stride;
+      if constexpr (F::kRowCopies) {  // where each row's copy put the stage's first unit
+        const uint32_t u0 = static_cast<uint32_t>(k0 + ul) * F::kUnitBytes;
+        const uint32_t na = static_cast<uint32_t>((t0 + tl) * 16 + g), rb = static_cast<uint32_t>(p.row_bytes);
+        sa += (na * rb + u0) & 15u;  // modulo 2^32 keeps the residue modulo 16
+        sb += ((na + 8u) * rb + u0) & 15u;
+      }
       for (int i = 0; i < nu; ++i) {
         typename F::Raw raw;
         F::template load<LdShared>(raw, sa + i * p.unit_bytes, sb + i * p.unit_bytes, q);
@@ -590,7 +620,7 @@ int launch_tma(const CUtensorMap& tm, const TmaParams& prm, size_t smem, int gri
 }
 
 int unit_bytes_of(int fmt) {
-  return fmt == FMT_Q4_K ? 144 : (fmt == FMT_Q5_K ? 176 : (fmt == FMT_Q8_0 ? 272 : 160));
+  return fmt == FMT_Q4_K ? 144 : (fmt == FMT_Q5_K ? 176 : (fmt == FMT_Q6_K ? 210 : (fmt == FMT_Q8_0 ? 272 : 160)));
 }
 // Units per stage: one tensor copy brings 16 rows of >= 544 bytes each (row-strided copies
 // below ~576 bytes per row measured well under the HBM rate).
@@ -605,7 +635,8 @@ bool tma_layout(int fmt, const TmaPlan& pl, int M, TmaParams* prm, size_t* smem)
   auto al = [](size_t v) { return (v + 127) & ~size_t(127); };
   const int T = M > 8 ? 16 : 8;
   const int ub = unit_bytes_of(fmt);
-  const bool half_x = fmt == FMT_Q4_K || fmt == FMT_Q5_K;
+  const bool half_x = fmt == FMT_Q4_K || fmt == FMT_Q5_K || fmt == FMT_Q6_K;
+  const bool row_copies = fmt == FMT_Q6_K;
   const int smax = (pl.units + pl.C - 1) / pl.C;
   int xstride = 0, xts = 0, s2ts = 0;
   size_t xbytes = 0, sbytes = 0;
@@ -632,13 +663,13 @@ bool tma_layout(int fmt, const TmaPlan& pl, int M, TmaParams* prm, size_t* smem)
   off = al(off + (size_t)kWarps * 8 * 8);
   const size_t off_ring = off;
   for (int su = stage_units_of(fmt); su >= 1; --su) {
-    int stride = su * ub;
+    int stride = row_copies ? (su * ub + 30 + 15) / 16 * 16 : su * ub;  // + the span's alignment slack
     if (half_x) {  // quad loads of 16 bytes at 16 + 32q: rows must differ by 16 mod 32 bytes
       while (stride % 32 != 16) stride += 16;
     } else {       // 8-byte loads of 4 rows per phase: rows must differ by 32 or 96 mod 128
       while (stride % 128 != 32 && stride % 128 != 96) stride += 16;
     }
-    if (stride / 4 > 256) continue;  // tensor-map box limit (256 elements)
+    if (!row_copies && stride / 4 > 256) continue;  // tensor-map box limit (256 elements)
     const size_t per_stage = (size_t)kWarps * 16 * stride;
     if (off + 2 * per_stage > (size_t)kSmemCap) continue;
     const int depth = (int)std::min<size_t>(8, ((size_t)kSmemCap - off) / per_stage);
@@ -674,6 +705,7 @@ int max_clusters(int fmt, int C, size_t smem) {
   const void* fn = nullptr;
   if (fmt == FMT_Q4_K) fn = (const void*)gemv_tma_kernel<FmtQ4KH, 2>;
   else if (fmt == FMT_Q5_K) fn = (const void*)gemv_tma_kernel<FmtQ5KH, 2>;
+  else if (fmt == FMT_Q6_K) fn = (const void*)gemv_tma_kernel<FmtQ6KH, 2>;
   else if (fmt == FMT_Q8_0) fn = (const void*)gemv_tma_kernel<FmtQ8_0, 2>;
   else fn = (const void*)gemv_tma_kernel<FmtAffine4, 2>;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemCap) != cudaSuccess)
@@ -794,7 +826,13 @@ int launch_gemv_mma(int fmt, const void* w, const void* x, float* y, int M, int 
     *err = "internal: this GEMV shape cannot run the fused epilogue";
     return -1;
   }
-  if (tp.ok && enc) {
+  if (fmt == FMT_Q6_K) {
+    // per-row copies round each row's span out to 16 bytes, which stays inside the weights
+    // only if their total size is a multiple of 16; other shapes take the CUDA-core kernel
+    if (!tp.ok || ((long long)N * row_bytes) % 16 != 0)
+      return launch_gemv_q6k_bf16(w, static_cast<const uint16_t*>(x), y, M, N, K, row_bytes, stream, err);
+  }
+  if (tp.ok && (enc || fmt == FMT_Q6_K)) {
     TmaParams prm;
     prm.x = static_cast<const uint16_t*>(x);
     prm.y = y;
@@ -814,6 +852,8 @@ int launch_gemv_mma(int fmt, const void* w, const void* x, float* y, int M, int 
     prm.e_group = epi ? epi->group : 1;
     prm.e_w = epi ? epi->out_w : 0;
     prm.half = N / 2;
+    prm.w = static_cast<const uint8_t*>(w);
+    prm.row_bytes = row_bytes;
     size_t smem = 0;
     if (!tma_layout(fmt, tp, M, &prm, &smem)) {
       *err = "internal: streaming plan does not fit shared memory";
@@ -821,6 +861,10 @@ int launch_gemv_mma(int fmt, const void* w, const void* x, float* y, int M, int 
     }
     // W as a 2-D tensor of 4-byte words: rows of row_bytes, box = 16 rows x row_stride bytes
     CUtensorMap tm;
+    std::memset(&tm, 0, sizeof(tm));
+    if (fmt == FMT_Q6_K)  // rows copied one by one: no tensor map
+      return two ? launch_tma<FmtQ6KH, 2>(tm, prm, smem, tp.G * tp.C, stream, overlap, err)
+                 : launch_tma<FmtQ6KH, 1>(tm, prm, smem, tp.G * tp.C, stream, overlap, err);
     const cuuint64_t gdim[2] = {(cuuint64_t)(row_bytes / 4), (cuuint64_t)N};
     const cuuint64_t gstride[1] = {(cuuint64_t)row_bytes};
     const cuuint32_t box[2] = {(cuuint32_t)(prm.row_stride / 4), kind == 2 ? 8u : 16u};

@@ -81,10 +81,7 @@ int gemv_impl(int fmt, const void* w, int x_dtype, const void* x, float* y, int 
   }
   std::string err;
   const long long row_bytes = (long long)kq_row_bytes(fmt, K);
-  if (fmt == KQ_Q6_K && x_dtype == KQ_BF16) {  // 2-byte aligned rows: the CUDA-core kernel
-    if (kq::launch_gemv_q6k_bf16(w, static_cast<const uint16_t*>(x), y, M, N, K, row_bytes, s, &err) != 0)
-      return fail(KQ_ERR_CUDA, err);
-  } else if (x_dtype == KQ_BF16) {
+  if (x_dtype == KQ_BF16) {
     const int sms = sm_count(&err);
     if (sms < 0) return fail(KQ_ERR_CUDA, err);
     if (kq::launch_gemv_mma(fmt, w, x, y, M, N, K, row_bytes, sms, s, (flags & KQ_OVERLAP_PREVIOUS) != 0,
