@@ -16,21 +16,37 @@
 //  * epilogue warps read each finished group from tensor memory and add d_s times it (fp32)
 //    into registers, so the only roundings are fp32 ones.
 //
-// Orientation: the tensor-core A operand is the weight tile (128 rows of W), B is the token
-// tile (256 tokens), so tensor-memory lane = weight row and column = token: d_s is one scalar
-// per thread, and Y stores are 128-byte rows. Roles in a CTA (persistent over output tiles):
+// Two SMs per MMA (tcgen05 cta_group::2): a cluster of two CTAs owns an output tile of 256
+// weight rows x 256 tokens. CTA rank r holds the A operand for weight rows 128r.. of the tile
+// and the B operand for tokens 128r..; one thread of rank 0 issues M = 256, N = 256, K = 16
+// MMAs that read both CTAs' shared memory, and each CTA's tensor memory receives its own 128
+// rows x 256 tokens. Per SM and k-tile that is 16 KB of t and 16 KB of tokens written and read
+// once, against 16 + 32 KB for a one-SM MMA of the same shape: the copies, the unpacking
+// stores and the tensor core's operand reads share each SM's shared-memory bandwidth.
+//
+// Orientation: A = weight tile, B = token tile, so tensor-memory lane = weight row and column =
+// token: d_s is one scalar per thread, and Y stores are 128-byte rows. Roles in each CTA
+// (persistent over output tiles, both CTAs of a pair walk the same tile sequence):
 //   warps 0..7   epilogue (warp w: lanes 32*(w%4).., tokens 128*(w/4)..), 128 fp32 sums each
-//   warps 8..9   unpack t = sc*q for the 128 weight rows of the tile (2 rows per thread) into
-//                the K-major 128-byte-swizzled A tile of the stage ring
-//   warp 10      TMA: token tiles (256 x 64 fp16) and the W min-term tiles (128 x 64 fp16)
-//   warp 11      one thread issues tcgen05.mma (M=128, N=256, K=16) and owns tensor memory
-// Every mbarrier wait is bounded: a timeout records the device error word, raises an abort
-// flag that every role checks, and the CTA drains its own copies and MMAs and returns.
+//   warps 8..9   unpack t = sc*q for the CTA's 128 weight rows (2 rows per thread) from raw
+//                Q4_K super-blocks that a tensor copy brought into shared memory, into the
+//                K-major 128-byte-swizzled A tile of the stage ring
+//   warp 10      tensor copies: the CTA's half of each token tile (128 x 64 fp16) and of the
+//                W min-term tiles (128 x 64 fp16), completing on rank 0's barrier
+//   warp 11      tensor memory (both ranks); rank 0: one thread issues the MMAs
+// Stage handshakes meet on rank 0's barriers: the copies by byte count, the unpacking and
+// epilogue warps of rank 1 through one forwarding thread of rank 1 (a cluster-scope release
+// stalls the warp that makes it); MMA completions are multicast to both CTAs. Every mbarrier wait is bounded: a
+// timeout records the device error word, raises the abort flag of both CTAs (every role checks
+// it), and the CTAs drain their copies and MMAs and return.
+#include <cooperative_groups.h>
 #include <cuda.h>
 #include <cuda_fp16.h>
 
 #include "kq_device.cuh"
 #include "kq_internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace kq {
 
@@ -38,23 +54,35 @@ __device__ unsigned int g_tc_errors = 0;  // bit 0: a bounded wait in the prefil
 
 namespace {
 
-constexpr int TM = 128;  // weight rows per tile (MMA M)
-constexpr int TN = 256;  // tokens per tile (MMA N)
+constexpr int TM = 128;  // weight rows per CTA (half of the pair's MMA M = 256)
+constexpr int TN = 256;  // tokens per tile (MMA N); each CTA stages TN / 2 of them
 constexpr int BK = 64;   // k per stage (one 128-byte swizzle row of fp16)
-constexpr int STAGES = 4;
-constexpr int kWTileBytes = TM * BK * 2;  // 16 KB
-constexpr int kXTileBytes = TN * BK * 2;  // 32 KB
+constexpr int STAGES = 5;
+constexpr int RAW_STAGES = 3;
+// A parity wait is only sound while its barrier cannot be two phases behind the one awaited.
+// Stages free in k-tile order (MMA completion); a waiter for k-tile e waits for the MMAs of
+// e - STAGES and already knows those of some e - d to be done; it needs d <= 2 * STAGES.
+constexpr int kWTileBytes = TM * BK * 2;        // 16 KB
+constexpr int kXTileBytes = (TN / 2) * BK * 2;  // 16 KB: this CTA's half of the token tile
 constexpr int kStageBytes = kWTileBytes + kXTileBytes;
-constexpr int kEpiWarps = 8, kDqWarps = 2;
-constexpr int kDqBase = kEpiWarps * 32;
-constexpr int kDqThreads = kDqWarps * 32;  // each unpacks rows u and u + 64
+constexpr int kRawBytes = TM * 144;  // one Q4_K super-block of the CTA's 128 rows
+// Four warpgroups: 0-1 epilogue, 2 unpacking, 3 copies / MMA (warps 14-15 idle). The
+// epilogue's 128 fp32 sums per thread need more registers than the 128 a 512-thread CTA starts
+// with: warpgroups 2 and 3 hand theirs over (setmaxnreg), 2*128*176 + 128*104 + 128*56 = 512*128.
+constexpr int kEpiWarps = 8, kDqWarps = 4;
+constexpr int kDqBase = kEpiWarps;  // first unpacking warp
 constexpr int kTmaWarp = kEpiWarps + kDqWarps, kMmaWarp = kTmaWarp + 1;
-constexpr int kTcThreads = (kMmaWarp + 1) * 32;
+constexpr int kTcThreads = 16 * 32;
+constexpr int kLaunchRegs = 128, kEpiRegs = 176, kDqRegs = 104, kCtlRegs = 56;
+static_assert(kTcThreads * kLaunchRegs == 65536, "the CTA holds the whole register file");
+static_assert(kDqWarps <= STAGES, "an unpacking warp's previous wait was kDqWarps + STAGES k-tiles back");
+static_assert(2 * 128 * kEpiRegs + 128 * kDqRegs + 128 * kCtlRegs == kTcThreads * kLaunchRegs, "register split");
 constexpr int kTmemCols = 2 * TN;  // two accumulator groups in flight
+constexpr int kBarBytes = 1024;
 constexpr int kInvBytes = kEpiWarps * (TN / 2) * 4;  // per epilogue warp: its tokens' 2^-e_j
-constexpr int kTcSmem = STAGES * kStageBytes + 1024 /*barriers*/ + kInvBytes + 1024 /*alignment slack*/;
+constexpr int kTcSmem = STAGES * kStageBytes + RAW_STAGES * kRawBytes + kBarBytes + kInvBytes + 1024 /*alignment*/;
 constexpr uint64_t kTcWaitNs = 2000000000ull;
-static_assert(kDqThreads * 2 == TM, "two weight rows per unpacking thread");
+static_assert(kTcSmem <= 232448, "shared memory per CTA");
 
 struct TcParams {
   const uint8_t* w;
@@ -64,7 +92,7 @@ struct TcParams {
   long long row_bytes;
   int n_ext;    // min-term k-tiles per tile
   int m_tiles;  // token tiles
-  int tiles;    // m_tiles * weight-row tiles
+  int tiles;    // m_tiles * weight-row tiles (of 2 * TM rows)
 };
 
 // UMMA shared-memory descriptor: K-major operand, 128-byte swizzle, 8-row groups 1024 B apart.
@@ -74,37 +102,64 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
          | ((uint64_t)2 << 61) /* SWIZZLE_128B */;
 }
 
-// Instruction descriptor, kind::f16: D fp32, A and B fp16, both K-major, M = 128, N = 256.
-constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(TN >> 3) << 17) | ((uint32_t)(TM >> 4) << 24);
+// Instruction descriptor, kind::f16: D fp32, A and B fp16, both K-major, M = 256 (the pair),
+// N = 256.
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(TN >> 3) << 17) | ((uint32_t)((2 * TM) >> 4) << 24);
 
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst_smem)),
+// Tensor memory of the pair: one warp of each CTA takes part in both calls.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst_smem)),
                "r"(ncols)
                : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate) {
+__device__ __forceinline__ void umma_pair_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
       : "memory");
 }
-// Arrive on `bar` once every tcgen05.mma issued so far by this thread has completed.
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
-               : "memory");
+// Arrive once on `bar` (the same offset in both CTAs of the pair) when every tcgen05.mma issued
+// so far by this thread has completed.
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_addr(bar)),
+      "h"((uint16_t)3)
+      : "memory");
 }
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+// The shared::cluster address of `p`'s counterpart in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+  return r;
+}
+// Arrive on a barrier of either CTA (default semantics: a cluster-scope release here stalled
+// the arriving thread for ~0.4 us per call).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_local(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
-
+// Non-blocking test of a phase (this CTA's barrier).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // 16 consecutive fp32 columns of this warp's 32 tensor-memory lanes.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
@@ -118,10 +173,13 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void tma_load_2d_sw(void* dst, const void* tmap, int x, int y, uint64_t* bar) {
+// 2-D tensor copy into this CTA's shared memory whose completion (bytes) is counted on a
+// barrier of either CTA of the pair (bar: shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const void* tmap, int x, int y, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(smem_addr(dst)), "l"(tmap), "r"(x), "r"(y), "r"(smem_addr(bar))
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
 
@@ -173,61 +231,65 @@ __device__ __forceinline__ void unpack_t(uint32_t s0, uint32_t s2, const uint4& 
   }
 }
 
-// Bring super-block `sb` of a weight row into L2 (no registers, no completion to wait for).
-__device__ __forceinline__ void prefetch_block_l2(const uint8_t* rowp, int sb) {
-  const uint8_t* b = rowp + (long long)sb * 144;  // 144 bytes: at most two 128-byte lines
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(b) : "memory");
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(b + 143) : "memory");
-}
-constexpr int kPrefetchBlocks = 3;  // super-blocks (12 k-tiles) ahead of the unpacking
-
-struct RowChunk {  // what one row needs for one k-tile: header words, 32 quant bytes
-  uint4 h, a, b;
-};
-
-__device__ __forceinline__ void load_chunk(RowChunk& c, const uint8_t* rowp, int kt, bool new_block) {
-  const uint8_t* blk = rowp + (long long)(kt >> 2) * 144;
-  if (new_block) c.h = ldg128(blk);
-  c.a = ldg128(blk + 16 + 32 * (kt & 3));
-  c.b = ldg128(blk + 32 + 32 * (kt & 3));
+// k-chunk kc of the super-block of row r (144 bytes at row * 144 of a raw stage) into row r of
+// the swizzled tile.
+__device__ __forceinline__ void unpack_row(const uint8_t* raw_stage, int r, int kc, uint8_t* tile) {
+  const uint8_t* b = raw_stage + r * 144;
+  const uint4 h = lds128(b), qa = lds128(b + 16 + 32 * kc), qb = lds128(b + 32 + 32 * kc);
+  unpack_t(h.y, h.w, qa, qb, kc, tile, r);
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     gemm_q4k_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap emap,
-                       const TcParams p) {
+                       const __grid_constant__ CUtensorMap wmap, const TcParams p) {
   extern __shared__ uint8_t tc_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full_x = reinterpret_cast<uint64_t*>(smem + STAGES * kStageBytes);  // TMA bytes landed
-  uint64_t* full_w = full_x + STAGES;                                             // t tile written
-  uint64_t* empty = full_w + STAGES;                                              // MMAs read the stage
-  uint64_t* acc_full = empty + STAGES;                                            // [2] group finished
-  uint64_t* acc_empty = acc_full + 2;                                             // [2] group read out
-  uint64_t* mma_done = acc_empty + 2;
+  uint8_t* raw = smem + STAGES * kStageBytes;     // stage s: t tile, then this CTA's token tile
+  uint64_t* full_x = reinterpret_cast<uint64_t*>(raw + RAW_STAGES * kRawBytes);  // rank 0: copies landed
+  uint64_t* full_w = full_x + STAGES;             // each: the CTA's t tile written (rank 0: and rank 1's)
+  uint64_t* empty = full_w + STAGES;              // each: the pair's MMAs read the stage
+  uint64_t* acc_full = empty + STAGES;            // each [2]: group finished
+  uint64_t* acc_empty = acc_full + 2;             // each [2]: the CTA's epilogue read the group (rank 0: and rank 1's)
+  uint64_t* raw_full = acc_empty + 2;             // each [RAW_STAGES]: raw super-block landed
+  uint64_t* raw_empty = raw_full + RAW_STAGES;    // each [RAW_STAGES]: the super-block's 4 k-tiles unpacked
+  uint64_t* mma_done = raw_empty + RAW_STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   unsigned int* abort_flag = tmem_slot + 1;
+  float* inv_base = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full_x) + kBarBytes);
 
+  cg::cluster_group cluster = cg::this_cluster();
+  const uint32_t rank = cluster.block_rank();
+  const bool leader = rank == 0;
+  const int pair = static_cast<int>(blockIdx.x >> 1), npairs = static_cast<int>(gridDim.x >> 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nsb = p.K / 256, kt_main = p.K / BK, kt_tile = p.n_ext + kt_main;
 
   if (threadIdx.x == 0) {
+    // rank 1's unpacking and epilogue warps arrive on their own barriers; one thread of rank 1
+    // forwards each completed phase to rank 0 (a cluster-scope release per stage, not per warp)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full_x[s], 1);
-      mbar_init(&full_w[s], kDqThreads);
+      mbar_init(&full_w[s], 1 + (leader ? 1 : 0));  // the warp that unpacked the stage (+ rank 1's)
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], kEpiWarps);
+      mbar_init(&acc_empty[b], kEpiWarps + (leader ? 1 : 0));
+    }
+    for (int r = 0; r < RAW_STAGES; ++r) {
+      mbar_init(&raw_full[r], 1);
+      mbar_init(&raw_empty[r], 4);  // one arrival per k-tile of the super-block
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0u;
     fence_mbar_init();
     asm volatile("prefetch.tensormap [%0];" ::"l"(&xmap) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(&emap) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&wmap) : "memory");
   }
-  if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc_pair(tmem_slot, kTmemCols);
   tc_fence_before();
-  __syncthreads();
+  cluster.sync();  // both CTAs' barriers initialised and tensor memory allocated
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -235,47 +297,50 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   auto fail = [&]() {
     atomicOr(&g_tc_errors, 1u);
     atomicOr(abort_flag, 1u);
+    atomicOr(cluster.map_shared_rank(abort_flag, rank ^ 1u), 1u);
   };
   auto stage_free = [&](int it) {  // wait until the MMAs of the stage's previous use are done
     return it < STAGES ||
            mbar_wait_bounded(&empty[it % STAGES], static_cast<uint32_t>(it / STAGES - 1) & 1u, kTcWaitNs);
   };
 
-  if (warp == kTmaWarp) {
+  const int wg = warp >> 2;  // each role's register budget is set at the top of its branch
+  if (wg == 3) {
+   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtlRegs));
+   if (warp == kTmaWarp) {
     if (lane == 0) {
       int it = 0;
       bool stop = false;
-      for (int tile = blockIdx.x; tile < p.tiles && !stop; tile += gridDim.x) {
-        const int m0 = (tile % p.m_tiles) * TN, n0 = (tile / p.m_tiles) * TM;
+      for (int tile = pair; tile < p.tiles && !stop; tile += npairs) {
+        const int m0 = (tile % p.m_tiles) * TN + static_cast<int>(rank) * (TN / 2);
+        const int n0 = (tile / p.m_tiles) * (2 * TM) + static_cast<int>(rank) * TM;
         for (int kt = 0; kt < kt_tile; ++kt) {
           const int s = it % STAGES;
           if (!stage_free(it)) { fail(); stop = true; break; }
           if (aborted()) { stop = true; break; }
           uint8_t* st = smem + s * kStageBytes;
+          const uint32_t fb = cluster_addr(&full_x[s], 0);
           if (kt < p.n_ext) {  // min-term tile: the tokens' sums and W's -64*dmin*m, both by TMA
-            mbar_arrive_expect_tx(&full_x[s], kXTileBytes + kWTileBytes);
-            tma_load_2d_sw(st + kWTileBytes, &xmap, p.K + kt * BK, m0, &full_x[s]);
-            tma_load_2d_sw(st, &emap, kt * BK, n0, &full_x[s]);
+            if (leader) mbar_arrive_expect_tx(&full_x[s], 2 * (kXTileBytes + kWTileBytes));
+            tma_load_2d_pair(st + kWTileBytes, &xmap, p.K + kt * BK, m0, fb);
+            tma_load_2d_pair(st, &emap, kt * BK, n0, fb);
           } else {
-            mbar_arrive_expect_tx(&full_x[s], kXTileBytes);
-            tma_load_2d_sw(st + kWTileBytes, &xmap, (kt - p.n_ext) * BK, m0, &full_x[s]);
+            if (leader) mbar_arrive_expect_tx(&full_x[s], 2 * kXTileBytes);
+            tma_load_2d_pair(st + kWTileBytes, &xmap, (kt - p.n_ext) * BK, m0, fb);
           }
           ++it;
         }
       }
-      // On an abort, let the copies still in flight land before the CTA can exit.
-      if (aborted())
-        for (int j = max(0, it - STAGES); j < it; ++j)
-          mbar_wait_bounded(&full_x[j % STAGES], static_cast<uint32_t>(j / STAGES) & 1u, kTcWaitNs);
     }
   } else if (warp == kMmaWarp) {
-    if (lane == 0) {
+    if (leader && lane == 0) {
       int it = 0, grp = 0;
       bool stop = false;
-      for (int tile = blockIdx.x; tile < p.tiles && !stop; tile += gridDim.x) {
+      for (int tile = pair; tile < p.tiles && !stop; tile += npairs) {
         for (int g = 0; g <= nsb && !stop; ++g, ++grp) {  // group 0: min term; 1..nsb: super-blocks
           const int buf = grp & 1;
-          if (grp >= 2 && !mbar_wait_bounded(&acc_empty[buf], static_cast<uint32_t>(grp / 2 - 1) & 1u, kTcWaitNs)) {
+          if (grp >= 2 &&
+              !mbar_wait_bounded(&acc_empty[buf], static_cast<uint32_t>(grp / 2 - 1) & 1u, kTcWaitNs)) {
             fail();
             stop = true;
             break;
@@ -295,73 +360,119 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t wa = smem_addr(smem + s * kStageBytes), xa = wa + kWTileBytes;
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
-              umma_f16(tmem + (uint32_t)(buf * TN), smem_desc_sw128(wa + 32 * kk), smem_desc_sw128(xa + 32 * kk),
-                       (kt != kt0 || kk != 0) ? 1u : 0u);
-            umma_commit(&empty[s]);
+              umma_pair_f16(tmem + (uint32_t)(buf * TN), smem_desc_sw128(wa + 32 * kk),
+                            smem_desc_sw128(xa + 32 * kk), (kt != kt0 || kk != 0) ? 1u : 0u);
+            umma_commit_pair(&empty[s]);
             ++it;
           }
-          if (!stop) umma_commit(&acc_full[buf]);
+          if (!stop) umma_commit_pair(&acc_full[buf]);
         }
       }
-      umma_commit(mma_done);  // the wait point for every MMA this thread issued
+      umma_commit_pair(mma_done);  // the wait point for every MMA this thread issued
       if (!mbar_wait_bounded(mma_done, 0u, kTcWaitNs)) fail();
-    }
-  } else if (warp >= kEpiWarps) {  // warps 8..9: unpack t = sc*q for rows u and u + 64
-    const int u = threadIdx.x - kDqBase;
-    int it = 0;
-    bool stop = false;
-    for (int tile = blockIdx.x; tile < p.tiles && !stop; tile += gridDim.x) {
-      const int n0 = (tile / p.m_tiles) * TM;
-      // rows past N repeat row N-1; their outputs are never stored
-      const uint8_t* rowa = p.w + (long long)min(n0 + u, p.N - 1) * p.row_bytes;
-      const uint8_t* rowb = p.w + (long long)min(n0 + u + 64, p.N - 1) * p.row_bytes;
-      RowChunk na, nb;
-      load_chunk(na, rowa, 0, true);
-      load_chunk(nb, rowb, 0, true);
-      // the unpacking reads each row from HBM one k-tile ahead, too late to hide its latency:
-      // keep the next few super-blocks of both rows on their way into L2
-      for (int j = 1; j <= kPrefetchBlocks && j < nsb; ++j) {
-        prefetch_block_l2(rowa, j);
-        prefetch_block_l2(rowb, j);
+    } else if (!leader && lane == 0) {
+      // forwarder: passes on, in order, each stage's "t written" and each group's "read out"
+      // (polling both sequences, so neither waits behind the other)
+      const int my_tiles = pair < p.tiles ? (p.tiles - 1 - pair) / npairs + 1 : 0;
+      const int ns = my_tiles * kt_tile, ng = my_tiles * (nsb + 1);
+      int i = 0, j = 0;
+      uint64_t t_last = globaltimer_ns();
+      while (i < ns || j < ng) {
+        bool moved = false;
+        if (i < ns && mbar_test_wait(&full_w[i % STAGES], static_cast<uint32_t>(i / STAGES) & 1u)) {
+          mbar_arrive_remote(cluster_addr(&full_w[i % STAGES], 0));
+          ++i;
+          moved = true;
+        }
+        if (j < ng && mbar_test_wait(&acc_empty[j & 1], static_cast<uint32_t>(j >> 1) & 1u)) {
+          mbar_arrive_remote(cluster_addr(&acc_empty[j & 1], 0));
+          ++j;
+          moved = true;
+        }
+        if (moved) {
+          t_last = globaltimer_ns();
+        } else if (aborted()) {
+          break;
+        } else if (globaltimer_ns() - t_last > kTcWaitNs) {
+          fail();
+          break;
+        }
       }
-      for (int kt = 0; kt < kt_tile; ++kt) {
-        const int s = it % STAGES;
-        const RowChunk ca = na, cb = nb;
-        const int km = kt - p.n_ext;  // main k-tile index, < 0 for min-term tiles
-        if (km >= 0 && km + 1 < kt_main) {  // next chunk's bytes in flight while this one unpacks
-          load_chunk(na, rowa, km + 1, ((km + 1) & 3) == 0);
-          load_chunk(nb, rowb, km + 1, ((km + 1) & 3) == 0);
-        }
-        if (km >= 0 && (km & 3) == 0 && (km >> 2) + kPrefetchBlocks + 1 < nsb) {
-          prefetch_block_l2(rowa, (km >> 2) + kPrefetchBlocks + 1);
-          prefetch_block_l2(rowb, (km >> 2) + kPrefetchBlocks + 1);
-        }
-        if (!stage_free(it)) { fail(); stop = true; break; }
-        if (aborted()) { stop = true; break; }
+    }
+   }
+  } else if (wg == 2) {  // warps 8..11: unpack t = sc*q, whole k-tiles (all 128 rows) in turn
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kDqRegs));
+    const int dw = warp - kDqBase;
+    // raw super-blocks in the order they are unpacked: item i = super-block i % nsb of the
+    // (i / nsb)-th tile of this pair
+    auto raw_issue = [&](int item) {
+      const int k = item / nsb, g = item - k * nsb;
+      const int tile = pair + k * npairs;
+      if (tile >= p.tiles) return;
+      const int n0 = (tile / p.m_tiles) * (2 * TM) + static_cast<int>(rank) * TM;
+      uint64_t* b = &raw_full[item % RAW_STAGES];
+      mbar_arrive_expect_tx(b, kRawBytes);
+      tma_load_2d(raw + (item % RAW_STAGES) * kRawBytes, &wmap, g * 36, n0, b);  // 36 words = 144 bytes
+    };
+    if (dw == 0 && lane == 0)
+      for (int i = 0; i < RAW_STAGES; ++i) raw_issue(i);
+    const int my_tiles = pair < p.tiles ? (p.tiles - 1 - pair) / npairs + 1 : 0;
+    const int total = my_tiles * kt_tile;
+    for (int it = dw; it < total; it += kDqWarps) {
+      const int tk = it / kt_tile, kt = it - tk * kt_tile;
+      const int s = it % STAGES;
+      const int km = kt - p.n_ext;  // main k-tile index, < 0 for min-term tiles
+      const int q = km >= 0 ? tk * nsb + (km >> 2) : 0;  // its raw super-block
+      const int slot = q % RAW_STAGES;
+      const uint32_t rpar = static_cast<uint32_t>(q / RAW_STAGES) & 1u;
+      // every lane waits; the outcome is made warp-uniform so that no lane leaves the loop alone
+      // (a lane that left would strand the others at the __syncwarp below)
+      bool ok = km < 0 || mbar_wait_bounded(&raw_full[slot], rpar, kTcWaitNs);
+      ok = ok && stage_free(it);
+      if (!__all_sync(0xFFFFFFFFu, ok)) {
+        if (lane == 0) fail();
+        break;
+      }
+      if (__any_sync(0xFFFFFFFFu, aborted())) break;
+      if (km >= 0) {
+        uint8_t* wt = smem + s * kStageBytes;
+        const uint8_t* rs = raw + slot * kRawBytes;
+#pragma unroll 1
+        for (int r = lane; r < TM; r += 32) unpack_row(rs, r, km & 3, wt);
+        fence_proxy_async_smem();  // generic-proxy smem writes -> visible to the tensor core
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_local(&full_w[s]);
         if (km >= 0) {
-          uint8_t* wt = smem + s * kStageBytes;
-          unpack_t(ca.h.y, ca.h.w, ca.a, ca.b, km & 3, wt, u);
-          unpack_t(cb.h.y, cb.h.w, cb.a, cb.b, km & 3, wt, u + 64);
-          fence_proxy_async_smem();  // generic-proxy smem writes -> visible to the tensor core
+          mbar_arrive_local(&raw_empty[slot]);
+          if ((km & 3) == 3) {  // the super-block's last k-tile: refill the slot once all four are done
+            if (!mbar_wait_bounded(&raw_empty[slot], rpar, kTcWaitNs)) {
+              fail();
+            } else {
+              fence_proxy_async_smem();
+              raw_issue(q + RAW_STAGES);
+            }
+          }
         }
-        mbar_arrive(&full_w[s]);
-        ++it;
       }
     }
   } else {  // warps 0..7: epilogue
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
     const int quarter = warp & 3, half = warp >> 2;
     int grp = 0;
     bool stop = false;
-    for (int tile = blockIdx.x; tile < p.tiles && !stop; tile += gridDim.x) {
-      const int m0 = (tile % p.m_tiles) * TN, n0 = (tile / p.m_tiles) * TM;
-      const int n = n0 + quarter * 32 + lane;
+    for (int tile = pair; tile < p.tiles && !stop; tile += npairs) {
+      // tensor-memory column c holds token m0 + c (rank 0's tokens, then rank 1's)
+      const int m0 = (tile % p.m_tiles) * TN;
+      const int n = (tile / p.m_tiles) * (2 * TM) + static_cast<int>(rank) * TM + quarter * 32 + lane;
       const uint8_t* rowp = p.w + (long long)min(n, p.N - 1) * p.row_bytes;
       float acc[TN / 2];
 #pragma unroll
       for (int c = 0; c < TN / 2; ++c) acc[c] = 0.f;
       // this warp's tokens' 2^-e_j, fetched now (their latency hides behind the first group)
       // and read back from shared memory by the stores at the end of the tile
-      float* winv = reinterpret_cast<float*>(smem + STAGES * kStageBytes + 1024) + warp * (TN / 2);
+      float* winv = inv_base + warp * (TN / 2);
       for (int c = lane; c < TN / 2; c += 32) winv[c] = p.inv_scale[m0 + half * (TN / 2) + c];
       for (int g = 0; g <= nsb; ++g, ++grp) {
         const int buf = grp & 1;
@@ -380,7 +491,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        if (lane == 0) mbar_arrive_local(&acc_empty[buf]);
       }
       if (stop) break;
       // Y[j][n] = acc * 2^-e_j: for each token, the warp's 32 lanes write 32 consecutive floats
@@ -400,11 +511,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
   }
+  // After an abort, copies issued before it may still be landing (their byte counts go to
+  // rank 0's barriers): give them time before either CTA can exit.
+  if (threadIdx.x == 0 && aborted()) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 200000ull) {
+    }
+  }
   tc_fence_before();
   __syncthreads();
+  cluster.sync();  // no remote arrival or MMA operand read is still aimed at either CTA
   if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc_pair(tmem, kTmemCols);
   }
 }
 
@@ -562,6 +681,50 @@ int encode_f16_2d(CUtensorMap* map, void* base, int cols, int rows, int box_rows
   return 0;
 }
 
+// Q4_K weight rows as a 2-D tensor of 4-byte words (rows of row_bytes), 36-word (one
+// super-block) x TM-row boxes, no swizzle: the raw stages the unpacking warps read.
+int encode_raw_w(CUtensorMap* map, const void* w, int N, long long row_bytes, std::string* err) {
+  void* fp = nullptr;
+  cudaDriverEntryPointQueryResult qr;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fp, 12000, cudaEnableDefault, &qr) != cudaSuccess ||
+      qr != cudaDriverEntryPointSuccess) {
+    *err = "cuTensorMapEncodeTiled is unavailable";
+    return -1;
+  }
+  EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(fp);
+  const cuuint64_t gdim[2] = {(cuuint64_t)(row_bytes / 4), (cuuint64_t)N};
+  const cuuint64_t gstride[1] = {(cuuint64_t)row_bytes};
+  const cuuint32_t box[2] = {36u, (cuuint32_t)TM};
+  const cuuint32_t es[2] = {1u, 1u};
+  const CUresult cr = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(w), gdim, gstride, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) {
+    *err = "cuTensorMapEncodeTiled failed for the weights (" + std::to_string((int)cr) + ")";
+    return -1;
+  }
+  return 0;
+}
+
+// Co-resident pairs of the prefill kernel (clusters of two CTAs at kTcSmem each), per device.
+int max_pairs(int num_sms) {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return num_sms / 2;
+  if (cache[dev] > 0) return cache[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = kTcSmem;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_q4k_tc_kernel, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return num_sms / 2;
+  }
+  cache[dev] = n;
+  return n;
+}
+
 }  // namespace
 
 size_t gemm_tc_workspace(int M, int N, int K) { return tc_layout(M, N, K).bytes; }
@@ -569,7 +732,7 @@ size_t gemm_tc_workspace(int M, int N, int K) { return tc_layout(M, N, K).bytes;
 int launch_gemm_tc(const void* w, const void* x, float* y, int M, int N, int K, long long row_bytes, void* ws,
                    int num_sms, cudaStream_t stream, std::string* err) {
   const TcLayout L = tc_layout(M, N, K);
-  const long long m_tiles = (M + TN - 1) / TN, n_tiles = (N + TM - 1) / TM;
+  const long long m_tiles = (M + TN - 1) / TN, n_tiles = (N + 2 * TM - 1) / (2 * TM);
   if (m_tiles * n_tiles > 0x7FFFFFFFLL) { *err = "M x N has too many output tiles"; return -1; }
   const long long prep_w_blocks = ((long long)N * (K / 256) + 255) / 256;
   if ((long long)M + prep_w_blocks > 0x7FFFFFFFLL) { *err = "M and N too large for the pre-pass grid"; return -1; }
@@ -582,15 +745,27 @@ int launch_gemm_tc(const void* w, const void* x, float* y, int M, int N, int K, 
       row_bytes);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) { *err = std::string("prefill pre-pass launch: ") + cudaGetErrorString(e); return -1; }
-  CUtensorMap xmap, emap;
-  if (encode_f16_2d(&xmap, xc, L.kc_x, M, TN, err) || encode_f16_2d(&emap, wext, L.k_ext, N, TM, err)) return -1;
+  CUtensorMap xmap, emap, wmap;
+  if (encode_f16_2d(&xmap, xc, L.kc_x, M, TN / 2, err) || encode_f16_2d(&emap, wext, L.k_ext, N, TM, err) ||
+      encode_raw_w(&wmap, w, N, row_bytes, err))
+    return -1;
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
+  if (dev >= 64 || !attr_done[dev]) {
     e = cudaFuncSetAttribute(gemm_q4k_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
     if (e != cudaSuccess) { *err = std::string("cudaFuncSetAttribute (gemm): ") + cudaGetErrorString(e); return -1; }
-    attr_done[dev] = true;
+    // the warpgroups' register budgets add up to exactly 512 threads x kLaunchRegs: a build
+    // that starts the CTA with fewer registers would leave the epilogue's increase waiting forever
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, gemm_q4k_tc_kernel);
+    if (e != cudaSuccess) { *err = std::string("cudaFuncGetAttributes (gemm): ") + cudaGetErrorString(e); return -1; }
+    if (fa.numRegs != kLaunchRegs) {
+      *err = "internal: the prefill kernel was built with " + std::to_string(fa.numRegs) + " registers per thread, not " +
+             std::to_string(kLaunchRegs);
+      return -1;
+    }
+    if (dev < 64) attr_done[dev] = true;
   }
   TcParams prm;
   prm.w = static_cast<const uint8_t*>(w);
@@ -603,8 +778,8 @@ int launch_gemm_tc(const void* w, const void* x, float* y, int M, int N, int K, 
   prm.n_ext = L.k_ext / BK;
   prm.m_tiles = (int)m_tiles;
   prm.tiles = (int)(m_tiles * n_tiles);
-  const int grid = (int)std::min<long long>(prm.tiles, num_sms);
-  gemm_q4k_tc_kernel<<<grid, kTcThreads, kTcSmem, stream>>>(xmap, emap, prm);
+  const int pairs = (int)std::min<long long>(prm.tiles, max_pairs(num_sms));
+  gemm_q4k_tc_kernel<<<2 * pairs, kTcThreads, kTcSmem, stream>>>(xmap, emap, wmap, prm);
   e = cudaGetLastError();
   if (e != cudaSuccess) { *err = std::string("gemm launch: ") + cudaGetErrorString(e); return -1; }
   return 0;

@@ -53,11 +53,12 @@ def run_gemm(kq, blocks, x_bits, N, K):
     return y.cpu().numpy().astype(np.float64)
 
 
-# (M, N, K) of the tensor-core route (M > 32): one tile; ragged M (tails of 33, 72 and 1 tokens); ragged N (tails of 8 and 232
-# rows); several K super-blocks; more tiles than SMs; N % 4 != 0 (rows not 16-byte aligned:
-# the direct-store path) with an odd number of 128-row tiles (a cluster CTA with no rows).
+# (M, N, K) of the tensor-core route (M > 32): one tile; ragged M (tails of 33, 72, 1 and 16
+# tokens); ragged N (tails of 8 and 232 rows of a 256-row pair tile, where rank 1 of the pair
+# has no rows); several K super-blocks; N % 4 != 0 (rows not 16-byte aligned); more pair tiles
+# (80) than co-resident pairs, so some pairs take a second tile.
 SHAPES = [(33, 256, 256), (200, 520, 1024), (129, 300, 512), (257, 1000, 2560), (384, 2048, 768),
-          (130, 258, 512)]
+          (130, 258, 512), (784, 5120, 256)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
