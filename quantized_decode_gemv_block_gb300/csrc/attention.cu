@@ -32,6 +32,8 @@ namespace {
 constexpr int kChunk = 128;
 constexpr int kAttnThreads = 256;  // 8 warps x 16 query rows
 constexpr int kAttnMaxRows = 128;
+// from this many 16-row blocks on, each warp takes whole row blocks (same arithmetic)
+constexpr int kRowSplitBlocks = 4;
 
 struct AttnParams {
   const float* q;      // M rows of n_q*hd, q_stride apart
@@ -65,35 +67,88 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 __device__ __forceinline__ float bf16_rn_f(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 
+// 16-byte asynchronous copy global -> shared; src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// o = P V for one warp's NP pieces: row block rb, dimension groups dg0 + j*dstride (j < NP),
+// each summed over the chunk's 128 positions in order (hi part, then lo part, per 16).
+template <int HD, int NP>
+__device__ __forceinline__ void pv_pieces(const uint16_t* Ph, const uint16_t* Pl, const uint16_t* Vs, int rb, int dg0,
+                                          int dstride, int lane, float* base, int R) {
+  constexpr int LD = HD + 8, PLD = kChunk + 8, DW = HD / (kAttnThreads / 32), NDT = DW / 8;
+  float acc[NP][NDT][4];
+#pragma unroll
+  for (int j = 0; j < NP; ++j)
+#pragma unroll
+    for (int dt = 0; dt < NDT; ++dt) acc[j][dt][0] = acc[j][dt][1] = acc[j][dt][2] = acc[j][dt][3] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < kChunk / 16; ++kk) {
+    uint32_t ah[4], al[4];
+    ldsm_x4(ah, Ph + (16 * rb + (lane & 15)) * PLD + kk * 16 + (lane >> 4) * 8);
+    ldsm_x4(al, Pl + (16 * rb + (lane & 15)) * PLD + kk * 16 + (lane >> 4) * 8);
+#pragma unroll
+    for (int j = 0; j < NP; ++j)
+#pragma unroll
+      for (int dt = 0; dt < NDT; ++dt) {
+        uint32_t b0, b1;
+        ldsm_x2_t(b0, b1, Vs + (kk * 16 + (lane & 15)) * LD + (dg0 + j * dstride) * DW + dt * 8);
+        mma_bf16_16816(acc[j][dt], ah, b0, b1, acc[j][dt]);
+        mma_bf16_16816(acc[j][dt], al, b0, b1, acc[j][dt]);
+      }
+  }
+  const int g = lane >> 2, q4 = lane & 3, ra = 16 * rb + g, rbb = ra + 8;
+#pragma unroll
+  for (int j = 0; j < NP; ++j)
+#pragma unroll
+    for (int dt = 0; dt < NDT; ++dt) {
+      const int d = (dg0 + j * dstride) * DW + dt * 8 + 2 * q4;
+      if (ra < R) *reinterpret_cast<float2*>(base + (long long)ra * (HD + 2) + d) = make_float2(acc[j][dt][0], acc[j][dt][1]);
+      if (rbb < R) *reinterpret_cast<float2*>(base + (long long)rbb * (HD + 2) + d) = make_float2(acc[j][dt][2], acc[j][dt][3]);
+    }
+}
+
+// One CTA per (chunk, kv head); all eight warps take part at any M. Warp w copies chunk rows
+// 16w..16w+15 of K and V asynchronously (V lands behind the K work). For each 16-row block of
+// query rows, warp w forms S = Q K^T for its 16 positions; the chunk's row maxima meet in
+// shared memory, and each warp writes p = exp(s - m) for its positions (bf16 hi / lo parts)
+// and its partial row sums. The warps then share o = P V by pieces of 16 rows x HD/8
+// dimensions, the row blocks padded to a power of two so that a warp keeps one row block
+// (padding rows are never stored; MMA rows are independent). Every sum runs in an order fixed
+// by positions (never by M), and which warp takes a piece changes nothing in its arithmetic.
 template <int HD>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_chunk_kernel(const AttnParams p) {
-  constexpr int LD = HD + 8;  // shared row stride (elements): 16-byte pad, conflict-free ldmatrix
+  constexpr int LD = HD + 8;       // shared row stride (elements): 16-byte pad, conflict-free ldmatrix
+  constexpr int PLD = kChunk + 8;  // the same for P
+  constexpr int NW = kAttnThreads / 32;
+  static_assert(kChunk == 16 * NW, "16 positions per warp");
+  static_assert((HD / NW) % 8 == 0, "whole 8-wide MMA tiles per warp");
   extern __shared__ __align__(16) uint16_t asmem[];
-  uint16_t* Qs = asmem;                  // [128][LD]
-  uint16_t* Ks = Qs + kAttnMaxRows * LD;  // [kChunk][LD]
-  uint16_t* Vs = Ks + kChunk * LD;        // [kChunk][LD]
+  uint16_t* Qs = asmem;                       // [128][LD]
+  uint16_t* Ks = Qs + kAttnMaxRows * LD;      // [kChunk][LD]
+  uint16_t* Vs = Ks + kChunk * LD;            // [kChunk][LD]
+  uint16_t* Ph = Vs + kChunk * LD;            // [128][PLD]: P rounded to bf16
+  uint16_t* Pl = Ph + kAttnMaxRows * PLD;     // [128][PLD]: P - hi, rounded to bf16
+  float* red_m = reinterpret_cast<float*>(Pl + kAttnMaxRows * PLD);  // [NW][128]: per-warp row maxima
+  float* red_l = red_m + NW * kAttnMaxRows;                          // [NW][128]: per-warp row sums
+  // the combine kernel may be launched now; it waits for this grid before reading anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int c = blockIdx.x, kvh = blockIdx.y;
   const int pos0 = c * kChunk;
   const int npos = min(kChunk, p.L + p.M - pos0);
   const int wcol = p.L - pos0;  // column of window position 0: columns before it are cached positions
   const int kvw = p.n_kv * HD, qw = p.q_stride;
-  const int rows16 = (p.R + 15) & ~15;
+  const int rows16 = (p.R + 15) & ~15, nrb = rows16 / 16;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q4 = lane & 3;
 
-  // every load of the chunk's K and V rows and of the Q rows leaves before the first store
-  constexpr int KV_PER_T = kChunk * (HD / 8) / kAttnThreads;      // 16-byte pieces per thread
+  // the Q rows of the head group (fp32), loads first; rows R..rows16-1 as zeros
   constexpr int Q_PER_T = kAttnMaxRows * (HD / 4) / kAttnThreads;  // float4 pieces per thread
-  uint4 kv[KV_PER_T], vv[KV_PER_T];
   float4 qf[Q_PER_T];
-#pragma unroll
-  for (int t = 0; t < KV_PER_T; ++t) {
-    const int e = threadIdx.x + t * kAttnThreads, r = e / (HD / 8), c8 = e - r * (HD / 8);
-    kv[t] = vv[t] = make_uint4(0u, 0u, 0u, 0u);
-    if (r < npos) {
-      const long long off = (long long)(pos0 + r) * kvw + kvh * HD + c8 * 8;
-      kv[t] = ldg128(p.k + off);
-      vv[t] = ldg128(p.v + off);
-    }
-  }
 #pragma unroll
   for (int t = 0; t < Q_PER_T; ++t) {
     const int e = threadIdx.x + t * kAttnThreads, r = e / (HD / 4), c4 = e - r * (HD / 4);
@@ -103,12 +158,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_chunk_kernel(const AttnP
       qf[t] = __ldg(reinterpret_cast<const float4*>(p.q + (long long)i * qw + hq * HD + c4 * 4));
     }
   }
+  // this warp's 16 K rows (group 0) and 16 V rows (group 1); rows past the chunk read zeros
+  constexpr int PIECES = 16 * (HD / 8) / 32;  // 16-byte pieces per lane per matrix
 #pragma unroll
-  for (int t = 0; t < KV_PER_T; ++t) {
-    const int e = threadIdx.x + t * kAttnThreads, r = e / (HD / 8), c8 = e - r * (HD / 8);
-    *reinterpret_cast<uint4*>(Ks + r * LD + c8 * 8) = kv[t];
-    *reinterpret_cast<uint4*>(Vs + r * LD + c8 * 8) = vv[t];
+  for (int t = 0; t < PIECES; ++t) {
+    const int e = lane + 32 * t, r = 16 * warp + e / (HD / 8), c8 = e % (HD / 8);
+    const bool in = r < npos;
+    const long long off = in ? (long long)(pos0 + r) * kvw + kvh * HD + c8 * 8 : 0;
+    cp_async16(Ks + r * LD + c8 * 8, p.k + off, in ? 16u : 0u);
   }
+  cp_async_commit();
+#pragma unroll
+  for (int t = 0; t < PIECES; ++t) {
+    const int e = lane + 32 * t, r = 16 * warp + e / (HD / 8), c8 = e % (HD / 8);
+    const bool in = r < npos;
+    const long long off = in ? (long long)(pos0 + r) * kvw + kvh * HD + c8 * 8 : 0;
+    cp_async16(Vs + r * LD + c8 * 8, p.v + off, in ? 16u : 0u);
+  }
+  cp_async_commit();
 #pragma unroll
   for (int t = 0; t < Q_PER_T; ++t) {
     const int e = threadIdx.x + t * kAttnThreads, r = e / (HD / 4), c4 = e - r * (HD / 4);
@@ -117,105 +184,221 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_chunk_kernel(const AttnP
           make_uint2(pack_bf16(qf[t].x, qf[t].y), pack_bf16(qf[t].z, qf[t].w));
   }
   __syncthreads();
+  float* base = p.part + ((long long)kvh * p.nchunks + c) * p.R * (HD + 2);
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q4 = lane & 3;
-  if (16 * warp >= p.R) return;  // no rows for this warp (uniform)
-  const int r0 = 16 * warp;
-
-  // S = Q K^T for this warp's 16 rows and the chunk's kChunk positions
-  float s[kChunk / 8][4];
+  if (nrb >= kRowSplitBlocks) {
+    // Many rows: warp w takes row block w over all 128 positions (S, p and P V in registers),
+    // with the same arithmetic as the position split below: the same MMAs, an exact maximum,
+    // and each row sum formed per 16 positions (4 values per thread, then the quad butterfly)
+    // and added in position-group order.
+    cp_async_wait<0>();
+    __syncthreads();  // all K and V rows
+    if (warp < nrb) {
+      const int r0 = 16 * warp;
+      float sr[kChunk / 8][4];
 #pragma unroll
-  for (int nt = 0; nt < kChunk / 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+      for (int nt = 0; nt < kChunk / 8; ++nt) sr[nt][0] = sr[nt][1] = sr[nt][2] = sr[nt][3] = 0.f;
 #pragma unroll
-  for (int kk = 0; kk < HD / 16; ++kk) {
-    uint32_t a[4];
-    ldsm_x4(a, Qs + (r0 + (lane & 15)) * LD + kk * 16 + (lane >> 4) * 8);
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        uint32_t a[4];
+        ldsm_x4(a, Qs + (r0 + (lane & 15)) * LD + kk * 16 + (lane >> 4) * 8);
 #pragma unroll
-    for (int nt = 0; nt < kChunk / 8; ++nt) {
-      uint32_t b0, b1;
-      ldsm_x2(b0, b1, Ks + (nt * 8 + (lane & 7)) * LD + kk * 16 + ((lane >> 3) & 1) * 8);
-      mma_bf16_16816(s[nt], a, b0, b1, s[nt]);
+        for (int nt = 0; nt < kChunk / 8; ++nt) {
+          uint32_t b0, b1;
+          ldsm_x2(b0, b1, Ks + (nt * 8 + (lane & 7)) * LD + kk * 16 + ((lane >> 3) & 1) * 8);
+          mma_bf16_16816(sr[nt], a, b0, b1, sr[nt]);
+        }
+      }
+      const int ra = r0 + g, rbb = ra + 8;
+      const int ia = ra / p.group, ib = rbb / p.group;
+      const uint32_t ma = p.mask ? __ldg(p.mask + min(ia, p.M - 1)) : (ia >= 31 ? 0xFFFFFFFFu : ((2u << ia) - 1u));
+      const uint32_t mb = p.mask ? __ldg(p.mask + min(ib, p.M - 1)) : (ib >= 31 ? 0xFFFFFFFFu : ((2u << ib) - 1u));
+      float mxa = -INFINITY, mxb = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < kChunk / 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int col = nt * 8 + 2 * q4 + e, jw = col - wcol;
+          const bool va = ra < p.R && col < npos && (jw < 0 || ((ma >> jw) & 1u));
+          const bool vb = rbb < p.R && col < npos && (jw < 0 || ((mb >> jw) & 1u));
+          sr[nt][e] = va ? sr[nt][e] * p.scale : -INFINITY;
+          sr[nt][2 + e] = vb ? sr[nt][2 + e] * p.scale : -INFINITY;
+          mxa = fmaxf(mxa, sr[nt][e]);
+          mxb = fmaxf(mxb, sr[nt][2 + e]);
+        }
+#pragma unroll
+      for (int o = 1; o <= 2; o <<= 1) {
+        mxa = fmaxf(mxa, __shfl_xor_sync(0xFFFFFFFFu, mxa, o));
+        mxb = fmaxf(mxb, __shfl_xor_sync(0xFFFFFFFFu, mxb, o));
+      }
+      const float ca = mxa == -INFINITY ? 0.f : mxa, cb = mxb == -INFINITY ? 0.f : mxb;
+      float la = 0.f, lb = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {  // position group w: tiles 2w, 2w + 1
+        float pa = 0.f, pb = 0.f;
+#pragma unroll
+        for (int nt = 2 * w; nt < 2 * w + 2; ++nt) {
+          sr[nt][0] = __expf(sr[nt][0] - ca);
+          sr[nt][1] = __expf(sr[nt][1] - ca);
+          sr[nt][2] = __expf(sr[nt][2] - cb);
+          sr[nt][3] = __expf(sr[nt][3] - cb);
+          pa += sr[nt][0];
+          pa += sr[nt][1];
+          pb += sr[nt][2];
+          pb += sr[nt][3];
+        }
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+          pa += __shfl_xor_sync(0xFFFFFFFFu, pa, o);
+          pb += __shfl_xor_sync(0xFFFFFFFFu, pb, o);
+        }
+        if (w == 0) {
+          la = pa;
+          lb = pb;
+        } else {
+          la += pa;
+          lb += pb;
+        }
+      }
+      // o = P V over all dimensions, P = hi + lo in bf16 straight from the S fragments
+      float acc[HD / 8][4];
+#pragma unroll
+      for (int dt = 0; dt < HD / 8; ++dt) acc[dt][0] = acc[dt][1] = acc[dt][2] = acc[dt][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < kChunk / 16; ++kk) {
+        const float* p0 = sr[2 * kk];
+        const float* p1 = sr[2 * kk + 1];
+        const float h0 = bf16_rn_f(p0[0]), h1 = bf16_rn_f(p0[1]), h2 = bf16_rn_f(p0[2]), h3 = bf16_rn_f(p0[3]);
+        const float h4 = bf16_rn_f(p1[0]), h5 = bf16_rn_f(p1[1]), h6 = bf16_rn_f(p1[2]), h7 = bf16_rn_f(p1[3]);
+        const uint32_t ah[4] = {pack_bf16(h0, h1), pack_bf16(h2, h3), pack_bf16(h4, h5), pack_bf16(h6, h7)};
+        const uint32_t al[4] = {pack_bf16(p0[0] - h0, p0[1] - h1), pack_bf16(p0[2] - h2, p0[3] - h3),
+                                pack_bf16(p1[0] - h4, p1[1] - h5), pack_bf16(p1[2] - h6, p1[3] - h7)};
+#pragma unroll
+        for (int dt = 0; dt < HD / 8; ++dt) {
+          uint32_t b0, b1;
+          ldsm_x2_t(b0, b1, Vs + (kk * 16 + (lane & 15)) * LD + dt * 8);
+          mma_bf16_16816(acc[dt], ah, b0, b1, acc[dt]);
+          mma_bf16_16816(acc[dt], al, b0, b1, acc[dt]);
+        }
+      }
+#pragma unroll
+      for (int dt = 0; dt < HD / 8; ++dt) {
+        const int d = dt * 8 + 2 * q4;
+        if (ra < p.R) *reinterpret_cast<float2*>(base + (long long)ra * (HD + 2) + d) = make_float2(acc[dt][0], acc[dt][1]);
+        if (rbb < p.R) *reinterpret_cast<float2*>(base + (long long)rbb * (HD + 2) + d) = make_float2(acc[dt][2], acc[dt][3]);
+      }
+      if (q4 == 0) {
+        if (ra < p.R) *reinterpret_cast<float2*>(base + (long long)ra * (HD + 2) + HD) = make_float2(mxa, la);
+        if (rbb < p.R) *reinterpret_cast<float2*>(base + (long long)rbb * (HD + 2) + HD) = make_float2(mxb, lb);
+      }
     }
+    return;
   }
 
-  // scale, visibility, row maxima (rows g and g+8 of the block; a quad shares a row)
-  const int ra = r0 + g, rb = r0 + g + 8;
-  const int ia = ra / p.group, ib = rb / p.group;
-  // window positions each row's token may see: bit j for window position j
-  const uint32_t ma = p.mask ? __ldg(p.mask + min(ia, p.M - 1)) : (ia >= 31 ? 0xFFFFFFFFu : ((2u << ia) - 1u));
-  const uint32_t mb = p.mask ? __ldg(p.mask + min(ib, p.M - 1)) : (ib >= 31 ? 0xFFFFFFFFu : ((2u << ib) - 1u));
-  float mxa = -INFINITY, mxb = -INFINITY;
+  cp_async_wait<1>();  // this lane's K pieces
+  __syncwarp();        // ... and the warp's
+
+  for (int rb = 0; rb < nrb; ++rb) {
+    // S = Q K^T for this row block and positions 16w.. (two 8-wide tiles)
+    float s[2][4];
 #pragma unroll
-  for (int nt = 0; nt < kChunk / 8; ++nt)
+    for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int col = nt * 8 + 2 * q4 + e, jw = col - wcol;  // jw: window position, if >= 0
-      const bool va = ra < p.R && col < npos && (jw < 0 || ((ma >> jw) & 1u));
-      const bool vb = rb < p.R && col < npos && (jw < 0 || ((mb >> jw) & 1u));
-      s[nt][e] = va ? s[nt][e] * p.scale : -INFINITY;
-      s[nt][2 + e] = vb ? s[nt][2 + e] * p.scale : -INFINITY;
-      mxa = fmaxf(mxa, s[nt][e]);
-      mxb = fmaxf(mxb, s[nt][2 + e]);
+    for (int kk = 0; kk < HD / 16; ++kk) {
+      uint32_t a[4];
+      ldsm_x4(a, Qs + (16 * rb + (lane & 15)) * LD + kk * 16 + (lane >> 4) * 8);
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        uint32_t b0, b1;
+        ldsm_x2(b0, b1, Ks + (16 * warp + nt * 8 + (lane & 7)) * LD + kk * 16 + ((lane >> 3) & 1) * 8);
+        mma_bf16_16816(s[nt], a, b0, b1, s[nt]);
+      }
     }
+    // scale, visibility, this warp's row maxima over its 16 positions
+    const int ra = 16 * rb + g, rbb = ra + 8;
+    const int ia = ra / p.group, ib = rbb / p.group;
+    // window positions each row's token may see: bit j for window position j
+    const uint32_t ma = p.mask ? __ldg(p.mask + min(ia, p.M - 1)) : (ia >= 31 ? 0xFFFFFFFFu : ((2u << ia) - 1u));
+    const uint32_t mb = p.mask ? __ldg(p.mask + min(ib, p.M - 1)) : (ib >= 31 ? 0xFFFFFFFFu : ((2u << ib) - 1u));
+    float mxa = -INFINITY, mxb = -INFINITY;
 #pragma unroll
-  for (int o = 1; o <= 2; o <<= 1) {
-    mxa = fmaxf(mxa, __shfl_xor_sync(0xFFFFFFFFu, mxa, o));
-    mxb = fmaxf(mxb, __shfl_xor_sync(0xFFFFFFFFu, mxb, o));
-  }
-  const float ca = mxa == -INFINITY ? 0.f : mxa, cb = mxb == -INFINITY ? 0.f : mxb;
-  float la = 0.f, lb = 0.f;
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-  for (int nt = 0; nt < kChunk / 8; ++nt)
+      for (int e = 0; e < 2; ++e) {
+        const int col = 16 * warp + nt * 8 + 2 * q4 + e, jw = col - wcol;  // jw: window position, if >= 0
+        const bool va = ra < p.R && col < npos && (jw < 0 || ((ma >> jw) & 1u));
+        const bool vb = rbb < p.R && col < npos && (jw < 0 || ((mb >> jw) & 1u));
+        s[nt][e] = va ? s[nt][e] * p.scale : -INFINITY;
+        s[nt][2 + e] = vb ? s[nt][2 + e] * p.scale : -INFINITY;
+        mxa = fmaxf(mxa, s[nt][e]);
+        mxb = fmaxf(mxb, s[nt][2 + e]);
+      }
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
+    for (int o = 1; o <= 2; o <<= 1) {
+      mxa = fmaxf(mxa, __shfl_xor_sync(0xFFFFFFFFu, mxa, o));
+      mxb = fmaxf(mxb, __shfl_xor_sync(0xFFFFFFFFu, mxb, o));
+    }
+    if (q4 == 0) {
+      red_m[warp * kAttnMaxRows + ra] = mxa;
+      red_m[warp * kAttnMaxRows + rbb] = mxb;
+    }
+    __syncthreads();
+    // p = exp(s - m), m the chunk's row maximum (a maximum: exact in any order)
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      mxa = fmaxf(mxa, red_m[w * kAttnMaxRows + ra]);
+      mxb = fmaxf(mxb, red_m[w * kAttnMaxRows + rbb]);
+    }
+    const float ca = mxa == -INFINITY ? 0.f : mxa, cb = mxb == -INFINITY ? 0.f : mxb;
+    float la = 0.f, lb = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
       // the fast exponential (relative error ~2^-21, far inside the contract's 1e-4; the same
-      // instruction for every M): one warp runs the chunk at small M, and the accurate expf
-      // made this loop the kernel's longest phase. exp(-inf) = 0 for positions not seen.
-      s[nt][e] = __expf(s[nt][e] - ca);
-      s[nt][2 + e] = __expf(s[nt][2 + e] - cb);
-      la += s[nt][e];
-      lb += s[nt][2 + e];
+      // instruction for every M); exp(-inf) = 0 for positions not seen
+      const float p0 = __expf(s[nt][0] - ca), p1 = __expf(s[nt][1] - ca);
+      const float p2 = __expf(s[nt][2] - cb), p3 = __expf(s[nt][3] - cb);
+      la += p0;
+      la += p1;
+      lb += p2;
+      lb += p3;
+      const int col = 16 * warp + nt * 8 + 2 * q4;
+      const float h0 = bf16_rn_f(p0), h1 = bf16_rn_f(p1), h2 = bf16_rn_f(p2), h3 = bf16_rn_f(p3);
+      *reinterpret_cast<uint32_t*>(Ph + ra * PLD + col) = pack_bf16(h0, h1);
+      *reinterpret_cast<uint32_t*>(Ph + rbb * PLD + col) = pack_bf16(h2, h3);
+      *reinterpret_cast<uint32_t*>(Pl + ra * PLD + col) = pack_bf16(p0 - h0, p1 - h1);
+      *reinterpret_cast<uint32_t*>(Pl + rbb * PLD + col) = pack_bf16(p2 - h2, p3 - h3);
     }
 #pragma unroll
-  for (int o = 1; o <= 2; o <<= 1) {
-    la += __shfl_xor_sync(0xFFFFFFFFu, la, o);
-    lb += __shfl_xor_sync(0xFFFFFFFFu, lb, o);
-  }
-
-  // o = P V, P = hi + lo in bf16; the accumulator fragment of S is the A fragment of P
-  float acc[HD / 8][4];
-#pragma unroll
-  for (int dt = 0; dt < HD / 8; ++dt) acc[dt][0] = acc[dt][1] = acc[dt][2] = acc[dt][3] = 0.f;
-#pragma unroll
-  for (int kk = 0; kk < kChunk / 16; ++kk) {
-    const float* p0 = s[2 * kk];
-    const float* p1 = s[2 * kk + 1];
-    const float hi0 = bf16_rn_f(p0[0]), hi1 = bf16_rn_f(p0[1]), hi2 = bf16_rn_f(p0[2]), hi3 = bf16_rn_f(p0[3]);
-    const float hi4 = bf16_rn_f(p1[0]), hi5 = bf16_rn_f(p1[1]), hi6 = bf16_rn_f(p1[2]), hi7 = bf16_rn_f(p1[3]);
-    const uint32_t ah[4] = {pack_bf16(hi0, hi1), pack_bf16(hi2, hi3), pack_bf16(hi4, hi5), pack_bf16(hi6, hi7)};
-    const uint32_t al[4] = {pack_bf16(p0[0] - hi0, p0[1] - hi1), pack_bf16(p0[2] - hi2, p0[3] - hi3),
-                            pack_bf16(p1[0] - hi4, p1[1] - hi5), pack_bf16(p1[2] - hi6, p1[3] - hi7)};
-#pragma unroll
-    for (int dt = 0; dt < HD / 8; ++dt) {
-      uint32_t b0, b1;
-      ldsm_x2_t(b0, b1, Vs + (kk * 16 + (lane & 15)) * LD + dt * 8);
-      mma_bf16_16816(acc[dt], ah, b0, b1, acc[dt]);
-      mma_bf16_16816(acc[dt], al, b0, b1, acc[dt]);
+    for (int o = 1; o <= 2; o <<= 1) {
+      la += __shfl_xor_sync(0xFFFFFFFFu, la, o);
+      lb += __shfl_xor_sync(0xFFFFFFFFu, lb, o);
+    }
+    if (q4 == 0) {
+      red_l[warp * kAttnMaxRows + ra] = la;
+      red_l[warp * kAttnMaxRows + rbb] = lb;
     }
   }
+  cp_async_wait<0>();  // this lane's V pieces
+  __syncthreads();     // every warp's V rows, P and row sums
 
-  // the chunk's partial: unnormalised o, its row maximum and sum
-  constexpr int PW = HD + 2;
-  float* base = p.part + ((long long)kvh * p.nchunks + c) * p.R * PW;
+  // o = P V: row blocks padded to nrbp (a power of two); warp w takes row block w % nrbp and
+  // dimension groups w / nrbp + (NW / nrbp) j, j < nrbp
+  const int nrbp = nrb <= 1 ? 1 : nrb <= 2 ? 2 : nrb <= 4 ? 4 : 8;
+  const int prb = warp % nrbp, dg0 = warp / nrbp, dstride = NW / nrbp;
+  if (nrbp == 1) pv_pieces<HD, 1>(Ph, Pl, Vs, prb, dg0, dstride, lane, base, p.R);
+  else if (nrbp == 2) pv_pieces<HD, 2>(Ph, Pl, Vs, prb, dg0, dstride, lane, base, p.R);
+  else if (nrbp == 4) pv_pieces<HD, 4>(Ph, Pl, Vs, prb, dg0, dstride, lane, base, p.R);
+  else pv_pieces<HD, 8>(Ph, Pl, Vs, prb, dg0, dstride, lane, base, p.R);
+
+  // ... the chunk's row maximum and sum (the warps' sums added in warp order)
+  for (int r = threadIdx.x; r < p.R; r += kAttnThreads) {
+    float m = red_m[r], l = red_l[r];
 #pragma unroll
-  for (int dt = 0; dt < HD / 8; ++dt) {
-    const int d = dt * 8 + 2 * q4;
-    if (ra < p.R) *reinterpret_cast<float2*>(base + (long long)ra * PW + d) = make_float2(acc[dt][0], acc[dt][1]);
-    if (rb < p.R) *reinterpret_cast<float2*>(base + (long long)rb * PW + d) = make_float2(acc[dt][2], acc[dt][3]);
-  }
-  if (q4 == 0) {
-    if (ra < p.R) *reinterpret_cast<float2*>(base + (long long)ra * PW + HD) = make_float2(mxa, la);
-    if (rb < p.R) *reinterpret_cast<float2*>(base + (long long)rb * PW + HD) = make_float2(mxb, lb);
+    for (int w = 1; w < NW; ++w) {
+      m = fmaxf(m, red_m[w * kAttnMaxRows + r]);
+      l += red_l[w * kAttnMaxRows + r];
+    }
+    *reinterpret_cast<float2*>(base + (long long)r * (HD + 2) + HD) = make_float2(m, l);
   }
 }
 
@@ -239,6 +422,9 @@ __global__ void __launch_bounds__(HD * kCombGroups) attn_combine_kernel(const At
   __shared__ float sm_num[kCombGroups][HD], sm_den[kCombGroups];
   const int r = blockIdx.x, kvh = blockIdx.y, t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int grp = t / HD, d = t - grp * HD;
+  // launched while the chunk kernel runs (programmatic dependent launch): its partials are
+  // complete and visible once this returns
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const float* base = p.part + (long long)kvh * p.nchunks * p.R * PW + (long long)r * PW;
   const long long cs = (long long)p.R * PW;
   // the partials of this thread's first eight chunks: their loads do not depend on the
@@ -320,8 +506,9 @@ int attn_chunks(int L, int M) { return (L + M + kChunk - 1) / kChunk; }
 
 template <int HD>
 int launch_attn(const AttnParams& prm, cudaStream_t s, std::string* err) {
-  constexpr int LD = HD + 8;
-  const size_t smem = (size_t)(kAttnMaxRows + 2 * kChunk) * LD * 2;
+  constexpr int LD = HD + 8, PLD = kChunk + 8;
+  const size_t smem = (size_t)(kAttnMaxRows + 2 * kChunk) * LD * 2 + (size_t)2 * kAttnMaxRows * PLD * 2 +
+                      (size_t)2 * (kAttnThreads / 32) * kAttnMaxRows * 4;
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -335,9 +522,18 @@ int launch_attn(const AttnParams& prm, cudaStream_t s, std::string* err) {
   }
   attn_chunk_kernel<HD><<<dim3(prm.nchunks, prm.n_kv), kAttnThreads, smem, s>>>(prm);
   cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess) {
-    attn_combine_kernel<HD><<<dim3(prm.R, prm.n_kv), HD * kCombGroups, 0, s>>>(prm);
-    e = cudaGetLastError();
+  if (e == cudaSuccess) {  // the combine starts while the chunks run and waits for them
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(prm.R, prm.n_kv, 1);
+    cfg.blockDim = dim3(HD * kCombGroups, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, attn_combine_kernel<HD>, prm);
   }
   if (e != cudaSuccess) {
     *err = std::string("attention launch: ") + cudaGetErrorString(e);

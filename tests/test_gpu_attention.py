@@ -82,10 +82,13 @@ def test_tree_mask_and_tokens_that_see_nothing(built, orc):
 
 
 def test_a_tokens_output_is_the_same_for_every_window_size(built):
+    """Bit equality across window sizes, including across the kernel's two work splits (warps
+    over positions for up to 3 row blocks of 16 query rows, warps over row blocks from 4 on:
+    M <= 12 and M >= 13 here, with 4 query rows per token)."""
     L, n_q, n_kv, hd = 777, 16, 4, 128
     q, k, v = make(32, L, n_q, n_kv, hd, seed=11)
-    full = run(q[:8], k[:L + 8], v[:L + 8], L, n_q, n_kv, hd, 0.0883)
-    for M in (1, 3, 5, 8):
+    full = run(q[:32], k[:L + 32], v[:L + 32], L, n_q, n_kv, hd, 0.0883)
+    for M in (1, 3, 5, 8, 12, 13, 20, 24):
         o = run(q[:M], k[:L + M], v[:L + M], L, n_q, n_kv, hd, 0.0883)
         assert np.array_equal(o.view(np.uint32), full[:M].view(np.uint32)), f"M={M}"
 
