@@ -20,7 +20,6 @@ namespace {
 
 constexpr int kThreadsF = 256;
 constexpr int kRowsPerWarp = 2;
-constexpr int kRowsPerCtaF = 8 * kRowsPerWarp;
 
 __device__ __forceinline__ uint32_t ldg16(const void* p) {
   unsigned short v;

@@ -406,7 +406,7 @@ struct FmtQ4KH {
   __device__ static void sums(const Raw& r, const uint8_t* xh_unit, const int (&xo)[NT],
                               const uint8_t* s2_unit, const int (&so)[NT], int lane,
                               float (&ps)[NT][4], float (&mnv)[NT][4], float (&d)[2], float (&dmin)[2]) {
-    const int g = lane >> 2, q = lane & 3;
+    const int q = lane & 3;
     const uint32_t kMagic = 0x64006400u;   // fp16 1024 in both halves
     uint32_t sa[2], nsa[2], sb16[2], nsb64[2], ma[2], mb[2];
     // Thread q needs sub-blocks j = 2q and 2q+1. For j < 4 (q < 2): sc = scales[j] & 63,
@@ -461,7 +461,6 @@ struct FmtQ4KH {
       }
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
-        const int tok = 8 * t + g;
         // chunk i = k/2 holds MMAs 2i, 2i+1 of the low half; chunk 4 + k/2 of the high half
         const uint8_t* base = xh_unit + xo[t];
         const uint4 xlo = *reinterpret_cast<const uint4*>(base + 64 * (k >> 1));
@@ -477,7 +476,6 @@ struct FmtQ4KH {
     const uint32_t a2[4] = {ma[0], ma[1], mb[0], mb[1]};
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-      const int tok = 8 * t + g;
       const uint2 b2 = *reinterpret_cast<const uint2*>(s2_unit + so[t]);
       const float z[4] = {0.f, 0.f, 0.f, 0.f};
       mma_f16_16816(mnv[t], a2, b2.x, b2.y, z);
@@ -565,7 +563,7 @@ struct FmtQ5KH {
   __device__ static void sums(const Raw& r, const uint8_t* xh_unit, const int (&xo)[NT],
                               const uint8_t* s2_unit, const int (&so)[NT], int lane,
                               float (&ps)[NT][4], float (&mnv)[NT][4], float (&d)[2], float (&dmin)[2]) {
-    const int g = lane >> 2, q = lane & 3;
+    const int q = lane & 3;
     const uint32_t kMagic = 0x64006400u;   // fp16 1024 in both halves
     uint32_t sa[2], nsa[2], sb16[2], nsb64[2], ma[2], mb[2];
     // Thread q needs sub-blocks j = 2q and 2q+1. For j < 4 (q < 2): sc = scales[j] & 63,
@@ -625,7 +623,6 @@ struct FmtQ5KH {
       }
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
-        const int tok = 8 * t + g;
         // chunk i = k/2 holds MMAs 2i, 2i+1 of the low half; chunk 4 + k/2 of the high half
         const uint8_t* base = xh_unit + xo[t];
         const uint4 xlo = *reinterpret_cast<const uint4*>(base + 64 * (k >> 1));
@@ -641,7 +638,6 @@ struct FmtQ5KH {
     const uint32_t a2[4] = {ma[0], ma[1], mb[0], mb[1]};
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-      const int tok = 8 * t + g;
       const uint2 b2 = *reinterpret_cast<const uint2*>(s2_unit + so[t]);
       const float z[4] = {0.f, 0.f, 0.f, 0.f};
       mma_f16_16816(mnv[t], a2, b2.x, b2.y, z);
@@ -739,8 +735,7 @@ struct FmtQ6KH {
   template <int NT>
   __device__ static void compute(const Raw& r, float (&acc)[NT][4], const uint8_t* xh_unit, const int (&xo)[NT],
                                  const uint8_t* /*s2_unit*/, const int (&/*so*/)[NT], const float* iv_unit,
-                                 const int (&io)[NT], int lane) {
-    const int q = lane & 3;
+                                 const int (&io)[NT], int /*lane*/) {
     float u[NT][4];
 #pragma unroll
     for (int t = 0; t < NT; ++t) u[t][0] = u[t][1] = u[t][2] = u[t][3] = 0.f;

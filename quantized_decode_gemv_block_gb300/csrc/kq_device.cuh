@@ -153,8 +153,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-// 1-D bulk copy global -> shared, completion counted in bytes on `bar`. dst, src and
-// bytes must be multiples of 16.
 // 2-D tensor (TMA) copy global -> shared of the box at element coordinates (x, y) of the
 // tensor map, completion counted in bytes on `bar`. x * element size must be a multiple
 // of 16 bytes; y may run past the tensor (those rows arrive as zeros).
@@ -164,6 +162,8 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, 
       ::"r"(smem_addr(dst)), "l"(tmap), "r"(x), "r"(y), "r"(smem_addr(bar))
       : "memory");
 }
+// 1-D bulk copy global -> shared, completion counted in bytes on `bar`. dst, src and
+// bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(

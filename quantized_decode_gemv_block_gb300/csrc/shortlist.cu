@@ -61,29 +61,6 @@ __device__ __forceinline__ float from_ordered_bits(uint32_t o) {
   return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
 }
 
-// 32 consecutive activations (a 64- or 128-byte aligned group, in global or shared memory).
-__device__ __forceinline__ void load_x32(const float* x, float (&v)[32]) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float4 u = *reinterpret_cast<const float4*>(x + 4 * i);
-    v[4 * i] = u.x;
-    v[4 * i + 1] = u.y;
-    v[4 * i + 2] = u.z;
-    v[4 * i + 3] = u.w;
-  }
-}
-__device__ __forceinline__ void load_x32(const uint16_t* x, float (&v)[32]) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 u = *reinterpret_cast<const uint4*>(x + 8 * i);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      v[8 * i + 2 * e] = __uint_as_float(w[e] << 16);
-      v[8 * i + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
-    }
-  }
-}
 
 // ||x_j||_2 rounded up for every token (every product, sum and the square root rounded
 // toward +inf), in the same fixed order in every CTA: thread t sums its 16-byte chunks
