@@ -680,6 +680,92 @@ struct FmtQ5KH {
 };
 
 
+// ------------------------------------------------------- Q8_0, fp16 path --
+// The Q8_0 unit (eight 34-byte blocks) against fp16 activations under the staging's exact
+// per-(token, super-block) 2^e (shared with FmtQ4KH): an int8 pair becomes an exact fp16 pair
+// with one LOP3 and one subtraction. LOP3 with table 0x6A computes mask ? (v ^ c) : c; with
+// mask = the low byte of each half and c = 0x6480 per half it keeps bits 0..6 of the code,
+// flips bit 7 (q + 128 as an unsigned byte) and puts fp16 1024 above them: 1024 + 128 + q,
+// and subtracting 1152 leaves q (integers below 2048 are exact in fp16). Thread q takes codes
+// 8q..8q+7 of every block, the pairs (0, 2) and (1, 3) of each four as FmtQ8_0 does, so the
+// staged x of each block is in natural chunk order (the staging's pair packing gives 0213).
+__device__ __forceinline__ uint32_t i8pair_h(uint32_t v) {  // bytes 0 and 2 -> fp16 pair, exact
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(v), "r"(0x00FF00FFu), "r"(0x64806480u));
+  return h2_sub(d, 0x64806480u);
+}
+
+struct FmtQ8_0H {
+  static constexpr bool kHalfX = true;
+  static constexpr bool kRowCopies = false;
+  static constexpr int kXq = 16;  // bytes between threads q of a token's staged super-block
+  static constexpr int kUnitBytes = 272;
+  using Raw = FmtQ8_0::Raw;
+  template <class Ld>
+  __device__ static void load(Raw& r, const uint8_t* pa, const uint8_t* pb, int q) {
+    FmtQ8_0::load<Ld>(r, pa, pb, q);
+  }
+  // Byte offset, within a token's 512-byte super-block slot, of the staged 16-byte chunk
+  // holding values 32j + 8v .. +7: block j, thread v.
+  __device__ static int stage_chunk(int j, int v) { return 64 * j + 16 * v; }
+
+  template <int NT>
+  __device__ static void compute(const Raw& r, float (&acc)[NT][4], const uint8_t* xh_unit, const int (&xo)[NT],
+                                 const uint8_t* /*s2_unit*/, const int (&/*so*/)[NT], const float* iv_unit,
+                                 const int (&io)[NT], int lane) {
+    const int quad = lane & ~3;
+    float u[NT][4];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) u[t][0] = u[t][1] = u[t][2] = u[t][3] = 0.f;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+#pragma unroll
+      for (int odd = 0; odd < 2; ++odd) {
+        const int b = 2 * p + odd;
+        uint32_t a0[4], a1[4];
+        float dsc[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          uint32_t c0, c1;
+          if (!odd) {
+            c0 = prmt(r.w[i][p][0], r.w[i][p][1], 0x5432u);
+            c1 = prmt(r.w[i][p][1], r.w[i][p][2], 0x5432u);
+          } else {
+            c0 = r.w[i][p][3];
+            c1 = r.w[i][p][4];
+          }
+          const uint32_t dw = __shfl_sync(0xFFFFFFFFu, odd ? r.w[i][p][2] : r.w[i][p][0], quad | (odd ? 3 : 0));
+          dsc[i] = half_bits_to_float(odd ? (dw >> 16) : dw);
+          a0[i] = i8pair_h(c0);
+          a0[i + 2] = i8pair_h(c0 >> 8);
+          a1[i] = i8pair_h(c1);
+          a1[i + 2] = i8pair_h(c1 >> 8);
+        }
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const uint4 xb = *reinterpret_cast<const uint4*>(xh_unit + xo[t] + 64 * b);
+          const float z[4] = {0.f, 0.f, 0.f, 0.f};
+          float pr[4];
+          mma_f16_16816(pr, a0, xb.x, xb.y, z);
+          mma_f16_16816(pr, a1, xb.z, xb.w, pr);
+          u[t][0] = __fmaf_rn(dsc[0], pr[0], u[t][0]);
+          u[t][1] = __fmaf_rn(dsc[0], pr[1], u[t][1]);
+          u[t][2] = __fmaf_rn(dsc[1], pr[2], u[t][2]);
+          u[t][3] = __fmaf_rn(dsc[1], pr[3], u[t][3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const float2 iv = lds_f2(iv_unit + io[t]);
+      acc[t][0] = __fmaf_rn(u[t][0], iv.x, acc[t][0]);
+      acc[t][1] = __fmaf_rn(u[t][1], iv.y, acc[t][1]);
+      acc[t][2] = __fmaf_rn(u[t][2], iv.x, acc[t][2]);
+      acc[t][3] = __fmaf_rn(u[t][3], iv.y, acc[t][3]);
+    }
+  }
+};
+
 // ------------------------------------------------------- Q6_K, fp16 path --
 // One unit = one 210-byte super-block: ql[128], qh[64], int8 scales[16], fp16 d. Weight w:
 // half n = w / 128, quarter kq = (w % 128) / 32, l = w % 32; code q = (ql[64n + 32(kq % 2) + l]

@@ -635,7 +635,7 @@ bool tma_layout(int fmt, const TmaPlan& pl, int M, TmaParams* prm, size_t* smem)
   auto al = [](size_t v) { return (v + 127) & ~size_t(127); };
   const int T = M > 8 ? 16 : 8;
   const int ub = unit_bytes_of(fmt);
-  const bool half_x = fmt == FMT_Q4_K || fmt == FMT_Q5_K || fmt == FMT_Q6_K;
+  const bool half_x = fmt == FMT_Q4_K || fmt == FMT_Q5_K || fmt == FMT_Q6_K || fmt == FMT_Q8_0;
   const bool row_copies = fmt == FMT_Q6_K;
   const int smax = (pl.units + pl.C - 1) / pl.C;
   int xstride = 0, xts = 0, s2ts = 0;
@@ -664,7 +664,7 @@ bool tma_layout(int fmt, const TmaPlan& pl, int M, TmaParams* prm, size_t* smem)
   const size_t off_ring = off;
   for (int su = stage_units_of(fmt); su >= 1; --su) {
     int stride = row_copies ? (su * ub + 30 + 15) / 16 * 16 : su * ub;  // + the span's alignment slack
-    if (half_x) {  // quad loads of 16 bytes at 16 + 32q: rows must differ by 16 mod 32 bytes
+    if (half_x && fmt != FMT_Q8_0) {  // quad loads of 16 bytes at 16 + 32q: rows must differ by 16 mod 32 bytes
       while (stride % 32 != 16) stride += 16;
     } else {       // 8-byte loads of 4 rows per phase: rows must differ by 32 or 96 mod 128
       while (stride % 128 != 32 && stride % 128 != 96) stride += 16;
@@ -706,7 +706,7 @@ int max_clusters(int fmt, int C, size_t smem) {
   if (fmt == FMT_Q4_K) fn = (const void*)gemv_tma_kernel<FmtQ4KH, 2>;
   else if (fmt == FMT_Q5_K) fn = (const void*)gemv_tma_kernel<FmtQ5KH, 2>;
   else if (fmt == FMT_Q6_K) fn = (const void*)gemv_tma_kernel<FmtQ6KH, 2>;
-  else if (fmt == FMT_Q8_0) fn = (const void*)gemv_tma_kernel<FmtQ8_0, 2>;
+  else if (fmt == FMT_Q8_0) fn = (const void*)gemv_tma_kernel<FmtQ8_0H, 2>;
   else fn = (const void*)gemv_tma_kernel<FmtAffine4, 2>;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemCap) != cudaSuccess)
     return 0;
@@ -882,8 +882,8 @@ int launch_gemv_mma(int fmt, const void* w, const void* x, float* y, int M, int 
         return two ? launch_tma<FmtQ4KH, 2>(tm, prm, smem, grid, stream, overlap, err)
                    : launch_tma<FmtQ4KH, 1>(tm, prm, smem, grid, stream, overlap, err);
       case FMT_Q8_0:
-        return two ? launch_tma<FmtQ8_0, 2>(tm, prm, smem, grid, stream, overlap, err)
-                   : launch_tma<FmtQ8_0, 1>(tm, prm, smem, grid, stream, overlap, err);
+        return two ? launch_tma<FmtQ8_0H, 2>(tm, prm, smem, grid, stream, overlap, err)
+                   : launch_tma<FmtQ8_0H, 1>(tm, prm, smem, grid, stream, overlap, err);
       case FMT_AFFINE4:
         return two ? launch_tma<FmtAffine4, 2>(tm, prm, smem, grid, stream, overlap, err)
                    : launch_tma<FmtAffine4, 1>(tm, prm, smem, grid, stream, overlap, err);
