@@ -103,6 +103,10 @@ int kq_device_errors(void);
  *             16-byte aligned for vector loads); K == 0 writes zeros
  * Row j of Y is bit-identical for every M and every position j (the kernel and its
  * work split are chosen from (fmt, x_dtype, N, K) only; M masks loads and stores).
+ * Memory: w_blocks must be device memory (the weights are read by tensor copies); x and y
+ * may be device memory or pinned host memory that the device can address (cudaHostAlloc /
+ * cudaMallocHost under unified addressing): the kernels then read x and write y there over
+ * the host link, with the same results, and need no copy before or after the call.
  * Errors: KQ_ERR_ARG, KQ_ERR_UNSUPPORTED, KQ_ERR_CUDA. */
 int kq_gemv(int fmt, const void* w_blocks, int x_dtype, const void* x, float* y, int M, int N,
             int K, void* stream);

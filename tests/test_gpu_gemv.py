@@ -258,3 +258,21 @@ def test_overlap_flag_gives_identical_results_in_a_chain(kq, orc):
     for y in ys:
         assert np.array_equal(y.cpu().numpy().view(np.uint32), plain[0].view(np.uint32))
     assert kq.device_errors() == 0
+
+
+@pytest.mark.parametrize("fmt", ["q4_k", "q8_0", "q6_k"])
+def test_pinned_host_buffers(kq, orc, fmt):
+    """x in and y out in pinned host memory (device-addressable under unified addressing): the
+    kernels read and write them directly, with the same bits as device buffers."""
+    f = FMTS[fmt]
+    N, K, M = 700, 3072, 3
+    blocks = orc.quantize(f, inputs.weights(N, K, seed=31, tensor_id=f))
+    wd = dev(blocks)
+    x = make_x(M, K, "bf16", seed=31)
+    xd = x_tensor(x, "bf16")
+    ref = kq.gemv(fmt, wd, xd, N, K)
+    xh = xd.cpu().pin_memory()
+    yh = torch.full((M, N), 7.0, dtype=torch.float32).pin_memory()
+    kq.gemv(fmt, wd, xh, N, K, y=yh)
+    torch.cuda.synchronize()
+    assert np.array_equal(yh.numpy().view(np.uint32), ref.cpu().numpy().view(np.uint32))
