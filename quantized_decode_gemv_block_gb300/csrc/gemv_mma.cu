@@ -260,6 +260,7 @@ int launch_chunked(const Params& prm, size_t smem, cudaStream_t stream, std::str
 constexpr int kMaxSliceUnits = 10;     // K-units of activations a CTA stages
 constexpr int kAuxScaleBytes = kMaxSliceUnits * 16 * 4;  // 2^-e per (staged unit, token)
 constexpr int kMaxClusterTiles = 32;   // tiles per cluster when partials meet across CTAs
+constexpr int kMaxClusterSize = 8;     // K-split ranks per cluster (the plan tries 1, 2, 4, 8)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded waits give up after 2 s
 
 __device__ unsigned int g_device_errors = 0;  // bit 0: a bounded wait gave up
@@ -560,16 +561,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (p.C == 1) return;
 
-  // K-split across the cluster: add the ranks' tile results in rank order.
+  // K-split across the cluster: add the ranks' tile results in rank order. Every rank's
+  // value is loaded before the first addition, so the C remote reads are in flight together.
   cg::cluster_group cluster = cg::this_cluster();
-  __syncthreads();
-  cluster.sync();
+  cluster.sync();  // a cluster barrier: it also orders this CTA's own threads
+  const float* rsrc[kMaxClusterSize];
+#pragma unroll
+  for (int r = 0; r < kMaxClusterSize; ++r) rsrc[r] = r < p.C ? cluster.map_shared_rank(res, r) : res;
   const int total = nt * 16 * p.M;
   const int e0 = (int)((long long)rank * total / p.C), e1 = (int)((long long)(rank + 1) * total / p.C);
   for (int e = e0 + threadIdx.x; e < e1; e += kThreads) {
     const int tok = e % p.M, rt = e / p.M;  // rt = tile * 16 + row
+    const size_t off = (size_t)rt * T + tok;
+    float part[kMaxClusterSize];
+#pragma unroll
+    for (int r = 0; r < kMaxClusterSize; ++r) part[r] = r < p.C ? rsrc[r][off] : 0.f;
     float v = 0.f;
-    for (int r = 0; r < p.C; ++r) v += cluster.map_shared_rank(res, r)[(size_t)rt * T + tok];
+#pragma unroll
+    for (int r = 0; r < kMaxClusterSize; ++r)
+      if (r < p.C) v += part[r];
     put(t0 * 16 + rt, tok, v);
   }
   cluster.sync();
@@ -755,7 +765,7 @@ TmaPlan plan_gemv_tma(int fmt, int N, int K, int num_sms) {
   best.ok = false;
   const int U = K / kUnit, tiles = (N + 15) / 16;
   long long best_work = -1;
-  for (int C = 1; C <= 8; C *= 2) {
+  for (int C = 1; C <= kMaxClusterSize; C *= 2) {
     if (C > U) break;
     const int smax = (U + C - 1) / C;
     if (smax > kMaxSliceUnits) continue;
