@@ -369,6 +369,47 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // high nibbles of word m-8): slots (2q, 2q+1) get the pair (+0, +2), slots (2q+8,
 // 2q+9) the pair (+1, +3). The staged x of each thread's 64 positions is permuted the
 // same way within groups of four, so B fragments are plain 16-byte loads.
+// Scales and mins of one K-quant super-block row (Q4_K and Q5_K share the 12-byte packing:
+// s0 = scales[0..3], s1 = scales[4..7], s2 = scales[8..11]) for thread q, which owns
+// sub-blocks a = 2q and b = 2q + 1. For j < 4: sc_j = scales[j] & 63, m_j = scales[j+4] & 63;
+// for j >= 4: sc_j = (scales[j+4] & 15) | (scales[j-4] >> 6) << 4 and
+// m_j = (scales[j+4] >> 4) | (scales[j] >> 6) << 4. Threads 0, 1 take the first form and
+// threads 2, 3 the second; both are one masked formula over the same two permutes, with
+// per-thread masks, so no lane computes a form it then discards.
+struct KqHeadConst {
+  uint32_t sel_p, sel_l, m_p, m_h, m_l, m_l4;
+};
+__device__ __forceinline__ KqHeadConst kq_head_const(int q) {
+  const uint32_t ja = static_cast<uint32_t>((2 * q) & 3);
+  KqHeadConst c;
+  c.sel_p = ja | ((ja + 1) << 4) | ((ja + 4) << 8) | ((ja + 5) << 12);  // s0.ja, s0.ja+1, s1.ja, s1.ja+1
+  c.sel_l = ja | ((ja + 1) << 4) | (ja << 8) | ((ja + 1) << 12);        // s2.ja, s2.ja+1, s2.ja, s2.ja+1
+  const bool lo_form = q < 2;
+  c.m_p = lo_form ? 0x3F3F3F3Fu : 0u;          // the 6-bit values themselves
+  c.m_h = lo_form ? 0u : 0x30303030u;          // bits 6, 7 of s0 / s1 bytes, as bits 4, 5
+  c.m_l = lo_form ? 0u : 0x00000F0Fu;          // sc: low nibble of the s2 byte
+  c.m_l4 = lo_form ? 0u : 0x0F0F0000u;         // m: high nibble of the s2 byte
+  return c;
+}
+// From the row's 16-byte header h (d | dmin, s0, s1, s2): sa = (sc_a, sc_a), nsa = -1024 sc_a,
+// sb16 = (sc_b / 16, sc_b / 16), nsb64 = -64 sc_b, mm = (m_a, m_b) as exact fp16 pairs, and
+// d, dmin in fp32. 1024 + v and 64 + v/16 (v < 64) are exact fp16 values, so each pair is one
+// permute (v under the exponent byte 0x64 or 0x54) and one subtraction.
+__device__ __forceinline__ void kq_head(const uint4& h, const KqHeadConst& c, uint32_t& sa, uint32_t& nsa,
+                                        uint32_t& sb16, uint32_t& nsb64, uint32_t& mm, float& d, float& dmin) {
+  const uint32_t P = prmt(h.y, h.z, c.sel_p);
+  const uint32_t L = prmt(h.w, h.w, c.sel_l);
+  // bytes (sc_a, sc_b, m_a, m_b)
+  const uint32_t v = (P & c.m_p) | ((P >> 2) & c.m_h) | (L & c.m_l) | ((L >> 4) & c.m_l4);
+  sa = h2_sub(prmt(v, 0x64646464u, 0x4040u), 0x64006400u);
+  nsa = h2_mul(sa, 0xE400E400u);
+  sb16 = h2_sub(prmt(v, 0x54545454u, 0x4141u), 0x54005400u);
+  nsb64 = h2_mul(sb16, 0xE400E400u);
+  mm = h2_sub(prmt(v, 0x64646464u, 0x4342u), 0x64006400u);
+  d = half_bits_to_float(h.x);
+  dmin = half_bits_to_float(h.x >> 16);
+}
+
 struct FmtQ4KH {
   static constexpr bool kHalfX = true;
   static constexpr bool kRowCopies = false;
@@ -406,46 +447,15 @@ struct FmtQ4KH {
   __device__ static void sums(const Raw& r, const uint8_t* xh_unit, const int (&xo)[NT],
                               const uint8_t* s2_unit, const int (&so)[NT], int lane,
                               float (&ps)[NT][4], float (&mnv)[NT][4], float (&d)[2], float (&dmin)[2]) {
-    const int q = lane & 3;
     const uint32_t kMagic = 0x64006400u;   // fp16 1024 in both halves
-    uint32_t sa[2], nsa[2], sb16[2], nsb64[2], ma[2], mb[2];
-    // Thread q needs sub-blocks j = 2q and 2q+1. For j < 4 (q < 2): sc = scales[j] & 63,
-    // m = scales[j+4] & 63. For j >= 4 (q >= 2): sc = (scales[j+4] & 15) | (scales[j-4] >> 6) << 4,
-    // m = (scales[j+4] >> 4) | (scales[j] >> 6) << 4. One permute gathers, per thread,
-    // bytes (sc_a, sc_b, m_a, m_b) of the low form and one the high-bit sources.
-    const uint32_t ja = static_cast<uint32_t>((2 * q) & 3);
-    // low form: q < 2 -> [s0.ja, s0.ja+1, s1.ja, s1.ja+1]; q >= 2 -> [s2.ja, s2.ja+1, s2.ja, s2.ja+1]
-    const uint32_t sel_lo = q < 2 ? (ja | ((ja + 1) << 4) | ((ja + 4) << 8) | ((ja + 5) << 12))
-                                  : (ja | ((ja + 1) << 4) | (ja << 8) | ((ja + 1) << 12));
-    // high bits (q >= 2): [s0.ja, s0.ja+1, s1.ja, s1.ja+1] >> 6 << 4
-    const uint32_t sel_hi = ja | ((ja + 1) << 4) | ((ja + 4) << 8) | ((ja + 5) << 12);
-    const uint32_t pa_sel = 0x4040u, pb_sel = 0x4141u, pma_sel = 0x4242u, pmb_sel = 0x4343u;
+    uint32_t sa[2], nsa[2], sb16[2], nsb64[2], mm[2];
+    const KqHeadConst hc = kq_head_const(lane & 3);
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const uint32_t s0 = r.h[i].y, s1 = r.h[i].z, s2 = r.h[i].w;
-      // bytes: sc_2q, sc_2q+1, m_2q, m_2q+1 (both forms computed, one selected: no branch)
-      const uint32_t v6 = prmt(s0, s1, sel_lo) & 0x3F3F3F3Fu;
-      const uint32_t lo = prmt(s2, s2, sel_lo);
-      const uint32_t hb = (prmt(s0, s1, sel_hi) >> 2) & 0x30303030u;
-      const uint32_t v4 = (((lo & 0x0000FFFFu) | ((lo >> 4) & 0x0F0F0000u)) & 0x0F0F0F0Fu) | hb;
-      const uint32_t v = q < 2 ? v6 : v4;
-      sa[i] = h2_sub(prmt(v, 0x64646464u, pa_sel), kMagic);               // (sc_2q, sc_2q)
-      nsa[i] = h2_mul(sa[i], 0xE400E400u);                                 // -1024 * sc_2q
-      const uint32_t sb = h2_sub(prmt(v, 0x64646464u, pb_sel), kMagic);   // sc_2q+1
-      sb16[i] = h2_mul(sb, 0x2C002C00u);                                   // sc_2q+1 / 16
-      nsb64[i] = h2_mul(sb, 0xD400D400u);                                  // -64 * sc_2q+1
-      ma[i] = h2_sub(prmt(v, 0x64646464u, pma_sel), kMagic);              // (m_2q, m_2q)
-      mb[i] = h2_sub(prmt(v, 0x64646464u, pmb_sel), kMagic);              // (m_2q+1, m_2q+1)
-      d[i] = half_bits_to_float(r.h[i].x);
-      dmin[i] = half_bits_to_float(r.h[i].x >> 16);
-    }
-    // four independent accumulation chains (word parity x low/high nibbles), added in a
-    // fixed order at the end: the MMAs of one super-block overlap instead of queueing
-    float p[NT][4][4];
-#pragma unroll
-    for (int t = 0; t < NT; ++t)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) p[t][c][0] = p[t][c][1] = p[t][c][2] = p[t][c][3] = 0.f;
+    for (int i = 0; i < 2; ++i) kq_head(r.h[i], hc, sa[i], nsa[i], sb16[i], nsb64[i], mm[i], d[i], dmin[i]);
+    // two accumulation chains (low and high nibbles), added at the end; the first MMA of
+    // each starts from zero
+    float p[NT][2][4];
+    const float z0[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int k = 0; k < 8; ++k) {  // code word k: MMA k (low nibbles) and MMA 8+k (high nibbles)
       uint32_t alo[4], ahi[4];
@@ -467,20 +477,24 @@ struct FmtQ4KH {
         const uint4 xhi = *reinterpret_cast<const uint4*>(base + 64 * (4 + (k >> 1)));
         const uint32_t bl0 = (k & 1) ? xlo.z : xlo.x, bl1 = (k & 1) ? xlo.w : xlo.y;
         const uint32_t bh0 = (k & 1) ? xhi.z : xhi.x, bh1 = (k & 1) ? xhi.w : xhi.y;
-        const int c = 2 * (k & 1);
-        mma_f16_16816(p[t][c], alo, bl0, bl1, p[t][c]);
-        mma_f16_16816(p[t][c + 1], ahi, bh0, bh1, p[t][c + 1]);
+        if (k == 0) {
+          mma_f16_16816(p[t][0], alo, bl0, bl1, z0);
+          mma_f16_16816(p[t][1], ahi, bh0, bh1, z0);
+        } else {
+          mma_f16_16816(p[t][0], alo, bl0, bl1, p[t][0]);
+          mma_f16_16816(p[t][1], ahi, bh0, bh1, p[t][1]);
+        }
       }
     }
-    // min term: A2 slots (2q, 2q+1) = m_2q, (2q+8, 2q+9) = m_2q+1; B2 = S/64 hi/lo parts
-    const uint32_t a2[4] = {ma[0], ma[1], mb[0], mb[1]};
+    // min term: A2 slots (2q, 2q+1) and (2q+8, 2q+9) both = (m_2q, m_2q+1); B2 = the high
+    // parts (S_2q, S_2q+1)/64, then the low parts
+    const uint32_t a2[4] = {mm[0], mm[1], mm[0], mm[1]};
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const uint2 b2 = *reinterpret_cast<const uint2*>(s2_unit + so[t]);
-      const float z[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_f16_16816(mnv[t], a2, b2.x, b2.y, z);
+      mma_f16_16816(mnv[t], a2, b2.x, b2.y, z0);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) ps[t][e] = (p[t][0][e] + p[t][1][e]) + (p[t][2][e] + p[t][3][e]);
+      for (int e = 0; e < 4; ++e) ps[t][e] = p[t][0][e] + p[t][1][e];
     }
   }
 
@@ -565,44 +579,14 @@ struct FmtQ5KH {
                               float (&ps)[NT][4], float (&mnv)[NT][4], float (&d)[2], float (&dmin)[2]) {
     const int q = lane & 3;
     const uint32_t kMagic = 0x64006400u;   // fp16 1024 in both halves
-    uint32_t sa[2], nsa[2], sb16[2], nsb64[2], ma[2], mb[2];
-    // Thread q needs sub-blocks j = 2q and 2q+1. For j < 4 (q < 2): sc = scales[j] & 63,
-    // m = scales[j+4] & 63. For j >= 4 (q >= 2): sc = (scales[j+4] & 15) | (scales[j-4] >> 6) << 4,
-    // m = (scales[j+4] >> 4) | (scales[j] >> 6) << 4. One permute gathers, per thread,
-    // bytes (sc_a, sc_b, m_a, m_b) of the low form and one the high-bit sources.
-    const uint32_t ja = static_cast<uint32_t>((2 * q) & 3);
-    // low form: q < 2 -> [s0.ja, s0.ja+1, s1.ja, s1.ja+1]; q >= 2 -> [s2.ja, s2.ja+1, s2.ja, s2.ja+1]
-    const uint32_t sel_lo = q < 2 ? (ja | ((ja + 1) << 4) | ((ja + 4) << 8) | ((ja + 5) << 12))
-                                  : (ja | ((ja + 1) << 4) | (ja << 8) | ((ja + 1) << 12));
-    // high bits (q >= 2): [s0.ja, s0.ja+1, s1.ja, s1.ja+1] >> 6 << 4
-    const uint32_t sel_hi = ja | ((ja + 1) << 4) | ((ja + 4) << 8) | ((ja + 5) << 12);
-    const uint32_t pa_sel = 0x4040u, pb_sel = 0x4141u, pma_sel = 0x4242u, pmb_sel = 0x4343u;
+    uint32_t sa[2], nsa[2], sb16[2], nsb64[2], mm[2];
+    const KqHeadConst hc = kq_head_const(lane & 3);
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const uint32_t s0 = r.h[i].y, s1 = r.h[i].z, s2 = r.h[i].w;
-      // bytes: sc_2q, sc_2q+1, m_2q, m_2q+1 (both forms computed, one selected: no branch)
-      const uint32_t v6 = prmt(s0, s1, sel_lo) & 0x3F3F3F3Fu;
-      const uint32_t lo = prmt(s2, s2, sel_lo);
-      const uint32_t hb = (prmt(s0, s1, sel_hi) >> 2) & 0x30303030u;
-      const uint32_t v4 = (((lo & 0x0000FFFFu) | ((lo >> 4) & 0x0F0F0000u)) & 0x0F0F0F0Fu) | hb;
-      const uint32_t v = q < 2 ? v6 : v4;
-      sa[i] = h2_sub(prmt(v, 0x64646464u, pa_sel), kMagic);               // (sc_2q, sc_2q)
-      nsa[i] = h2_mul(sa[i], 0xE400E400u);                                 // -1024 * sc_2q
-      const uint32_t sb = h2_sub(prmt(v, 0x64646464u, pb_sel), kMagic);   // sc_2q+1
-      sb16[i] = h2_mul(sb, 0x2C002C00u);                                   // sc_2q+1 / 16
-      nsb64[i] = h2_mul(sb, 0xD400D400u);                                  // -64 * sc_2q+1
-      ma[i] = h2_sub(prmt(v, 0x64646464u, pma_sel), kMagic);              // (m_2q, m_2q)
-      mb[i] = h2_sub(prmt(v, 0x64646464u, pmb_sel), kMagic);              // (m_2q+1, m_2q+1)
-      d[i] = half_bits_to_float(r.h[i].x);
-      dmin[i] = half_bits_to_float(r.h[i].x >> 16);
-    }
-    // four independent accumulation chains (word parity x low/high nibbles), added in a
-    // fixed order at the end: the MMAs of one super-block overlap instead of queueing
-    float p[NT][4][4];
-#pragma unroll
-    for (int t = 0; t < NT; ++t)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) p[t][c][0] = p[t][c][1] = p[t][c][2] = p[t][c][3] = 0.f;
+    for (int i = 0; i < 2; ++i) kq_head(r.h[i], hc, sa[i], nsa[i], sb16[i], nsb64[i], mm[i], d[i], dmin[i]);
+    // two accumulation chains (low and high nibbles), added at the end; the first MMA of
+    // each starts from zero
+    float p[NT][2][4];
+    const float z0[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int k = 0; k < 8; ++k) {  // code word k: MMA k (low nibbles) and MMA 8+k (high nibbles)
       uint32_t alo[4], ahi[4];
@@ -629,20 +613,24 @@ struct FmtQ5KH {
         const uint4 xhi = *reinterpret_cast<const uint4*>(base + 64 * (4 + (k >> 1)));
         const uint32_t bl0 = (k & 1) ? xlo.z : xlo.x, bl1 = (k & 1) ? xlo.w : xlo.y;
         const uint32_t bh0 = (k & 1) ? xhi.z : xhi.x, bh1 = (k & 1) ? xhi.w : xhi.y;
-        const int c = 2 * (k & 1);
-        mma_f16_16816(p[t][c], alo, bl0, bl1, p[t][c]);
-        mma_f16_16816(p[t][c + 1], ahi, bh0, bh1, p[t][c + 1]);
+        if (k == 0) {
+          mma_f16_16816(p[t][0], alo, bl0, bl1, z0);
+          mma_f16_16816(p[t][1], ahi, bh0, bh1, z0);
+        } else {
+          mma_f16_16816(p[t][0], alo, bl0, bl1, p[t][0]);
+          mma_f16_16816(p[t][1], ahi, bh0, bh1, p[t][1]);
+        }
       }
     }
-    // min term: A2 slots (2q, 2q+1) = m_2q, (2q+8, 2q+9) = m_2q+1; B2 = S/64 hi/lo parts
-    const uint32_t a2[4] = {ma[0], ma[1], mb[0], mb[1]};
+    // min term: A2 slots (2q, 2q+1) and (2q+8, 2q+9) both = (m_2q, m_2q+1); B2 = the high
+    // parts (S_2q, S_2q+1)/64, then the low parts
+    const uint32_t a2[4] = {mm[0], mm[1], mm[0], mm[1]};
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const uint2 b2 = *reinterpret_cast<const uint2*>(s2_unit + so[t]);
-      const float z[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_f16_16816(mnv[t], a2, b2.x, b2.y, z);
+      mma_f16_16816(mnv[t], a2, b2.x, b2.y, z0);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) ps[t][e] = (p[t][0][e] + p[t][1][e]) + (p[t][2][e] + p[t][3][e]);
+      for (int e = 0; e < 4; ++e) ps[t][e] = p[t][0][e] + p[t][1][e];
     }
   }
 
@@ -989,7 +977,9 @@ struct StageQ4KH {
         const float hs = ((a[0] + a[1]) + (a[2] + a[3])) * 0.015625f;  // S / 64
         const uint32_t hh = f2_to_h2(hs, 0.f) & 0xFFFFu;
         const uint32_t hl = f2_to_h2(hs - h_lo_to_f(hh), 0.f) & 0xFFFFu;
-        *reinterpret_cast<uint32_t*>(s2 + tok * s2ts + ul * 32 + 8 * q + 4 * half) = hh | (hl << 16);
+        uint16_t* s2h = reinterpret_cast<uint16_t*>(s2 + tok * s2ts + ul * 32 + 8 * q);
+        s2h[half] = static_cast<uint16_t>(hh);      // (S_2q, S_2q+1) / 64, high parts
+        s2h[2 + half] = static_cast<uint16_t>(hl);  // then the low parts
       }
     }
   }
