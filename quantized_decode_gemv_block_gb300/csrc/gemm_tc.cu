@@ -309,6 +309,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtlRegs));
    if (warp == kTmaWarp) {
     if (lane == 0) {
+      // the token tiles and the min-term tiles are the pre-pass's output (the weights' raw
+      // super-blocks and their unpacking are not, so those roles start at once)
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       int it = 0;
       bool stop = false;
       for (int tile = pair; tile < p.tiles && !stop; tile += npairs) {
@@ -459,6 +462,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     }
   } else {  // warps 0..7: epilogue
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the tokens' 2^-e_j are the pre-pass's
     const int quarter = warp & 3, half = warp >> 2;
     int grp = 0;
     bool stop = false;
@@ -539,6 +543,8 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(const uint16_t* __res
                                                            float* __restrict__ inv_scale, const uint8_t* __restrict__ w,
                                                            __half* __restrict__ wext, int M, int N, int K, int kc_x,
                                                            int k_ext, long long row_bytes) {
+  // the GEMM that follows may launch now: it waits for this grid before it reads what it wrote
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int G = K / 32;
   if ((int)blockIdx.x < M) {
     __shared__ unsigned int smax;
@@ -546,8 +552,23 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(const uint16_t* __res
     if (threadIdx.x == 0) smax = 0u;
     __syncthreads();
     const uint16_t* xr = x + (long long)tok * K;
+    // the first kKeep chunks of each thread stay in registers for the conversion pass (every
+    // row up to K = 8192 is read once); the rest, if any, are read again there
+    constexpr int kKeep = 4;
+    uint4 keep[kKeep];
+#pragma unroll
+    for (int r = 0; r < kKeep; ++r) {
+      const int c = threadIdx.x + 256 * r;
+      keep[r] = c < nch ? ldg128(xr + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
+    }
     unsigned int best = 0u;
-    for (int c = threadIdx.x; c < nch; c += 256) {
+#pragma unroll
+    for (int r = 0; r < kKeep; ++r) {
+      const uint32_t wv[4] = {keep[r].x, keep[r].y, keep[r].z, keep[r].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) best = max(best, max((wv[i] & 0x7FFFu) << 16, wv[i] & 0x7FFF0000u));
+    }
+    for (int c = threadIdx.x + 256 * kKeep; c < nch; c += 256) {
       const uint4 v = ldg128(xr + 8 * c);
       const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -568,7 +589,14 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(const uint16_t* __res
       const int c = base + threadIdx.x;
       float s = 0.f;
       if (c < nch) {
-        const uint4 v = ldg128(xr + 8 * c);
+        uint4 v;
+        if (base < 256 * kKeep) {
+#pragma unroll
+          for (int r = 0; r < kKeep; ++r)
+            if (base == 256 * r) v = keep[r];
+        } else {
+          v = ldg128(xr + 8 * c);
+        }
         const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
         uint32_t o[4];
 #pragma unroll
@@ -779,8 +807,20 @@ int launch_gemm_tc(const void* w, const void* x, float* y, int M, int N, int K, 
   prm.m_tiles = (int)m_tiles;
   prm.tiles = (int)(m_tiles * n_tiles);
   const int pairs = (int)std::min<long long>(prm.tiles, max_pairs(num_sms));
-  gemm_q4k_tc_kernel<<<2 * pairs, kTcThreads, kTcSmem, stream>>>(xmap, emap, wmap, prm);
-  e = cudaGetLastError();
+  // programmatic dependent launch: the CTAs start (tensor memory, barriers, the weights' raw
+  // copies and their unpacking) while the pre-pass drains; the copies of its output wait for it
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = kTcSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, gemm_q4k_tc_kernel, xmap, emap, wmap, prm);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) { *err = std::string("gemm launch: ") + cudaGetErrorString(e); return -1; }
   return 0;
 }
