@@ -404,8 +404,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_chunk_kernel(const AttnP
 
 // out[i][hq][d] = sum_c e_c o_c[d] / sum_c e_c l_c, e_c = exp(m_c - max_c m_c); zeros when
 // the token sees no position. One CTA per (row, kv head) of kCombGroups x HD threads: group
-// g adds the chunks c = g (mod kCombGroups) in index order (eight chunks' loads in flight at
-// once; the first eight leave with the loads of the chunks' maxima), then the groups' sums
+// g adds the chunks c = g (mod kCombGroups) in index order (the first kPre chunks' loads leave
+// with the loads of the chunks' maxima, later ones go eight at a time), then the groups' sums
 // are added in group order. The chunks' (m, l) pass through
 // shared memory. Chunks are added in index order, and their number, ceil((L + M) / 128),
 // depends on L + M; a chunk holding no position the token may see has m = -inf, so its
@@ -415,6 +415,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_chunk_kernel(const AttnP
 // enters the P V product with P = 0, and 0 * Inf is NaN).
 constexpr int kMaxChunks = 1024;
 constexpr int kCombGroups = 4;
+constexpr int kPre = 12;  // chunks per group whose partials load before the maxima are known
 template <int HD>
 __global__ void __launch_bounds__(HD * kCombGroups) attn_combine_kernel(const AttnParams p) {
   constexpr int PW = HD + 2, NT = HD * kCombGroups;
@@ -427,11 +428,12 @@ __global__ void __launch_bounds__(HD * kCombGroups) attn_combine_kernel(const At
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const float* base = p.part + (long long)kvh * p.nchunks * p.R * PW + (long long)r * PW;
   const long long cs = (long long)p.R * PW;
-  // the partials of this thread's first eight chunks: their loads do not depend on the
-  // maxima, so they leave with the (m, l) loads instead of one round trip later
-  float ov0[8];
+  // the partials of this thread's first kPre chunks: their loads do not depend on the
+  // maxima, so they leave with the (m, l) loads instead of one round trip later (every chunk
+  // of a context up to kPre * kCombGroups * 128 positions)
+  float ov0[kPre];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
+  for (int j = 0; j < kPre; ++j) {
     const int cc = grp + j * kCombGroups;
     ov0[j] = cc < p.nchunks ? base[cc * cs + d] : 0.f;
   }
@@ -451,38 +453,30 @@ __global__ void __launch_bounds__(HD * kCombGroups) attn_combine_kernel(const At
   for (int w = 1; w < NT / 32; ++w) mt = fmaxf(mt, sm_red[w]);  // a maximum: exact in any order
   for (int c = t; c < p.nchunks; c += NT) sm_m[c] = (mt == -INFINITY || sm_m[c] == -INFINITY) ? 0.f : expf(sm_m[c] - mt);
   __syncthreads();
-  // chunks grp, grp + 4, ... in index order, one FMA each (the first eight from ov0)
+  // chunks grp, grp + 4, ... in index order, one FMA each (the first kPre from ov0)
   float num = 0.f, den = 0.f;
-  int c = grp;
-  if (c + 7 * kCombGroups < p.nchunks) {
+#pragma unroll
+  for (int j = 0; j < kPre; ++j) {
+    const int cc = grp + j * kCombGroups;
+    if (cc < p.nchunks) {
+      num = __fmaf_rn(sm_m[cc], ov0[j], num);
+      den = __fmaf_rn(sm_m[cc], sm_l[cc], den);
+    }
+  }
+  int c = grp + kPre * kCombGroups;
+  for (; c + 7 * kCombGroups < p.nchunks; c += 8 * kCombGroups) {
+    float ov[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ov[j] = base[(c + j * kCombGroups) * cs + d];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      num = __fmaf_rn(sm_m[c + j * kCombGroups], ov0[j], num);
+      num = __fmaf_rn(sm_m[c + j * kCombGroups], ov[j], num);
       den = __fmaf_rn(sm_m[c + j * kCombGroups], sm_l[c + j * kCombGroups], den);
     }
-    c += 8 * kCombGroups;
-    for (; c + 7 * kCombGroups < p.nchunks; c += 8 * kCombGroups) {
-      float ov[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) ov[j] = base[(c + j * kCombGroups) * cs + d];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        num = __fmaf_rn(sm_m[c + j * kCombGroups], ov[j], num);
-        den = __fmaf_rn(sm_m[c + j * kCombGroups], sm_l[c + j * kCombGroups], den);
-      }
-    }
-    for (; c < p.nchunks; c += kCombGroups) {
-      num = __fmaf_rn(sm_m[c], base[c * cs + d], num);
-      den = __fmaf_rn(sm_m[c], sm_l[c], den);
-    }
-  } else {  // at most eight chunks for this group: all prefetched
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (c + j * kCombGroups < p.nchunks) {
-        num = __fmaf_rn(sm_m[c + j * kCombGroups], ov0[j], num);
-        den = __fmaf_rn(sm_m[c + j * kCombGroups], sm_l[c + j * kCombGroups], den);
-      }
-    }
+  }
+  for (; c < p.nchunks; c += kCombGroups) {
+    num = __fmaf_rn(sm_m[c], base[c * cs + d], num);
+    den = __fmaf_rn(sm_m[c], sm_l[c], den);
   }
   sm_num[grp][d] = num;
   if (d == 0) sm_den[grp] = den;
