@@ -138,6 +138,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_chunk_kernel(const AttnP
   float* red_l = red_m + NW * kAttnMaxRows;                          // [NW][128]: per-warp row sums
   // the combine kernel may be launched now; it waits for this grid before reading anything
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // when this grid was itself launched early (programmatic dependent launch), wait for the
+  // previous one before the first read or write (a no-op otherwise)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int c = blockIdx.x, kvh = blockIdx.y;
   const int pos0 = c * kChunk;
   const int npos = min(kChunk, p.L + p.M - pos0);
@@ -499,7 +502,7 @@ __global__ void __launch_bounds__(HD * kCombGroups) attn_combine_kernel(const At
 int attn_chunks(int L, int M) { return (L + M + kChunk - 1) / kChunk; }
 
 template <int HD>
-int launch_attn(const AttnParams& prm, cudaStream_t s, std::string* err) {
+int launch_attn(const AttnParams& prm, cudaStream_t s, bool early, std::string* err) {
   constexpr int LD = HD + 8, PLD = kChunk + 8;
   const size_t smem = (size_t)(kAttnMaxRows + 2 * kChunk) * LD * 2 + (size_t)2 * kAttnMaxRows * PLD * 2 +
                       (size_t)2 * (kAttnThreads / 32) * kAttnMaxRows * 4;
@@ -514,8 +517,22 @@ int launch_attn(const AttnParams& prm, cudaStream_t s, std::string* err) {
     }
     attr_done[dev] = true;
   }
-  attn_chunk_kernel<HD><<<dim3(prm.nchunks, prm.n_kv), kAttnThreads, smem, s>>>(prm);
-  cudaError_t e = cudaGetLastError();
+  // early: the chunk kernel may start (shared-memory carve-up, its launch) while the previous
+  // kernel in the stream finishes; it waits for it before touching memory
+  cudaError_t e;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(prm.nchunks, prm.n_kv, 1);
+    cfg.blockDim = dim3(kAttnThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = early ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, attn_chunk_kernel<HD>, prm);
+  }
   if (e == cudaSuccess) {  // the combine starts while the chunks run and waits for them
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(prm.R, prm.n_kv, 1);
@@ -545,7 +562,7 @@ size_t attention_workspace(int M, int L, int n_q, int n_kv, int hd) {
 
 int launch_attention(const float* q, int q_stride, const uint16_t* k, const uint16_t* v, float* o, uint16_t* o16,
                      int M, int L, int n_q, int n_kv, int hd, const uint32_t* mask, float scale, void* ws,
-                     cudaStream_t s, std::string* err) {
+                     cudaStream_t s, bool early, std::string* err) {
   AttnParams prm;
   prm.q = q;
   prm.q_stride = q_stride;
@@ -563,8 +580,8 @@ int launch_attention(const float* q, int q_stride, const uint16_t* k, const uint
   prm.R = prm.group * M;
   prm.nchunks = attn_chunks(L, M);
   prm.scale = scale;
-  if (hd == 128) return launch_attn<128>(prm, s, err);
-  if (hd == 64) return launch_attn<64>(prm, s, err);
+  if (hd == 128) return launch_attn<128>(prm, s, early, err);
+  if (hd == 64) return launch_attn<64>(prm, s, early, err);
   *err = "head_dim must be 64 or 128";
   return -1;
 }

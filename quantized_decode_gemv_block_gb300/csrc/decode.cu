@@ -410,9 +410,10 @@ int decode_step_attn(const kq_decode_model* m, const kq_kv_cache* c, const uint1
                       m->q_dim, m->kv_dim, c->length),
            "kv_append"))
       return -1;
-    // attention over the cache; its output goes to the Wo GEMV's input as bf16
+    // attention over the cache; its output goes to the Wo GEMV's input as bf16. A plain launch
+    // here: starting its CTAs early behind the small append kernel measured slower at M = 8
     if (launch_attention(w.qkv, qkv_dim, kc, vc, nullptr, w.x, M, c->length, n_q, n_kv, m->head_dim, mask, scale,
-                         aws, s, err))
+                         aws, s, false, err))
       return -1;
     if (gemv(m->layer_fmt, m->w_o[l], w.x, w.y, m->hidden, m->q_dim)) return -1;
     if (ck(launch_pdl(add_rmsnorm_kernel, M, s, true, w.h, (const uint16_t*)nullptr, (const float*)w.y, w.x,

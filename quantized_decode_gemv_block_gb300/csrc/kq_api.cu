@@ -290,7 +290,7 @@ int kq_attention(const float* q, const void* k_cache, const void* v_cache, float
   if (kq::launch_attention(q, n_q * head_dim, static_cast<const uint16_t*>(k_cache),
                            static_cast<const uint16_t*>(v_cache), o, nullptr, M, L, n_q, n_kv, head_dim,
                            reinterpret_cast<const uint32_t*>(mask), scale, workspace,
-                           static_cast<cudaStream_t>(stream), &err) != 0)
+                           static_cast<cudaStream_t>(stream), true, &err) != 0)
     return fail(KQ_ERR_CUDA, err);
   return ok();
 }

@@ -90,9 +90,11 @@ size_t decode_trace_size(const kq_decode_model* m, int M);
 // Decode attention of a verify window over a KV cache (attention.cu).
 size_t attention_workspace(int M, int L, int n_q, int n_kv, int hd);
 // q rows q_stride elements apart; the output goes to o (fp32) and/or o16 (bf16), either may be null.
+// early: launch the first kernel as a programmatic dependent of the previous one in the stream
+// (it waits for it before its first memory access).
 int launch_attention(const float* q, int q_stride, const uint16_t* k, const uint16_t* v, float* o, uint16_t* o16,
                      int M, int L, int n_q, int n_kv, int hd, const uint32_t* mask, float scale, void* ws,
-                     cudaStream_t s, std::string* err);
+                     cudaStream_t s, bool early, std::string* err);
 
 // Shortlist output head (shortlist.cu; the small copy's build is in quantize.cu).
 size_t shortlist_small_bytes(int N, int K);
