@@ -459,18 +459,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   bool ok = true;
   int lc = l0, stage = 0, ctl = w_first, cul = l0 - w_first * S;
+  int slot = 0;            // stage % depth and the parity of stage / depth, kept as counters
+  uint32_t parity = 0u;
+  const size_t stage_stride = (size_t)16 * p.row_stride;
+  const uint8_t* ring_g = myring + (size_t)g * p.row_stride;
   while (lc < l1) {
     const int tl = ctl, ul = cul;
     const int nu = min(p.su, min(l1 - lc, S - ul));
-    const int slot = stage % p.depth;
-    const uint32_t parity = static_cast<uint32_t>(stage / p.depth) & 1u;
     if (ok && !mbar_wait_bounded(&mybar[slot], parity, kWaitLimitNs)) {
       ok = false;
       if (lane == 0) atomicOr(&g_device_errors, 1u);
     }
     ok = __all_sync(0xFFFFFFFFu, ok);  // the warp's MMAs and copies need every lane
     if (ok) {
-      const uint8_t* sa = myring + ((size_t)slot * 16 + g) * p.row_stride;
+      const uint8_t* sa = ring_g + (size_t)slot * stage_stride;
       const uint8_t* sb = sa + (size_t)8 * p.row_stride;
       if constexpr (F::kRowCopies) {  // where each row's copy put the stage's first unit
         const uint32_t u0 = static_cast<uint32_t>(k0 + ul) * F::kUnitBytes;
@@ -515,6 +517,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && lp < l1) {
       fence_proxy_async_smem();
       issue(slot);
+    }
+    if (++slot == p.depth) {
+      slot = 0;
+      parity ^= 1u;
     }
   }
   if (!ok) {  // let this warp's copies in flight land before the CTA can exit
