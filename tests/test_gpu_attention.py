@@ -49,9 +49,11 @@ def check(o, ref, base, what):
 
 
 # (M, L, n_q, n_kv, head_dim): one token and no context; a partial chunk; exactly one chunk;
-# one past a chunk; head_dim 64; 128 query rows (4 heads x 32 tokens); many chunks; no GQA
+# one past a chunk; head_dim 64; 128 query rows (4 heads x 32 tokens); many chunks; no GQA;
+# 94 chunks (the combine's groups then go past its prefetched chunks into both later loops)
 SHAPES = [(1, 0, 16, 4, 128), (1, 1, 16, 4, 128), (4, 63, 16, 4, 128), (8, 64, 16, 4, 128),
-          (16, 65, 8, 2, 64), (32, 200, 8, 2, 128), (5, 1000, 16, 4, 128), (32, 4096, 4, 4, 128)]
+          (16, 65, 8, 2, 64), (32, 200, 8, 2, 128), (5, 1000, 16, 4, 128), (32, 4096, 4, 4, 128),
+          (3, 12000, 16, 4, 128)]
 
 
 @pytest.mark.parametrize("M,L,n_q,n_kv,hd", SHAPES)
@@ -93,7 +95,7 @@ def test_a_tokens_output_is_the_same_for_every_window_size(built):
         assert np.array_equal(o.view(np.uint32), full[:M].view(np.uint32)), f"M={M}"
 
 
-@pytest.mark.parametrize("M,L,hd", [(8, 300, 128), (5, 125, 64), (3, 0, 128), (4, 128, 128)])
+@pytest.mark.parametrize("M,L,hd", [(8, 300, 128), (5, 125, 64), (3, 0, 128), (4, 128, 128), (3, 12000, 128)])
 def test_window_equals_one_token_at_a_time(built, M, L, hd):
     """Token i of a window over L cached positions equals token i alone over L + i cached
     positions (the window's earlier rows now part of the cache), bit for bit."""
