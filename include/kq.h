@@ -116,7 +116,8 @@ enum kq_flags {
   /* The kernel launched just before this call on `stream` does not write w_blocks (for
    * example the previous layer's GEMV). The GEMV may then start streaming its weights
    * before that kernel finishes (programmatic dependent launch); it still waits for it
-   * before reading x or writing y. Only the tensor-core path (KQ_BF16) uses it. */
+   * before reading x or writing y. Both the tensor-core path (KQ_BF16) and the CUDA-core
+   * path (KQ_F32) use it; the latter loads its first 256-weight unit before the wait. */
   KQ_OVERLAP_PREVIOUS = 1u
 };
 

@@ -174,6 +174,10 @@ __global__ void __launch_bounds__(kThreadsF) gemv_f32_kernel(const uint8_t* __re
                                                              int K, long long row_bytes) {
   constexpr int kGroups = 8 / KS;  // row pairs per CTA
   __shared__ float red[KS > 1 ? 8 * kRowsPerWarp * MT : 1];
+  // Programmatic dependent launch (when the launch allows it): a following launch may begin
+  // now; this one loads its first unit's weights before it waits for the previous grid, and
+  // reads x and writes y only after that wait (a no-op for a plain launch).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gi = lane >> 2, q = lane & 3;
   const int rg = warp / KS, ks = warp - rg * KS;
@@ -199,6 +203,7 @@ __global__ void __launch_bounds__(kThreadsF) gemv_f32_kernel(const uint8_t* __re
       for (int i = 0; i < kRowsPerWarp; ++i)
         q6_load_raw(nxt[i], w + min(nbase + i, N - 1) * row_bytes + (long long)u0 * 210, ql_off, qh_off, s_off);
     }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int u = u0; u < u1; ++u) {
       Q6Raw cur[kRowsPerWarp];
 #pragma unroll
@@ -247,6 +252,7 @@ __global__ void __launch_bounds__(kThreadsF) gemv_f32_kernel(const uint8_t* __re
       decode_slice<FMT>(w + row * row_bytes + (long long)u * unit_bytes<FMT>(), gi, q, c[i], sc[i],
                         off[i]);
     }
+    if (u == u0) asm volatile("griddepcontrol.wait;" ::: "memory");
 #pragma unroll
     for (int j = 0; j < MT; ++j) {
       if (j < M) {
@@ -267,6 +273,7 @@ __global__ void __launch_bounds__(kThreadsF) gemv_f32_kernel(const uint8_t* __re
     }
   }
   }
+  if (u0 >= u1) asm volatile("griddepcontrol.wait;" ::: "memory");  // a warp with no units still stores
 #pragma unroll
   for (int i = 0; i < kRowsPerWarp; ++i) {
 #pragma unroll
@@ -293,16 +300,30 @@ __global__ void __launch_bounds__(kThreadsF) gemv_f32_kernel(const uint8_t* __re
   }
 }
 
+template <int FMT, int MT, class XT, int KS>
+void launch_one(const uint8_t* w, const XT* x, float* y, int M, int N, int K, long long row_bytes,
+                cudaStream_t s, bool overlap) {
+  const int rows = (8 / KS) * kRowsPerWarp;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((N + rows - 1) / rows, 1, 1);
+  cfg.blockDim = dim3(kThreadsF, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap ? 1 : 0;
+  cudaLaunchKernelEx(&cfg, gemv_f32_kernel<FMT, MT, XT, KS>, w, x, y, M, N, K, row_bytes);
+}
+
 template <int FMT, class XT, int KS>
 void launch_ks(const uint8_t* w, const XT* x, float* y, int M, int N, int K, long long row_bytes,
-               cudaStream_t s) {
-  const int rows = (8 / KS) * kRowsPerWarp;
-  const dim3 grid((N + rows - 1) / rows), block(kThreadsF);
-  if (M <= 1) gemv_f32_kernel<FMT, 1, XT, KS><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
-  else if (M <= 2) gemv_f32_kernel<FMT, 2, XT, KS><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
-  else if (M <= 4) gemv_f32_kernel<FMT, 4, XT, KS><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
-  else if (M <= 8) gemv_f32_kernel<FMT, 8, XT, KS><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
-  else gemv_f32_kernel<FMT, 16, XT, KS><<<grid, block, 0, s>>>(w, x, y, M, N, K, row_bytes);
+               cudaStream_t s, bool overlap) {
+  if (M <= 1) launch_one<FMT, 1, XT, KS>(w, x, y, M, N, K, row_bytes, s, overlap);
+  else if (M <= 2) launch_one<FMT, 2, XT, KS>(w, x, y, M, N, K, row_bytes, s, overlap);
+  else if (M <= 4) launch_one<FMT, 4, XT, KS>(w, x, y, M, N, K, row_bytes, s, overlap);
+  else if (M <= 8) launch_one<FMT, 8, XT, KS>(w, x, y, M, N, K, row_bytes, s, overlap);
+  else launch_one<FMT, 16, XT, KS>(w, x, y, M, N, K, row_bytes, s, overlap);
 }
 
 // The K split: the smallest KS (1, 2, 4, 8) that gives at least eight CTAs per SM while every
@@ -327,12 +348,12 @@ int pick_ks(int N, int K) {
 
 template <int FMT, class XT>
 int launch_fmt(const uint8_t* w, const XT* x, float* y, int M, int N, int K,
-               long long row_bytes, cudaStream_t s) {
+               long long row_bytes, cudaStream_t s, bool overlap) {
   switch (pick_ks(N, K)) {
-    case 1: launch_ks<FMT, XT, 1>(w, x, y, M, N, K, row_bytes, s); break;
-    case 2: launch_ks<FMT, XT, 2>(w, x, y, M, N, K, row_bytes, s); break;
-    case 4: launch_ks<FMT, XT, 4>(w, x, y, M, N, K, row_bytes, s); break;
-    default: launch_ks<FMT, XT, 8>(w, x, y, M, N, K, row_bytes, s); break;
+    case 1: launch_ks<FMT, XT, 1>(w, x, y, M, N, K, row_bytes, s, overlap); break;
+    case 2: launch_ks<FMT, XT, 2>(w, x, y, M, N, K, row_bytes, s, overlap); break;
+    case 4: launch_ks<FMT, XT, 4>(w, x, y, M, N, K, row_bytes, s, overlap); break;
+    default: launch_ks<FMT, XT, 8>(w, x, y, M, N, K, row_bytes, s, overlap); break;
   }
   return 0;
 }
@@ -340,14 +361,14 @@ int launch_fmt(const uint8_t* w, const XT* x, float* y, int M, int N, int K,
 }  // namespace
 
 int launch_gemv_f32(int fmt, const void* w, const float* x, float* y, int M, int N, int K,
-                    long long row_bytes, cudaStream_t stream, std::string* err) {
+                    long long row_bytes, cudaStream_t stream, bool overlap, std::string* err) {
   const uint8_t* wb = static_cast<const uint8_t*>(w);
   switch (fmt) {
-    case FMT_Q4_K: launch_fmt<FMT_Q4_K>(wb, x, y, M, N, K, row_bytes, stream); break;
-    case FMT_Q8_0: launch_fmt<FMT_Q8_0>(wb, x, y, M, N, K, row_bytes, stream); break;
-    case FMT_AFFINE4: launch_fmt<FMT_AFFINE4>(wb, x, y, M, N, K, row_bytes, stream); break;
-    case FMT_Q5_K: launch_fmt<FMT_Q5_K>(wb, x, y, M, N, K, row_bytes, stream); break;
-    case FMT_Q6_K: launch_fmt<FMT_Q6_K>(wb, x, y, M, N, K, row_bytes, stream); break;
+    case FMT_Q4_K: launch_fmt<FMT_Q4_K>(wb, x, y, M, N, K, row_bytes, stream, overlap); break;
+    case FMT_Q8_0: launch_fmt<FMT_Q8_0>(wb, x, y, M, N, K, row_bytes, stream, overlap); break;
+    case FMT_AFFINE4: launch_fmt<FMT_AFFINE4>(wb, x, y, M, N, K, row_bytes, stream, overlap); break;
+    case FMT_Q5_K: launch_fmt<FMT_Q5_K>(wb, x, y, M, N, K, row_bytes, stream, overlap); break;
+    case FMT_Q6_K: launch_fmt<FMT_Q6_K>(wb, x, y, M, N, K, row_bytes, stream, overlap); break;
     default: *err = "unsupported format"; return -1;
   }
   const cudaError_t e = cudaGetLastError();
@@ -359,8 +380,8 @@ int launch_gemv_f32(int fmt, const void* w, const float* x, float* y, int M, int
 }
 
 int launch_gemv_q6k_bf16(const void* w, const uint16_t* x, float* y, int M, int N, int K, long long row_bytes,
-                         cudaStream_t stream, std::string* err) {
-  launch_fmt<FMT_Q6_K>(static_cast<const uint8_t*>(w), x, y, M, N, K, row_bytes, stream);
+                         cudaStream_t stream, bool overlap, std::string* err) {
+  launch_fmt<FMT_Q6_K>(static_cast<const uint8_t*>(w), x, y, M, N, K, row_bytes, stream, overlap);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     *err = std::string("gemv (Q6_K, bf16 x) launch: ") + cudaGetErrorString(e);

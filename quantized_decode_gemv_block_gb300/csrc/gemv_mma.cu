@@ -846,7 +846,7 @@ int launch_gemv_mma(int fmt, const void* w, const void* x, float* y, int M, int 
     // per-row copies round each row's span out to 16 bytes, which stays inside the weights
     // only if their total size is a multiple of 16; other shapes take the CUDA-core kernel
     if (!tp.ok || ((long long)N * row_bytes) % 16 != 0)
-      return launch_gemv_q6k_bf16(w, static_cast<const uint16_t*>(x), y, M, N, K, row_bytes, stream, err);
+      return launch_gemv_q6k_bf16(w, static_cast<const uint16_t*>(x), y, M, N, K, row_bytes, stream, overlap, err);
   }
   if (tp.ok && (enc || fmt == FMT_Q6_K)) {
     TmaParams prm;

@@ -88,7 +88,8 @@ int gemv_impl(int fmt, const void* w, int x_dtype, const void* x, float* y, int 
                             &err) != 0)
       return fail(KQ_ERR_CUDA, err);
   } else {
-    if (kq::launch_gemv_f32(fmt, w, static_cast<const float*>(x), y, M, N, K, row_bytes, s, &err) != 0)
+    if (kq::launch_gemv_f32(fmt, w, static_cast<const float*>(x), y, M, N, K, row_bytes, s,
+                            (flags & KQ_OVERLAP_PREVIOUS) != 0, &err) != 0)
       return fail(KQ_ERR_CUDA, err);
   }
   return ok();

@@ -62,11 +62,11 @@ int launch_gemv_mma(int fmt, const void* w, const void* x, float* y, int M, int 
 
 // Q6_K with bf16 activations, CUDA-core path (its rows are only 2-byte aligned).
 int launch_gemv_q6k_bf16(const void* w, const uint16_t* x, float* y, int M, int N, int K, long long row_bytes,
-                         cudaStream_t stream, std::string* err);
+                         cudaStream_t stream, bool overlap, std::string* err);
 
 // fp32 activations, CUDA-core path.
 int launch_gemv_f32(int fmt, const void* w, const float* x, float* y, int M, int N, int K,
-                    long long row_bytes, cudaStream_t stream, std::string* err);
+                    long long row_bytes, cudaStream_t stream, bool overlap, std::string* err);
 
 // Tensor-core prefill (gemm_tc.cu): Q4_K weights x bf16 activations, M > 16.
 size_t gemm_tc_workspace(int M, int N, int K);

@@ -260,6 +260,49 @@ def test_overlap_flag_gives_identical_results_in_a_chain(kq, orc):
     assert kq.device_errors() == 0
 
 
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_k", "q6_k"])
+def test_overlap_flag_on_the_fp32_path(kq, orc, fmt):
+    """KQ_OVERLAP_PREVIOUS on the CUDA-core (fp32 x) kernels: a chain where each GEMV reads
+    the previous one's output gives the same bits with and without the flag (eager and in a
+    CUDA graph), and the first link matches the oracle."""
+    f = FMTS[fmt]
+    dims = [1024, 2048, 512, 1024]
+    blocks = [orc.quantize(f, inputs.weights(dims[i + 1], dims[i], seed=60 + i, tensor_id=3))
+              for i in range(len(dims) - 1)]
+    wd = [dev(b) for b in blocks]
+    x0 = make_x(3, dims[0], "f32", seed=61)
+
+    def chain(overlap):
+        x = x_tensor(x0, "f32")
+        outs = []
+        for i, w in enumerate(wd):
+            y = kq.gemv(fmt, w, x, dims[i + 1], dims[i], overlap=overlap)
+            outs.append(y)
+            x = y
+        torch.cuda.synchronize()
+        return [o.cpu().numpy() for o in outs]
+
+    plain, over = chain(False), chain(True)
+    for a, b in zip(plain, over):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    yref, ay = orc.gemv(f, blocks[0], x0, dims[1], dims[0])
+    assert_close(over[0].astype(np.float64), yref, ay, f"{fmt} fp32 chain link 0")
+    x = x_tensor(x0, "f32")
+    ys = [torch.empty((3, dims[1]), device="cuda") for _ in range(6)]
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        kq.gemv(fmt, wd[0], x, dims[1], dims[0], y=ys[0], overlap=True)
+        s.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            for y in ys:
+                kq.gemv(fmt, wd[0], x, dims[1], dims[0], y=y, overlap=True)
+    g.replay()
+    torch.cuda.synchronize()
+    for y in ys:
+        assert np.array_equal(y.cpu().numpy().view(np.uint32), plain[0].view(np.uint32))
+
+
 @pytest.mark.parametrize("fmt", ["q4_k", "q8_0", "q6_k"])
 def test_pinned_host_buffers(kq, orc, fmt):
     """x in and y out in pinned host memory (device-addressable under unified addressing): the
