@@ -986,10 +986,10 @@ def run_decode(args, spec):
                        "tokens_per_s_equivalent": world * M / (ms_step * 1e-3),
                        "l2": f"weights per step {wbytes} B > 4x L2 ({l2} B): every step streams from HBM",
                        # per layer: qkv, o, gate|up, down GEMVs and two residual-add RMSNorms (the GQA
-                       # expand and the SwiGLU run in the GEMV epilogues at these shapes), plus the
-                       # kv append and the two attention kernels with a cache; then the first
-                       # RMSNorm and the head
-                       "launches_per_step": (9 if cache is not None else 6) * d["n_layers"] + 2,
+                       # expand, the SwiGLU and, with a cache, the kv append run in the GEMV
+                       # epilogues at these shapes), plus the two attention kernels with a cache;
+                       # then the first RMSNorm and the head
+                       "launches_per_step": (8 if cache is not None else 6) * d["n_layers"] + 2,
                        "kv_cache_bytes_per_step": kv_bytes,
                        "parallelism": "replicas" if world > 1 else "single gpu",
                        "pct_of_8tbs": value / world / 8000.0},
@@ -1001,7 +1001,7 @@ def run_decode(args, spec):
             "e2e": {"value": world * wbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": xh.numel() * 2, "d2h_bytes_per_step": lh.numel() * 4,
                     "note": "pinned-host x copied in, graph of kq_decode_step, logits copied out, every step"},
-            "gpu_launches": args.steps * ((9 if cache is not None else 6) * d["n_layers"] + 2),
+            "gpu_launches": args.steps * ((8 if cache is not None else 6) * d["n_layers"] + 2),
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

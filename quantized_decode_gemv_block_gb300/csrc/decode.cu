@@ -399,14 +399,25 @@ int decode_step_attn(const kq_decode_model* m, const kq_kv_cache* c, const uint1
   swiglu.kind = 2;
   swiglu.out = w.x2;
   const bool fuse_swiglu = gemv_epilogue_ok(m->layer_fmt, 2 * m->ffn, m->hidden, 2, num_sms);
+  // the window's k and v go into the cache from the qkv GEMV's stores (same bf16 rounding as the
+  // append kernel, which runs instead where the streaming kernel does not take the shape)
+  GemvEpilogue append;
+  append.kind = 3;
+  append.v0 = m->q_dim;
+  append.hd = m->kv_dim;
+  append.row0 = c->length;
+  const bool fuse_append = gemv_epilogue_ok(m->layer_fmt, qkv_dim, m->hidden, 3, num_sms);
   if (ck(launch_pdl(add_rmsnorm_kernel, M, s, false, w.h, x, (const float*)nullptr, w.x, m->hidden, m->rms_eps),
          "add_rmsnorm"))
     return -1;
   for (int l = 0; l < m->n_layers; ++l) {
     uint16_t* kc = static_cast<uint16_t*>(c->k[l]);
     uint16_t* vc = static_cast<uint16_t*>(c->v[l]);
-    if (gemv(m->layer_fmt, m->w_qkv[l], w.x, w.qkv, qkv_dim, m->hidden)) return -1;
-    if (ck(launch_pdl(kv_append_kernel, ew_grid((long long)M * m->kv_dim), s, true, (const float*)w.qkv, kc, vc, M,
+    append.out = kc;
+    append.out_b = vc;
+    if (gemv(m->layer_fmt, m->w_qkv[l], w.x, w.qkv, qkv_dim, m->hidden, fuse_append ? &append : nullptr)) return -1;
+    if (!fuse_append &&
+        ck(launch_pdl(kv_append_kernel, ew_grid((long long)M * m->kv_dim), s, true, (const float*)w.qkv, kc, vc, M,
                       m->q_dim, m->kv_dim, c->length),
            "kv_append"))
       return -1;

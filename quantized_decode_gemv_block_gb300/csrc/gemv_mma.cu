@@ -274,9 +274,12 @@ struct TmaParams {
   int off_ss, off_ring, off_bar, off_pb, off_res, off_aux;
   int xts, s2ts;  // fp16 path: row strides (bytes) of the staged x and min-term operands
   // epilogue (GemvEpilogue): 0 y only; 1 y plus the bf16 GQA copies of rows [e_v0, e_v0 + e_vn);
-  // 2 paired rows (tile t = gate rows 8t.. and up rows half + 8t..), out2 = bf16(silu(g) * u)
-  int epi, e_v0, e_vn, e_hd, e_group, e_w, half;
+  // 2 paired rows (tile t = gate rows 8t.. and up rows half + 8t..), out2 = bf16(silu(g) * u);
+  // 3 y plus bf16 rows [e_v0, e_v0 + e_hd) into out2 and [e_v0 + e_hd, e_v0 + 2 e_hd) into
+  // out3, row e_row0 + token of each (e_hd wide): a KV cache append
+  int epi, e_v0, e_vn, e_hd, e_group, e_w, half, e_row0;
   uint16_t* out2;
+  uint16_t* out3;
   // formats with per-row copies (F::kRowCopies): the weight rows, row_bytes apart
   const uint8_t* w;
   long long row_bytes;
@@ -411,6 +414,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint16_t b = f32_to_bf16_rn(v);
       uint16_t* o = p.out2 + (long long)tok * p.e_w + (long long)h * p.e_group * p.e_hd + d;
       for (int i = 0; i < p.e_group; ++i) o[i * p.e_hd] = b;
+    } else if (p.epi == 3 && n >= p.e_v0 && n < p.e_v0 + 2 * p.e_hd) {
+      const int c = n - p.e_v0;
+      const long long r = (long long)(p.e_row0 + tok) * p.e_hd;
+      if (c < p.e_hd) p.out2[r + c] = f32_to_bf16_rn(v);
+      else p.out3[r + c - p.e_hd] = f32_to_bf16_rn(v);
     }
   };
   // Epilogue 2: gate row i and up row half + i (paired in one tile) for token tok.
@@ -828,7 +836,7 @@ bool gemv_epilogue_ok(int fmt, int N, int K, int kind, int num_sms) {
   if (fmt != FMT_Q4_K && fmt != FMT_Q5_K && fmt != FMT_Q8_0 && fmt != FMT_AFFINE4) return false;
   const TmaPlan tp = plan_gemv_tma(fmt, N, K, num_sms);
   if (!tp.ok || !encode_tiled_fn()) return false;
-  return kind == 1 || (kind == 2 && tp.C == 1 && N % 16 == 0);
+  return kind == 1 || kind == 3 || (kind == 2 && tp.C == 1 && N % 16 == 0);
 }
 
 int launch_gemv_mma(int fmt, const void* w, const void* x, float* y, int M, int N, int K,
@@ -867,6 +875,8 @@ int launch_gemv_mma(int fmt, const void* w, const void* x, float* y, int M, int 
     prm.e_hd = epi ? epi->hd : 1;
     prm.e_group = epi ? epi->group : 1;
     prm.e_w = epi ? epi->out_w : 0;
+    prm.out3 = epi ? epi->out_b : nullptr;
+    prm.e_row0 = epi ? epi->row0 : 0;
     prm.half = N / 2;
     prm.w = static_cast<const uint8_t*>(w);
     prm.row_bytes = row_bytes;

@@ -43,11 +43,15 @@ size_t gemv_mma_smem(const GemvPlan& pl, int M);
 //         (out rows out_w wide): the attention stand-in's output feeding Wo;
 //  kind 2 (SwiGLU): W's rows pair up (row i is a gate row, row N/2 + i its up row; each 16-row tile
 //         takes 8 of each); out[tok][i] = bf16(silu(y_i) * y_(N/2+i)), rows N/2 wide; y is written
-//         only if not null.
+//         only if not null;
+//  kind 3 (KV append): y as usual, and rows [v0, v0 + hd) / [v0 + hd, v0 + 2 hd) also go as bf16
+//         to row row0 + tok of out / out_b (rows hd wide): the window's k and v into the cache.
 struct GemvEpilogue {
   int kind = 0;
   uint16_t* out = nullptr;
   int v0 = 0, vn = 0, hd = 1, group = 1, out_w = 0;
+  uint16_t* out_b = nullptr;  // kind 3: the second destination (v rows)
+  int row0 = 0;               // kind 3: the first destination row (tokens go to row0 + j)
 };
 // Whether the streaming kernel runs this shape with this epilogue kind (kind 2 needs a plan
 // without a K-split and N a multiple of 16).
