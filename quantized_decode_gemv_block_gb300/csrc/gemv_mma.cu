@@ -4,24 +4,18 @@
 // README, "What makes it fast": a decode step reads every weight once per token, a
 // speculative check runs all guesses through one pass over the weights).
 //
-// Layout of the work:
-//  * A CTA owns 128 consecutive rows of W (8 warps x 16 rows) and one K-slice.
-//    When N alone gives too few CTAs to keep the HBM busy, K is split across the
-//    CTAs of a thread-block cluster (2, 4 or 8); their partial sums meet in
-//    distributed shared memory and are added in rank order. The split depends on
-//    (N, K, SM count) only, never on M.
-//  * Each warp streams its 16 rows with 8- and 16-byte read-only loads, two
-//    256-weight units ahead, and dequantizes in registers to exact bf16 codes
-//    (4-bit codes and int8 codes are exact in bf16).
-//  * mma.sync m16n8k16 (bf16 in, fp32 accumulate) multiplies 16 weight rows by
-//    8 token columns per instruction; tokens 8..15 take a second column tile.
-//    The activations of the CTA's K-slice are staged once in shared memory, in
-//    the order the B fragments need, together with the per-32 sums of x used by
-//    the min/bias terms.
-//  * Per 32-weight group the fp32 MMA result is promoted by its scale with one
-//    FMA, and the min/bias term is added with a second FMA against the staged
-//    sum of x: acc += (d*sc)*P - (dmin*m)*S (Q4_K), acc += d*P (Q8_0),
-//    acc += s*P + b*S (affine4).
+// Two kernels, chosen by (format, N, K) only:
+//  * gemv_tma_kernel (the streaming kernel, section below): one CTA per SM; each warp
+//    streams its share of 16-row tiles through a private ring of shared-memory stages
+//    filled by tensor copies; the activations of the CTA's K-slice are staged once (the
+//    K-quant and Q8_0 formats as fp16 under an exact per-(token, super-block) power of two);
+//    mma.sync m16n8k16 multiplies 16 weight rows by 8 token columns (tokens 8..15 take a
+//    second column tile); K is split across a thread-block cluster when N alone gives too
+//    few tiles, the ranks' partials meeting in distributed shared memory in rank order.
+//  * gemv_chunked_kernel (K too long for the streaming kernel's staging): 128 rows per CTA,
+//    register-streamed 8- and 16-byte loads two units ahead, activations staged in chunks,
+//    K split over a cluster; per 32-group the fp32 MMA result is promoted by its scale and
+//    the min/bias term added against the staged sums of x.
 //
 // Batch invariance (Kinetic README, "What makes it fast", last paragraph: every row
 // of a batch is summed in the same order as that token alone): a token column's
